@@ -1,0 +1,470 @@
+"""Benchmark of the PQ2_0 ternary matmul hot path on GB300.
+
+One JSON line (rank 0).  A step is one pass of the hot path over one batch of
+synthetic input: for each of R distinct projections (distinct weight sets, so
+the step's weights exceed 4x L2 and come from HBM), quantise its fp16
+activations (pq2_quantize_act) and run its matmul (pq2_gemv for M = 1,
+pq2_gemm_small for M <= 16, pq2_gemm_prefill above).  The R projections are
+captured once in a CUDA graph and replayed; times are CUDA events on the
+replay stream.
+
+Workloads (--workload):
+  decode   M=1, K=6144 -> N=5120 (default; the o_proj-shaped decode GEMV)
+  pr1      M=1, K=1024 -> N=256
+  small    M=--m (2..16), --shape K,N (6144,5120 or 5120,17408)
+  mlp      M=--m (1 or 16): gate/up 5120 -> 34816, quantise the synthetic
+           intermediate h, down 17408 -> 5120
+  prefill  M=--m (128 or 4096), 5120 -> 17408
+
+--impl reference runs the CPU oracle (the method's plain definition) on the
+host cores on a bounded sample of the same workload, as the baseline arm.
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", HBM_FALLBACK_GBS), d.get("bf16_tflops", BF16_FALLBACK_TFLOPS), \
+            d.get("bf16_tflops_sustained", None), "measured"
+    return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, None, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+def gemm_bytes(M, N, K):
+    """Algorithmic bytes of one matmul call (each byte once): codes, weight
+    scales, quantised activations, S and T, fp32 output."""
+    G = K // 128
+    return N * K // 4 + 2 * N * G + M * K + 8 * M * G + 4 * M * N
+
+
+def quant_bytes(M, K):
+    return 2 * M * K + M * K + 8 * M * (K // 128)
+
+
+def workload_spec(args):
+    """-> (name, list of (M, K, N, code_dist, x_dist) per projection in a
+    layer, metric kind)"""
+    w = args.workload
+    if w == "decode":
+        return "decode_gemv_m1_k6144_n5120", [(1, 6144, 5120, "p343", "outliers")], "GB/s"
+    if w == "pr1":
+        return "pr1_gemv_m1_k1024_n256", [(1, 1024, 256, "uniform", "normal")], "GB/s"
+    if w == "small":
+        K, N = (int(v) for v in args.shape.split(","))
+        return f"small_m{args.m}_k{K}_n{N}", [(args.m, K, N, "p343", "outliers")], "GB/s"
+    if w == "mlp":
+        return f"mlp_pair_m{args.m}", [(args.m, 5120, 34816, "uniform", "normal"),
+                                       (args.m, 17408, 5120, "uniform", "normal")], "GB/s"
+    if w == "prefill":
+        return f"prefill_m{args.m}_k5120_n17408", [(args.m, 5120, 17408, "uniform", "normal")], \
+            "TOPS"
+    raise SystemExit(f"unknown workload {w}")
+
+
+def per_layer_units(layer, kind):
+    """Algorithmic bytes (GB/s workloads) or int8-equivalent ops (TOPS) of one
+    layer, and the dominant kernel's share."""
+    if kind == "TOPS":
+        return sum(2.0 * M * N * K for (M, K, N, _, _) in layer)
+    return float(sum(gemm_bytes(M, N, K) for (M, K, N, _, _) in layer))
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def build_layers(args, layer, R, device):
+    import torch
+    from gemm_pq2_ternary_gb300 import binding as pq2
+    from gemm_pq2_ternary_gb300 import inputs
+
+    layers = []
+    for r in range(R):
+        gen = torch.Generator(device=device)
+        gen.manual_seed(1000 + r)
+        projs = []
+        for (M, K, N, cdist, xdist) in layer:
+            tern = inputs.draw_ternary_torch(N, K, cdist, gen, device)
+            ws = inputs.draw_ws_torch(N, K, gen, device)
+            codes, ws_p = pq2.pack(tern, ws)
+            del tern
+            x = inputs.draw_x_torch(M, K, xdist, gen, device)
+            qp, S, T = pq2.alloc_act(M, K, device)
+            y = torch.empty((M, N), dtype=torch.float32, device=device)
+            op = pq2.PQ2_OP_GEMV if M == 1 else (pq2.PQ2_OP_SMALL if M <= 16 else pq2.PQ2_OP_PREFILL)
+            wsp = pq2.alloc_workspace(op, M, N, K, device)
+            mmws = pq2.alloc_workspace(pq2.PQ2_OP_MATMUL, M, N, K, device)
+            projs.append(dict(M=M, K=K, N=N, codes=codes, ws=ws_p, x=x, qp=qp, S=S, T=T, y=y,
+                              op=op, wsp=wsp, mmws=mmws))
+        layers.append(projs)
+    torch.cuda.synchronize()
+    return layers
+
+
+def run_matmul(pq2, p):
+    if p["op"] == pq2.PQ2_OP_GEMV:
+        pq2.pq2_gemv(p["qp"], p["S"], p["T"], p["codes"], p["ws"], p["y"])
+    elif p["op"] == pq2.PQ2_OP_SMALL:
+        pq2.pq2_gemm_small(p["qp"], p["S"], p["T"], p["codes"], p["ws"], p["y"], p["wsp"])
+    else:
+        pq2.pq2_gemm_prefill(p["qp"], p["S"], p["T"], p["codes"], p["ws"], p["y"], p["wsp"])
+
+
+def step_fn(pq2, layers, matmul_only=False):
+    def fn():
+        for projs in layers:
+            for p in projs:
+                if not matmul_only:
+                    pq2.pq2_quantize_act(p["x"], p["qp"], p["S"], p["T"])
+                run_matmul(pq2, p)
+    return fn
+
+
+def time_graph(torch, graph, steps, warmup, stream):
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
+def capture(torch, fn, stream):
+    fn()  # eager once (sets function attributes, warms caches)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def gpu_arm(args, rank, world, dist):
+    import torch
+    from gemm_pq2_ternary_gb300 import binding as pq2
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(device)
+    l2 = props.L2_cache_size
+    name, layer, kind = workload_spec(args)
+    layer_weight_bytes = sum(N * K // 4 + 2 * N * (K // 128) for (M, K, N, _, _) in layer)
+    R = args.projections or max(1, math.ceil(4 * l2 / layer_weight_bytes))
+    layers = build_layers(args, layer, R, device)
+
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        g_step = capture(torch, step_fn(pq2, layers), stream)
+        g_mm = capture(torch, step_fn(pq2, layers, matmul_only=True), stream)
+    assert pq2.pq2_last_device_error(stream) == pq2.PQ2_OK
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    for _ in range(args.warmup):
+        g_step.replay()
+    barrier()
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        g_step.replay()
+    t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms_step = t0.elapsed_time(t1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms_step], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # dominant kernel (the matmul) alone, same weight sets, for the roofline
+    ms_mm = time_graph(torch, g_mm, args.steps, args.warmup, stream)
+    mm_per_launch_ms = ms_mm / (R * len(layer))
+
+    units_layer = per_layer_units(layer, kind)
+    units_step = units_layer * R
+    scale = 1e-9 if kind == "GB/s" else 1e-12
+    value = units_step * world / (ms_step * 1e-3) * scale
+
+    hbm, bf16, bf16_sus, peak_src = load_peaks()
+    if kind == "GB/s":
+        per_launch = units_layer / len(layer)
+        achieved = per_launch / (mm_per_launch_ms * 1e-3) * 1e-9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": None,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
+    else:
+        per_launch = units_layer / len(layer)
+        achieved = per_launch / (mm_per_launch_ms * 1e-3) * 1e-12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
+                "frac": round(achieved / bf16, 4), "traffic": None,
+                "peak_source": f"{peak_src} bf16 burst; kind::f16 runs at the bf16 rate"}
+
+    # end to end through the public API, host buffers, copies inside the timing
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_arm(torch, pq2, layers, args, stream, kind, units_step, world, dist, device)
+
+    launches = args.steps * R * 2 * len(layer)
+    out = {
+        "metric": f"ternary matmul {kind} ({name})",
+        "value": round(value, 2), "unit": kind, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "i8",
+        "data": "synthetic (seeded; ternary codes, fp16 scales and activations drawn on device)",
+        "config": {"workload": name, "projections_per_step": R,
+                   "shapes": [{"M": M, "K": K, "N": N} for (M, K, N, _, _) in layer],
+                   "l2": f"inputs larger than L2: {R * layer_weight_bytes / 1e6:.0f} MB of weights "
+                         f"per step vs {l2 / 1e6:.0f} MB L2",
+                   "graph": "one CUDA graph per step, programmatic dependent launch",
+                   "arith": "int8 activations x 2-bit ternary codes, int32 group dots, fp32 sums",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "matmul_ms_per_launch": round(mm_per_launch_ms, 5),
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    return out, (name, layer, kind)
+
+
+def e2e_arm(torch, pq2, layers, args, stream, kind, units_step, world, dist, device):
+    """The same metric through pq2_matmul (the public call) with host
+    buffers: each step copies every projection's fp16 activations from pinned
+    host memory and reads every output back, inside the timed region."""
+    projs = [p for layer in layers for p in layer]
+    xs_h = [p["x"].cpu().pin_memory() for p in projs]
+    ys_h = [torch.empty_like(p["y"], device="cpu").pin_memory() for p in projs]
+    h2d = sum(x.numel() * x.element_size() for x in xs_h)
+    d2h = sum(y.numel() * y.element_size() for y in ys_h)
+
+    def one_step():
+        for p, xh, yh in zip(projs, xs_h, ys_h):
+            p["x"].copy_(xh, non_blocking=True)
+            pq2.pq2_matmul(p["x"], p["codes"], p["ws"], p["y"], p["mmws"])
+            yh.copy_(p["y"], non_blocking=True)
+
+    steps = max(1, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one_step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one_step()
+        torch.cuda.synchronize()
+        dt = (time.perf_counter() - t0) / steps
+    if dist is not None:
+        t = torch.tensor([dt], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt = float(t.item())
+    scale = 1e-9 if kind == "GB/s" else 1e-12
+    return {"value": round(units_step * world / dt * scale, 2), "unit": kind,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(dt * 1e3, 4), "timer": "host wall clock around synchronised steps"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline) arm
+# ---------------------------------------------------------------------------
+def oracle_sample(layer, kind, seconds):
+    """Time the oracle on a bounded sample: the first `rows` output rows of
+    each projection of one layer, drawn from the seeded host generator.
+    Returns (units per second, description, threads)."""
+    import oracle
+    from gemm_pq2_ternary_gb300 import inputs
+
+    probs = []
+    for i, (M, K, N, cdist, xdist) in enumerate(layer):
+        rows = min(N, 64)
+        p = inputs.Problem("sample", M, K, rows, cdist, xdist, 100 + i)
+        tern, ws, x = inputs.generate(p)
+        qp, S, T = oracle.quantize_act(x)
+        codes = oracle.pack(tern)
+        probs.append((M, K, rows, qp, S, codes, ws))
+
+    def run(rows_frac):
+        units = 0.0
+        t0 = time.perf_counter()
+        for (M, K, rows, qp, S, codes, ws) in probs:
+            r = max(1, int(rows * rows_frac))
+            oracle.matmul(qp, S, codes[:r], ws[:r])
+            units += (gemm_bytes(M, r, K) if kind == "GB/s" else 2.0 * M * r * K)
+        return units, time.perf_counter() - t0
+
+    u, dt = run(1.0)
+    reps = max(1, int(seconds / max(dt, 1e-6)))
+    t0 = time.perf_counter()
+    tot = 0.0
+    for _ in range(reps):
+        tot += run(1.0)[0]
+    dt = time.perf_counter() - t0
+    scale = 1e-9 if kind == "GB/s" else 1e-12
+    desc = (f"{reps} x first {[p[2] for p in probs]} output rows of the "
+            f"{[(p[0], p[1]) for p in probs]} (M,K) projections; all M tokens, all K")
+    return tot / dt * scale, desc, oracle.threads(), dt
+
+
+def reference_arm(args, rank, world):
+    name, layer, kind = workload_spec(args)
+    if rank != 0:
+        return None
+    vals = []
+    t_start = time.perf_counter()
+    for i in range(args.warmup + args.steps):
+        v, desc, threads, dt = oracle_sample(layer, kind, args.ref_step_seconds)
+        if i >= args.warmup:
+            vals.append((v, dt))
+    value = float(np.median([v for v, _ in vals]))
+    ms = float(np.mean([dt for _, dt in vals])) * 1e3
+    return {
+        "impl": "reference",
+        "metric": f"ternary matmul {kind} ({name})", "value": round(value, 6), "unit": kind,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i8",
+        "data": "synthetic (seeded host draws)",
+        "config": {"workload": name, "parallelism": "host cores, one process"},
+        "cpu_baseline": {"value": round(value, 6), "unit": kind, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": kind, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s": round(time.perf_counter() - t_start, 1),
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="pq2", choices=["pq2", "reference"])
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "pr1", "small", "mlp", "prefill"])
+    ap.add_argument("--m", type=int, default=16)
+    ap.add_argument("--shape", default="5120,17408")
+    ap.add_argument("--projections", type=int, default=0, help="weight sets per step (0: auto)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+
+    if args.impl == "reference":
+        out = reference_arm(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    out, (name, layer, kind) = gpu_arm(args, rank, world, dist)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            v, desc, threads, _ = oracle_sample(layer, kind, args.cpu_seconds)
+            out["cpu_baseline"] = {"value": round(v, 6), "unit": kind, "cores": threads,
+                                   "kind": "oracle", "sample": desc}
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

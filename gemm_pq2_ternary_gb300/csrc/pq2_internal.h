@@ -1,0 +1,32 @@
+// Host-side prototypes shared by the translation units of the library.
+// Every launcher validates nothing (pq2_api.cu does) and returns the CUDA
+// error of its launch.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "pq2_common.cuh"
+
+namespace pq2h {
+
+cudaError_t launch_quantize(const __half* x, int8_t* qp, float* S, int32_t* T, int64_t M,
+                            int64_t K, cudaStream_t st, const pq2::DevCtl& ctl,
+                            const DeviceInfo& dev);
+
+cudaError_t launch_pack(const int8_t* tern, uint8_t* codes, int64_t N, int64_t K,
+                        cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev);
+
+// M == 1.  dots != nullptr selects the integer-dot debug output instead of y.
+cudaError_t launch_gemv(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
+                        const __half* ws, float* y, int32_t* dots, int64_t N, int64_t K,
+                        cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev);
+
+// Plain warp-per-output kernel, any M (first correct path for M > 1).
+cudaError_t launch_simple(const int8_t* qp, const float* S, const int32_t* T,
+                          const uint8_t* codes, const __half* ws, float* y, int32_t* dots,
+                          int64_t M, int64_t N, int64_t K, cudaStream_t st,
+                          const pq2::DevCtl& ctl, const DeviceInfo& dev);
+
+}  // namespace pq2h

@@ -1,0 +1,218 @@
+/*
+ * pq2.h -- C ABI of the GB300 (sm_103a) PQ2_0 ternary-weight matmul library.
+ *
+ * The operation, as the pages define it:
+ *   [P1] "Making a ternary reasoning model fast in vLLM", page "From CUDA to
+ *        Triton and Gluon";
+ *   [P2] the same series, page "Chasing llama.cpp at batch one".
+ *
+ *   y[m,n] = sum_g (dot(codes[n,g], q[m,g]) - sum(q[m,g])) * S[m,g] * WS[n,g]
+ *
+ * Weights are 2-bit codes 0,1,2 standing for -1,0,+1, four to a byte, with
+ * one fp16 scale per 128 weights ([P1] "One token at a time": the PQ2_0 code
+ * and the per-group scale).  Activations are quantised to int8 per 128 values
+ * and stored in plane order, so the activation of weight 4*byte+s sits at
+ * position s*32+byte of its group; plane s of a 32-bit code word,
+ * (w >> 2s) & 0x03030303, then lines up with four consecutive activation
+ * bytes, and the -1 offset is one subtraction of sum(q) per group (same
+ * section).
+ *
+ * Notation and layouts (all row-major, all buffers owned by the caller):
+ *   M tokens, K inputs (K % 128 == 0), N outputs, G = K / 128.
+ *   x      fp16  [M, K]      activations
+ *   qp     int8  [M, K]      quantised activations, plane order: the value of
+ *                            natural index k is at g*128 + (k&3)*32 + ((k&127)>>2)
+ *   S      fp32  [M, G]      activation scale per group
+ *   T      int32 [M, G]      sum of the group's int8 values
+ *   codes  uint8 [N, K/4]    weight k of row n in byte n*K/4 + (k>>2), bits 2*(k&3)
+ *   WS     fp16  [N, G]      weight scale per group
+ *   y      fp32  [M, N]      output (fully overwritten, never accumulated into)
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers are device pointers unless stated, 16-byte aligned
+ *     (PQ2_ERR_MISALIGNED otherwise); sizes are element counts.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously on it; nothing here
+ *     synchronises, except pq2_last_device_error.
+ *   - The library allocates and frees no memory.  Scratch space, where an
+ *     operation needs it, is passed in as `workspace` / `workspace_bytes`
+ *     (size from pq2_workspace_bytes).
+ *   - Arguments are checked on the host before any launch; on error nothing
+ *     is enqueued and the status says why.  A failed launch returns
+ *     PQ2_ERR_CUDA.  Device faults surface at the caller's next
+ *     synchronisation, as for any CUDA call.
+ *   - Results are deterministic: the same inputs give bit-identical outputs
+ *     (fixed-order reductions, no atomics on data).
+ *   - NaN or Inf in x is not checked; the result is then undefined.
+ *   - Kernels wait on on-chip barriers with a bounded spin; a wait that runs
+ *     out sets a device error word that pq2_last_device_error reports as
+ *     PQ2_ERR_TIMEOUT.
+ */
+#ifndef PQ2_H
+#define PQ2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pq2_status {
+    PQ2_OK = 0,
+    PQ2_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad op  */
+    PQ2_ERR_UNSUPPORTED_SHAPE = 2, /* K % 128 != 0, M out of range, ...    */
+    PQ2_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned      */
+    PQ2_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed  */
+    PQ2_ERR_TIMEOUT = 5,           /* a kernel's bounded wait ran out       */
+    PQ2_ERR_WORKSPACE = 6          /* workspace missing or too small        */
+} pq2_status;
+
+/* Operation selectors for pq2_workspace_bytes and pq2_group_dots. */
+enum {
+    PQ2_OP_GEMV = 0,     /* pq2_gemv            (M == 1)            */
+    PQ2_OP_SMALL = 1,    /* pq2_gemm_small      (2 <= M <= 16)      */
+    PQ2_OP_PREFILL = 2,  /* pq2_gemm_prefill    (M >= 1)            */
+    PQ2_OP_MATMUL = 3    /* pq2_matmul          (M >= 1, from fp16) */
+};
+
+/* Largest K any entry point accepts (G <= 2048 groups). */
+#define PQ2_MAX_K 262144
+
+/* Static text for a status code; never NULL. */
+const char* pq2_status_string(int status);
+
+/* Library version string, e.g. "pq2-gb300 0.1 sm_103a". */
+const char* pq2_version(void);
+
+/*
+ * pq2_quantize_act -- fused activation quantisation and plane reorder.
+ *   [P1] "Prompt processing": the quantize kernel writes q [m,k] int8,
+ *   s [m,G] fp32 and t [m,G] int32 per 128-value group; [P1] "One token at
+ *   a time": q is stored in plane order.
+ * Per (m, g): amax = max |x|; d = amax / 127 (fp32, round to nearest even);
+ * q = round-half-even(x / d) clamped to [-127, 127]; S = d; T = sum q.  A
+ * group of zeros gives d = 0, q = 0, T = 0.  (The pages fix the outputs but
+ * not the scale formula; this is the plain symmetric reading.)
+ *   x_f16  in   fp16 [M, K]
+ *   qp     out  int8 [M, K] plane order
+ *   S, T   out  fp32 / int32 [M, G]
+ * M >= 0 (M == 0 enqueues nothing), 1 <= K <= PQ2_MAX_K, K % 128 == 0.
+ */
+pq2_status pq2_quantize_act(const void* x_f16, int64_t M, int64_t K,
+                            int8_t* qp, float* S, int32_t* T, void* stream);
+
+/*
+ * pq2_pack_weights -- the "prepared" weight planes: ternary values to codes.
+ *   [P1] "One token at a time": codes 0,1,2 for -1,0,+1, four to a byte,
+ *   weight 4*byte+s in bits 2s; [P1] "A power proxy for the rest of the
+ *   model": prepared weights carry the scales as a separate plane.
+ *   tern    in   int8 [N, K], every value in {-1, 0, +1}
+ *   ws_f16  in   fp16 [N, G]  (may be NULL together with ws_out)
+ *   codes   out  uint8 [N, K/4]
+ *   ws_out  out  fp16 [N, G]  copy of ws_f16 (may alias ws_f16)
+ * A value outside {-1,0,1} is stored as code 3 (read as +2 by the matmul
+ * kernels) and sets the device error word; the host cannot see it without a
+ * synchronisation, so validate ternary inputs before packing.
+ */
+pq2_status pq2_pack_weights(const int8_t* tern, const void* ws_f16, int64_t N, int64_t K,
+                            uint8_t* codes, void* ws_out, void* stream);
+
+/*
+ * pq2_gemv -- the M = 1 decode matmul y[n] for all n.
+ *   [P1] "One token at a time: plain Triton is enough" (plane extraction
+ *   with (w >> 2s) & 0x03030303 feeding DP4A, the per-group sum(q)
+ *   subtraction, fp32 accumulation of dot * s * ws); [P2] "The win: a program
+ *   just for one token" (no token dimension, separate scale plane).
+ *   qp [1,K], S [1,G], T [1,G], codes [N,K/4], ws_f16 [N,G] in; y [1,N] out.
+ * N >= 1, 128 <= K <= PQ2_MAX_K, K % 128 == 0.
+ */
+pq2_status pq2_gemv(const int8_t* qp, const float* S, const int32_t* T,
+                    const uint8_t* codes, const void* ws_f16, float* y,
+                    int64_t N, int64_t K, void* stream);
+
+/*
+ * pq2_gemm_small -- small batches, 2 <= M <= 16 token rows.
+ *   [P1] "Small batches: make the register layout explicit", "Use a ring
+ *   buffer for longer rows", "Extend the kernels to sixteen token rows";
+ *   split-K partial sums, where used, are reduced in the fixed order
+ *   0,1,2,... ([P1] "Choose the configuration with the proxy").
+ *   Same operands as pq2_gemv with M rows; y [M,N].
+ *   workspace: device scratch of pq2_workspace_bytes(PQ2_OP_SMALL, M, N, K)
+ *   bytes (may be NULL when that is 0).
+ */
+pq2_status pq2_gemm_small(const int8_t* qp, const float* S, const int32_t* T,
+                          const uint8_t* codes, const void* ws_f16, float* y,
+                          int64_t M, int64_t N, int64_t K,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pq2_gemm_prefill -- prompt processing, any M >= 1 (built for M > 16).
+ *   [P1] "Prompt processing: check configuration and launch costs" (2-D
+ *   output tiles, per-group integer products and the same per-group
+ *   dequantise-accumulate order as the M = 1 path).
+ *   Same operands as pq2_gemm_small; y [M,N].
+ *   workspace: pq2_workspace_bytes(PQ2_OP_PREFILL, M, N, K) bytes.
+ */
+pq2_status pq2_gemm_prefill(const int8_t* qp, const float* S, const int32_t* T,
+                            const uint8_t* codes, const void* ws_f16, float* y,
+                            int64_t M, int64_t N, int64_t K,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pq2_matmul -- the whole path from fp16 activations: pq2_quantize_act, then
+ * pq2_gemv (M == 1), pq2_gemm_small (M <= 16) or pq2_gemm_prefill.  The
+ * pages' routing by token count ([P1] "Defaults and switches").
+ *   x_f16 [M,K] fp16, codes, ws_f16 in; y [M,N] fp32 out.
+ *   workspace: pq2_workspace_bytes(PQ2_OP_MATMUL, M, N, K) bytes (holds the
+ *   quantised activations plus the chosen kernel's own scratch).
+ */
+pq2_status pq2_matmul(const void* x_f16, const uint8_t* codes, const void* ws_f16, float* y,
+                      int64_t M, int64_t N, int64_t K,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pq2_workspace_bytes -- scratch bytes `op` needs for this shape (0 if none,
+ * SIZE_MAX if the shape is not supported).
+ */
+size_t pq2_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
+
+/*
+ * pq2_group_dots -- debug view of the integer part of a kernel: the same
+ * kernel as `op` (PQ2_OP_GEMV, PQ2_OP_SMALL or PQ2_OP_PREFILL), writing the
+ * per-group ternary dots dot(codes,q) - sum(q) instead of y
+ * ([P1] "One token at a time": the -1 offset as one subtraction per group).
+ *   dots out int32 [M, N, G].  Other operands as for `op`; workspace as for
+ *   `op`.  For PQ2_OP_GEMV, M must be 1.
+ */
+pq2_status pq2_group_dots(int op, const int8_t* qp, const int32_t* T, const uint8_t* codes,
+                          int64_t M, int64_t N, int64_t K, int32_t* dots,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pq2_last_device_error -- synchronises `stream`, then reads and clears the
+ * current device's error word: PQ2_ERR_TIMEOUT if a kernel's bounded wait ran
+ * out, PQ2_ERR_INVALID_ARG if pq2_pack_weights met a non-ternary value,
+ * PQ2_OK otherwise (PQ2_ERR_CUDA if the synchronisation itself failed).
+ */
+pq2_status pq2_last_device_error(void* stream);
+
+/*
+ * pq2_debug_set_wait_limit_ns -- bound on every on-chip barrier wait, in
+ * nanoseconds (default 2e9).  For tests of the timeout path only.
+ */
+pq2_status pq2_debug_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * pq2_debug_skip_stage -- test hook: from now on, the producer of every
+ * bulk-copy pipeline withholds its stage number `stage` (never issues it), so
+ * the consumers' bounded wait runs out and the call reports PQ2_ERR_TIMEOUT
+ * through pq2_last_device_error.  -1 turns it off (the default).
+ */
+pq2_status pq2_debug_skip_stage(int stage);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PQ2_H */

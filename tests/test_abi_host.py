@@ -1,0 +1,120 @@
+"""CPU-only checks of the C ABI: the library loads, exports every function
+include/pq2.h declares, and rejects bad arguments on the host before any CUDA
+call (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pq2.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gemm_pq2_ternary_gb300 import _build
+    _build.build()
+    from gemm_pq2_ternary_gb300 import binding
+    return binding._lib
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pq2_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for want in ["pq2_quantize_act", "pq2_pack_weights", "pq2_gemv", "pq2_gemm_small",
+                 "pq2_gemm_prefill", "pq2_matmul", "pq2_workspace_bytes", "pq2_group_dots",
+                 "pq2_last_device_error", "pq2_status_string"]:
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from gemm_pq2_ternary_gb300 import binding
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in binding.SIGNATURES, name
+
+
+def test_version_and_status_strings(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    assert "sm_103a" in b.pq2_version()
+    for s in range(7):
+        assert b.pq2_status_string(s) not in ("", "unknown status")
+    assert b.pq2_status_string(99) == "unknown status"
+
+
+FAKE = 0x10000          # 16-byte aligned, never dereferenced
+ODD = 0x10008           # 8-byte aligned only
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def test_gemv_rejects_bad_arguments(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    ok = [_p(FAKE)] * 6
+    assert lib.pq2_gemv(*ok, 256, 100, None) == b.PQ2_ERR_UNSUPPORTED_SHAPE   # K % 128
+    assert lib.pq2_gemv(*ok, 0, 128, None) == b.PQ2_ERR_INVALID_ARG           # N < 1
+    assert lib.pq2_gemv(*ok, 1, 0, None) == b.PQ2_ERR_INVALID_ARG             # K < 1
+    assert lib.pq2_gemv(*ok, 1, 128 * 4096, None) == b.PQ2_ERR_UNSUPPORTED_SHAPE
+    bad = list(ok)
+    bad[3] = None
+    assert lib.pq2_gemv(*bad, 4, 128, None) == b.PQ2_ERR_INVALID_ARG          # codes null
+    bad = list(ok)
+    bad[5] = _p(ODD)
+    assert lib.pq2_gemv(*bad, 4, 128, None) == b.PQ2_ERR_MISALIGNED           # y misaligned
+
+
+def test_small_and_prefill_reject_bad_arguments(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    ok = [_p(FAKE)] * 6
+    for M in (1, 17, 0):
+        st = lib.pq2_gemm_small(*ok, M, 64, 128, None, 0, None)
+        assert st in (b.PQ2_ERR_UNSUPPORTED_SHAPE, b.PQ2_ERR_INVALID_ARG)
+    assert lib.pq2_gemm_prefill(*ok, 0, 64, 128, None, 0, None) == b.PQ2_ERR_INVALID_ARG
+    assert lib.pq2_gemm_prefill(*ok, 64, 64, 200, None, 0, None) == b.PQ2_ERR_UNSUPPORTED_SHAPE
+
+
+def test_workspace_query(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    assert b.pq2_workspace_bytes(b.PQ2_OP_GEMV, 1, 5120, 6144) == 0
+    assert b.pq2_workspace_bytes(b.PQ2_OP_GEMV, 2, 5120, 6144) == b.SIZE_MAX
+    assert b.pq2_workspace_bytes(b.PQ2_OP_SMALL, 17, 5120, 6144) == b.SIZE_MAX
+    assert b.pq2_workspace_bytes(b.PQ2_OP_SMALL, 4, 5120, 100) == b.SIZE_MAX
+    assert b.pq2_workspace_bytes(99, 4, 5120, 6144) == b.SIZE_MAX
+    mm = b.pq2_workspace_bytes(b.PQ2_OP_MATMUL, 4, 5120, 6144)
+    assert mm >= 4 * 6144 + 2 * 4 * 48 * 4
+
+
+def test_matmul_rejects_small_workspace(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    st = lib.pq2_matmul(_p(FAKE), _p(FAKE), _p(FAKE), _p(FAKE), 4, 64, 128, _p(FAKE), 16, None)
+    assert st == b.PQ2_ERR_WORKSPACE
+    st = lib.pq2_matmul(_p(FAKE), _p(FAKE), _p(FAKE), _p(FAKE), 4, 64, 128, None, 1 << 20, None)
+    assert st == b.PQ2_ERR_WORKSPACE
+
+
+def test_group_dots_rejects_bad_op(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    st = lib.pq2_group_dots(7, _p(FAKE), _p(FAKE), _p(FAKE), 1, 8, 128, _p(FAKE), None, 0, None)
+    assert st == b.PQ2_ERR_INVALID_ARG
+    st = lib.pq2_group_dots(b.PQ2_OP_GEMV, _p(FAKE), _p(FAKE), _p(FAKE), 3, 8, 128, _p(FAKE),
+                            None, 0, None)
+    assert st == b.PQ2_ERR_UNSUPPORTED_SHAPE
+
+
+def test_quantize_and_pack_reject_bad_arguments(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    P = _p(FAKE)
+    assert lib.pq2_quantize_act(P, 2, 130, P, P, P, None) == b.PQ2_ERR_UNSUPPORTED_SHAPE
+    assert lib.pq2_quantize_act(P, -1, 128, P, P, P, None) == b.PQ2_ERR_INVALID_ARG
+    assert lib.pq2_quantize_act(P, 0, 128, P, P, P, None) == b.PQ2_OK   # nothing to do
+    assert lib.pq2_quantize_act(P, 2, 128, _p(ODD), P, P, None) == b.PQ2_ERR_MISALIGNED
+    assert lib.pq2_pack_weights(P, P, 4, 96, P, P, None) == b.PQ2_ERR_UNSUPPORTED_SHAPE
+    assert lib.pq2_pack_weights(P, P, 4, 128, P, None, None) == b.PQ2_ERR_INVALID_ARG
