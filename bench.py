@@ -106,7 +106,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -150,31 +150,36 @@ class ClockSampler:
 # GPU arm
 # ---------------------------------------------------------------------------
 def build_layers(args, layer, R, device):
+    """R layers of distinct weight sets.  Each projection type j keeps its
+    activations of all R layers in one tensor X[j] [R, M, K] and its outputs
+    in Y[j] [R, M, N] (contiguous, so the end-to-end arm copies them in one
+    transfer each)."""
     import torch
     from gemm_pq2_ternary_gb300 import binding as pq2
     from gemm_pq2_ternary_gb300 import inputs
 
+    X = [torch.empty((R, M, K), dtype=torch.float16, device=device) for (M, K, N, _, _) in layer]
+    Y = [torch.empty((R, M, N), dtype=torch.float32, device=device) for (M, K, N, _, _) in layer]
     layers = []
     for r in range(R):
         gen = torch.Generator(device=device)
         gen.manual_seed(1000 + r)
         projs = []
-        for (M, K, N, cdist, xdist) in layer:
+        for j, (M, K, N, cdist, xdist) in enumerate(layer):
             tern = inputs.draw_ternary_torch(N, K, cdist, gen, device)
             ws = inputs.draw_ws_torch(N, K, gen, device)
             codes, ws_p = pq2.pack(tern, ws)
             del tern
-            x = inputs.draw_x_torch(M, K, xdist, gen, device)
+            X[j][r].copy_(inputs.draw_x_torch(M, K, xdist, gen, device))
             qp, S, T = pq2.alloc_act(M, K, device)
-            y = torch.empty((M, N), dtype=torch.float32, device=device)
             op = pq2.PQ2_OP_GEMV if M == 1 else (pq2.PQ2_OP_SMALL if M <= 16 else pq2.PQ2_OP_PREFILL)
             wsp = pq2.alloc_workspace(op, M, N, K, device)
             mmws = pq2.alloc_workspace(pq2.PQ2_OP_MATMUL, M, N, K, device)
-            projs.append(dict(M=M, K=K, N=N, codes=codes, ws=ws_p, x=x, qp=qp, S=S, T=T, y=y,
-                              op=op, wsp=wsp, mmws=mmws))
+            projs.append(dict(M=M, K=K, N=N, codes=codes, ws=ws_p, x=X[j][r], qp=qp, S=S, T=T,
+                              y=Y[j][r], op=op, wsp=wsp, mmws=mmws))
         layers.append(projs)
     torch.cuda.synchronize()
-    return layers
+    return layers, X, Y
 
 
 def run_matmul(pq2, p):
@@ -196,28 +201,29 @@ def step_fn(pq2, layers, matmul_only=False):
     return fn
 
 
-def time_graph(torch, graph, steps, warmup, stream):
-    for _ in range(warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(steps):
-        graph.replay()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    return t0.elapsed_time(t1) / steps
-
-
 def capture(torch, fn, stream):
-    fn()  # eager once (sets function attributes, warms caches)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        fn()
+    with torch.cuda.stream(stream):
+        fn()  # eager once (sets kernel attributes, warms caches)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
     torch.cuda.synchronize()
     return g
+
+
+def timed_replays(torch, graph, n, stream):
+    """Replays `graph` n times on `stream`; returns elapsed ms (CUDA events
+    recorded on that stream)."""
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(n):
+            graph.replay()
+        t1.record(stream)
+    t1.synchronize()
+    return t0.elapsed_time(t1)
 
 
 def gpu_arm(args, rank, world, dist):
@@ -232,13 +238,18 @@ def gpu_arm(args, rank, world, dist):
     name, layer, kind = workload_spec(args)
     layer_weight_bytes = sum(N * K // 4 + 2 * N * (K // 128) for (M, K, N, _, _) in layer)
     R = args.projections or max(1, math.ceil(4 * l2 / layer_weight_bytes))
-    layers = build_layers(args, layer, R, device)
+    layers, X, Y = build_layers(args, layer, R, device)
 
     stream = torch.cuda.Stream(device)
-    with torch.cuda.stream(stream):
-        g_step = capture(torch, step_fn(pq2, layers), stream)
-        g_mm = capture(torch, step_fn(pq2, layers, matmul_only=True), stream)
+    g_step = capture(torch, step_fn(pq2, layers), stream)
+    g_mm = capture(torch, step_fn(pq2, layers, matmul_only=True), stream)
     assert pq2.pq2_last_device_error(stream) == pq2.PQ2_OK
+
+    # A step replays the R-layer graph `reps` times, so the timed region
+    # lasts long enough for the clock sampler (>= ~1.5 s over all steps).
+    timed_replays(torch, g_step, 3, stream)
+    t_rep = timed_replays(torch, g_step, 3, stream) / 3
+    reps = args.reps or max(1, math.ceil(1500.0 / (args.steps * t_rep)))
 
     def barrier():
         if dist is not None:
@@ -247,67 +258,65 @@ def gpu_arm(args, rank, world, dist):
 
     clocks = ClockSampler(local)
     for _ in range(args.warmup):
-        g_step.replay()
+        timed_replays(torch, g_step, reps, stream)
     barrier()
     clocks.start()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        g_step.replay()
-    t1.record(stream)
+    time.sleep(0.25)  # let the sampler attach
+    ms_total = timed_replays(torch, g_step, reps * args.steps, stream)
     barrier()
     clk = clocks.stop()
-    ms_step = t0.elapsed_time(t1) / args.steps
+    ms_step = ms_total / args.steps
     if dist is not None:
         t = torch.tensor([ms_step], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_step = float(t.item())
 
     # dominant kernel (the matmul) alone, same weight sets, for the roofline
-    ms_mm = time_graph(torch, g_mm, args.steps, args.warmup, stream)
-    mm_per_launch_ms = ms_mm / (R * len(layer))
+    timed_replays(torch, g_mm, reps, stream)
+    ms_mm = timed_replays(torch, g_mm, reps * args.steps, stream)
+    mm_per_launch_ms = ms_mm / (reps * args.steps * R * len(layer))
 
     units_layer = per_layer_units(layer, kind)
-    units_step = units_layer * R
+    units_step = units_layer * R * reps
     scale = 1e-9 if kind == "GB/s" else 1e-12
     value = units_step * world / (ms_step * 1e-3) * scale
 
     hbm, bf16, bf16_sus, peak_src = load_peaks()
+    per_launch = units_layer / len(layer)
     if kind == "GB/s":
-        per_launch = units_layer / len(layer)
         achieved = per_launch / (mm_per_launch_ms * 1e-3) * 1e-9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": None,
-                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
+                "peak_source": f"{peak_src}: MEASURED_PEAKS.json hbm_gbs (copy)"}
     else:
-        per_launch = units_layer / len(layer)
         achieved = per_launch / (mm_per_launch_ms * 1e-3) * 1e-12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
                 "frac": round(achieved / bf16, 4), "traffic": None,
-                "peak_source": f"{peak_src} bf16 burst; kind::f16 runs at the bf16 rate"}
+                "peak_source": f"{peak_src}: MEASURED_PEAKS.json bf16_tflops (burst)"}
 
-    # end to end through the public API, host buffers, copies inside the timing
     e2e = None
     if not args.no_e2e:
-        e2e = e2e_arm(torch, pq2, layers, args, stream, kind, units_step, world, dist, device)
+        e2e = e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_layer * R, world,
+                      dist, device)
 
-    launches = args.steps * R * 2 * len(layer)
+    launches = args.steps * reps * R * 2 * len(layer)
     out = {
         "metric": f"ternary matmul {kind} ({name})",
         "value": round(value, 2), "unit": kind, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "i8",
         "data": "synthetic (seeded; ternary codes, fp16 scales and activations drawn on device)",
-        "config": {"workload": name, "projections_per_step": R,
+        "config": {"workload": name, "projections_per_pass": R * len(layer),
+                   "passes_per_step": reps,
                    "shapes": [{"M": M, "K": K, "N": N} for (M, K, N, _, _) in layer],
-                   "l2": f"inputs larger than L2: {R * layer_weight_bytes / 1e6:.0f} MB of weights "
-                         f"per step vs {l2 / 1e6:.0f} MB L2",
-                   "graph": "one CUDA graph per step, programmatic dependent launch",
+                   "l2": f"inputs larger than L2: {R * layer_weight_bytes / 1e6:.0f} MB of distinct "
+                         f"weights per pass vs {l2 / 1e6:.0f} MB L2",
+                   "graph": "one CUDA graph per pass (quantise + matmul per projection), "
+                            "programmatic dependent launch",
                    "arith": "int8 activations x 2-bit ternary codes, int32 group dots, fp32 sums",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
-        "matmul_ms_per_launch": round(mm_per_launch_ms, 5),
+        "matmul_us_per_launch": round(mm_per_launch_ms * 1e3, 3),
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk,
@@ -315,40 +324,47 @@ def gpu_arm(args, rank, world, dist):
     return out, (name, layer, kind)
 
 
-def e2e_arm(torch, pq2, layers, args, stream, kind, units_step, world, dist, device):
-    """The same metric through pq2_matmul (the public call) with host
-    buffers: each step copies every projection's fp16 activations from pinned
-    host memory and reads every output back, inside the timed region."""
+def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dist, device):
+    """The same metric through pq2_matmul (the public call, eager) with host
+    buffers: every pass copies all activations in from pinned host memory
+    and all outputs back, inside the timed region (CUDA events on the
+    stream)."""
+    Xh = [x.cpu().pin_memory() for x in X]
+    Yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in Y]
+    h2d = sum(x.numel() * x.element_size() for x in Xh)
+    d2h = sum(y.numel() * y.element_size() for y in Yh)
     projs = [p for layer in layers for p in layer]
-    xs_h = [p["x"].cpu().pin_memory() for p in projs]
-    ys_h = [torch.empty_like(p["y"], device="cpu").pin_memory() for p in projs]
-    h2d = sum(x.numel() * x.element_size() for x in xs_h)
-    d2h = sum(y.numel() * y.element_size() for y in ys_h)
 
-    def one_step():
-        for p, xh, yh in zip(projs, xs_h, ys_h):
-            p["x"].copy_(xh, non_blocking=True)
+    def one_pass():
+        for x, xh in zip(X, Xh):
+            x.copy_(xh, non_blocking=True)
+        for p in projs:
             pq2.pq2_matmul(p["x"], p["codes"], p["ws"], p["y"], p["mmws"])
-            yh.copy_(p["y"], non_blocking=True)
+        for y, yh in zip(Y, Yh):
+            yh.copy_(y, non_blocking=True)
 
-    steps = max(1, min(args.steps, 10))
+    passes = max(3, min(args.steps, 20))
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         for _ in range(2):
-            one_step()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(steps):
-            one_step()
-        torch.cuda.synchronize()
-        dt = (time.perf_counter() - t0) / steps
+            one_pass()
+        stream.synchronize()
+        t0.record(stream)
+        for _ in range(passes):
+            one_pass()
+        t1.record(stream)
+    t1.synchronize()
+    dt = t0.elapsed_time(t1) * 1e-3 / passes
     if dist is not None:
         t = torch.tensor([dt], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         dt = float(t.item())
     scale = 1e-9 if kind == "GB/s" else 1e-12
-    return {"value": round(units_step * world / dt * scale, 2), "unit": kind,
+    return {"value": round(units_pass * world / dt * scale, 2), "unit": kind,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(dt * 1e3, 4), "timer": "host wall clock around synchronised steps"}
+            "ms_per_step": round(dt * 1e3, 4),
+            "step": "one pass over all projections: copy in, pq2_matmul each, copy out"}
 
 
 # ---------------------------------------------------------------------------
@@ -430,6 +446,8 @@ def main():
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--shape", default="5120,17408")
     ap.add_argument("--projections", type=int, default=0, help="weight sets per step (0: auto)")
+    ap.add_argument("--reps", type=int, default=0,
+                    help="passes over the R weight sets per step (0: auto, >= 1.5 s timed)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

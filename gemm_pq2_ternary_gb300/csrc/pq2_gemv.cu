@@ -9,25 +9,26 @@
 // "The win: a program just for one token": no token dimension at all.
 //
 // GB300 layout of the work (not the pages' tiling):
-//  * One persistent CTA per SM owns a contiguous range of output rows.  Rows
-//    are contiguous in memory (codes [N, K/4] row-major), so a stage of R
-//    rows is ONE contiguous chunk: a single 1-D bulk copy (TMA engine) per
-//    stage streams it into a shared-memory ring, completion tracked by an
-//    mbarrier.  One elected producer thread keeps `stages` copies in flight,
-//    enough bytes to cover HBM latency with no register cost.
-//  * Consumer thread (rp, gi) always works on the same 128-weight groups
-//    gi, gi+GT, ... of every row it handles, so its 128 activation bytes per
-//    group, s and t live in registers for the whole kernel: activations cost
-//    no shared-memory traffic.  RP rows are processed side by side.
+//  * Persistent CTAs (up to two per SM) each own a contiguous range of output
+//    rows.  Rows are contiguous in memory (codes [N, K/4] row-major), so a
+//    stage of R rows is ONE contiguous chunk: a single 1-D bulk copy (TMA
+//    engine) per stage streams it into a shared-memory ring, completion
+//    tracked by an mbarrier.  One elected producer thread keeps the ring full.
+//  * Consumer thread (rp, gi) always works on the same 128-weight group gi of
+//    the rows it handles, so the group's 128 activation bytes, s and t live
+//    in registers for the whole kernel.  Two rows are processed at once for
+//    instruction-level parallelism.
 //  * Per group: two 16-byte shared loads of codes, 32 mask + 32 DP4A (plane
-//    s masked in place as 4^s * code, rescaled exactly by shifts), the
-//    -sum(q) correction, one fp32 multiply and one FMA.
-//  * Row sums: per-thread partials go to a double-buffered shared array and
-//    a warp sums each row in a fixed order (deterministic), one named
-//    barrier per stage (which also ORs the consumers' wait failures, so all
-//    of them stop at the same stage).
+//    s masked in place is 4^s times the codes; the four plane sums are
+//    rescaled exactly by shifts), the -sum(q) correction, one fp32 multiply
+//    and one FMA.
+//  * Each consumer warp releases a ring slot on its own (mbarrier arrive);
+//    per-thread group terms go to a shared array and are summed per row, in
+//    a fixed order, once per chunk of rows (one named barrier per chunk).
 //  * Every mbarrier wait is bounded; on expiry the block sets the device
 //    error word, stops, and the producer waits for its copies in flight.
+#include <cstdlib>
+
 #include "pq2_internal.h"
 
 namespace {
@@ -44,17 +45,37 @@ struct GemvParams {
     int GT;            // threads per row (each owns GPT groups)
     int RP;            // rows handled side by side
     int TC;            // consumer threads (multiple of 32)
-    int R;             // rows per stage (multiple of RP)
+    int R;             // rows per stage (multiple of 2*RP)
     int stages;
+    int chunk_stages;  // stages per row-sum chunk
     int rows_per_cta;
     uint32_t stage_bytes;      // ring slot size (codes + ws, 16-aligned)
     uint32_t codes_row_bytes;  // K / 4
     pq2::DevCtl ctl;
 };
 
-constexpr int kRingBudget = 160 * 1024;
-constexpr int kTargetConsumers = 256;
 constexpr int kMaxThreads = 512 + 32;  // consumers (<= 512) + producer warp
+
+// The group's 32 code bytes are read as two 16-byte halves, half `h` first
+// (h alternates every 4 lanes, which makes each 8-lane phase of the shared
+// loads hit 8 distinct bank groups).  The thread's activation words were
+// permuted the same way when they were loaded, so word i of `w` still meets
+// its own activation word.
+template <bool WS_SMEM, bool DOTS>
+__device__ __forceinline__ float group_term(const uint8_t* crow, const uint8_t* wsrow_smem,
+                                            const __half* wsrow_gmem, int32_t* dotrow, int g,
+                                            const uint32_t* q, int t, float s, int h) {
+    const uint4* cw = reinterpret_cast<const uint4*>(crow + g * 32);
+    const uint4 c0 = cw[h], c1 = cw[h ^ 1];
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const int dot = pq2::group_codes_dot(w, q) - t;
+    if (DOTS) {
+        dotrow[g] = dot;
+        return 0.0f;
+    }
+    const __half wsh = WS_SMEM ? reinterpret_cast<const __half*>(wsrow_smem)[g] : wsrow_gmem[g];
+    return static_cast<float>(dot) * s * __half2float(wsh);
+}
 
 template <int GPT, bool WS_SMEM, bool DOTS>
 __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p) {
@@ -63,33 +84,36 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
     uint64_t* empty = full + p.stages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + p.stages);
     float* red = reinterpret_cast<float*>(smem + 16 * p.stages + 16);
-    const int red_stride = p.R * p.GT;  // floats per buffer
+    const int chunk_rows = p.chunk_stages * p.R;
+    const int red_stride = chunk_rows * p.GT;  // floats per buffer
     uint8_t* ring = smem + ((16 * p.stages + 16 + 8 * red_stride + 127) & ~127);
 
     const int n_begin = blockIdx.x * p.rows_per_cta;
     const int n_end = min(p.N, n_begin + p.rows_per_cta);
     if (n_begin >= n_end) return;
     const int nst = (n_end - n_begin + p.R - 1) / p.R;
+    const int tid = threadIdx.x;
+    const int nwarps = p.TC >> 5;
 
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         for (int i = 0; i < p.stages; ++i) {
             pq2::mbar_init(&full[i], 1);
-            pq2::mbar_init(&empty[i], 1);
+            pq2::mbar_init(&empty[i], nwarps);
         }
         *abort_flag = 0;
         pq2::fence_mbar_init();
     }
     __syncthreads();
-    // Every input may have been written by the preceding kernel.
+    // Activations, scales and (possibly) weights may come from the preceding
+    // kernel: wait for it before reading any of them.
     pq2::pdl_wait();
     pq2::pdl_launch_dependents();
 
-    const int tid = threadIdx.x;
     if (tid >= p.TC) {
         // ------------------------------ producer ------------------------------
         if (tid != p.TC) return;
         const uint64_t policy = pq2::policy_evict_first();
-        int issued_end = 0;  // stages [0, issued_end) were armed, except the withheld one
+        int issued_end = 0;  // stages [0, issued_end) were armed, except a withheld one
         for (int i = 0; i < nst; ++i) {
             const int slot = i % p.stages;
             if (i >= p.stages) {
@@ -127,7 +151,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
     const int rp = tid / p.GT;
     const int gi = tid - rp * p.GT;
     const bool active = rp < p.RP;
-    const int RI = p.R / p.RP;
+    const int RI = p.R / p.RP;  // even
+    const int hswap = (tid >> 2) & 1;  // which 16-byte half of a group to read first
 
     uint32_t qreg[GPT][32];
     float sg[GPT];
@@ -141,7 +166,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
         const uint4* src = reinterpret_cast<const uint4*>(p.qp + static_cast<size_t>(gl) * 128);
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-            const uint4 w = src[v];
+            // plane v/2, words 4*(v&1)..+3; stored at the half this thread reads first
+            const uint4 w = src[v ^ hswap];
             qreg[j][4 * v + 0] = w.x;
             qreg[j][4 * v + 1] = w.y;
             qreg[j][4 * v + 2] = w.z;
@@ -153,67 +179,78 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
 
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int nwarps = p.TC >> 5;
+    bool failed = false;
 
-    for (int i = 0; i < nst; ++i) {
-        const int slot = i % p.stages;
-        const bool ok = pq2::mbar_wait_bounded(&full[slot], (i / p.stages) & 1, p.ctl, abort_flag);
-        if (!ok) *abort_flag = 1;
-        const int row0 = n_begin + i * p.R;
-        const int rows = min(p.R, n_end - row0);
-        const uint8_t* stage = ring + static_cast<size_t>(slot) * p.stage_bytes;
-        float* redb = red + (i & 1) * red_stride;
-        if (ok && active) {
-            for (int t = 0; t < RI; ++t) {
-                const int r = rp + t * p.RP;
-                if (r >= rows) break;
-                const uint8_t* crow = stage + static_cast<size_t>(r) * p.codes_row_bytes;
-                float acc = 0.0f;
+    for (int c0 = 0; c0 < nst; c0 += p.chunk_stages) {
+        const int c1 = min(nst, c0 + p.chunk_stages);
+        float* redb = red + ((c0 / p.chunk_stages) & 1) * red_stride;
+        for (int i = c0; i < c1; ++i) {
+            const int slot = i % p.stages;
+            if (!failed) {
+                if (!pq2::mbar_wait_bounded(&full[slot], (i / p.stages) & 1, p.ctl, abort_flag)) {
+                    failed = true;
+                    *abort_flag = 1;
+                }
+            }
+            if (!failed && active) {
+                const int row0 = n_begin + i * p.R;
+                const int rows = min(p.R, n_end - row0);
+                const uint8_t* stage = ring + static_cast<size_t>(slot) * p.stage_bytes;
+                const uint8_t* wsm = stage + static_cast<size_t>(p.R) * p.codes_row_bytes;
+                for (int t = 0; t < RI; t += 2) {
+                    const int ra = rp + t * p.RP;
+                    const int rb = ra + p.RP;
+                    if (ra >= rows) break;
+                    const bool hb = rb < rows;
+                    const int rbs = hb ? rb : ra;  // recompute row a when b is past the end
+                    const uint8_t* ca = stage + static_cast<size_t>(ra) * p.codes_row_bytes;
+                    const uint8_t* cb = stage + static_cast<size_t>(rbs) * p.codes_row_bytes;
+                    float acc_a = 0.0f, acc_b = 0.0f;
 #pragma unroll
-                for (int j = 0; j < GPT; ++j) {
-                    if (!gval[j]) continue;
-                    const int g = gi + j * p.GT;
-                    const uint4* cw = reinterpret_cast<const uint4*>(crow + g * 32);
-                    const uint4 c0 = cw[0], c1 = cw[1];
-                    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                    const int dot = pq2::group_codes_dot(w, qreg[j]) - tg[j];
-                    if (DOTS) {
-                        p.dots[static_cast<size_t>(row0 + r) * p.G + g] = dot;
-                    } else {
-                        __half wsh;
-                        if (WS_SMEM)
-                            wsh = reinterpret_cast<const __half*>(
-                                stage + static_cast<size_t>(p.R) * p.codes_row_bytes)[r * p.G + g];
-                        else
-                            wsh = p.ws[static_cast<size_t>(row0 + r) * p.G + g];
-                        acc = fmaf(static_cast<float>(dot) * sg[j], __half2float(wsh), acc);
+                    for (int j = 0; j < GPT; ++j) {
+                        if (!gval[j]) continue;
+                        const int g = gi + j * p.GT;
+                        acc_a += group_term<WS_SMEM, DOTS>(
+                            ca, wsm + ra * p.G * 2, p.ws + static_cast<size_t>(row0 + ra) * p.G,
+                            p.dots + static_cast<size_t>(row0 + ra) * p.G, g, qreg[j], tg[j],
+                            sg[j], hswap);
+                        acc_b += group_term<WS_SMEM, DOTS>(
+                            cb, wsm + rbs * p.G * 2, p.ws + static_cast<size_t>(row0 + rbs) * p.G,
+                            p.dots + static_cast<size_t>(row0 + rbs) * p.G, g, qreg[j], tg[j],
+                            sg[j], hswap);
+                    }
+                    if (!DOTS) {
+                        const int la = (i - c0) * p.R + ra;
+                        redb[la * p.GT + gi] = acc_a;
+                        if (hb) redb[(la + p.RP) * p.GT + gi] = acc_b;
                     }
                 }
-                if (!DOTS) redb[r * p.GT + gi] = acc;
             }
+            __syncwarp();
+            if (lane == 0) pq2::mbar_arrive(&empty[slot]);
         }
-        // all consumers are done with this slot; agree on whether to stop
-        const bool any_fail = pq2::named_bar_any(1, p.TC, !ok);
-        if (tid == 0) {
-            pq2::mbar_arrive(&empty[slot]);
-            if (any_fail) *abort_flag = 1;
+        // all consumers have written this chunk's terms; agree on stopping
+        const bool any_fail = pq2::named_bar_any(1, p.TC, failed);
+        if (any_fail) {
+            if (tid == 0) *abort_flag = 1;
+            break;
         }
-        if (any_fail) break;
         if (!DOTS) {
-            for (int r = warp; r < rows; r += nwarps) {
+            const int crow0 = n_begin + c0 * p.R;
+            const int crows = min(n_end, n_begin + c1 * p.R) - crow0;
+            for (int r = warp; r < crows; r += nwarps) {
                 float s = 0.0f;
                 for (int c = lane; c < p.GT; c += 32) s += redb[r * p.GT + c];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == 0) p.y[row0 + r] = s;
+                if (lane == 0) p.y[crow0 + r] = s;
             }
         }
     }
 }
 
 template <int GPT, bool WS_SMEM, bool DOTS>
-cudaError_t launch_variant(const GemvParams& p, int grid, size_t smem, cudaStream_t st,
-                           const pq2h::DeviceInfo& dev) {
+cudaError_t launch_variant(const GemvParams& p, int grid, size_t smem, cudaStream_t st) {
     auto kern = gemv_kernel<GPT, WS_SMEM, DOTS>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -223,10 +260,36 @@ cudaError_t launch_variant(const GemvParams& p, int grid, size_t smem, cudaStrea
 
 template <int GPT>
 cudaError_t launch_gpt(const GemvParams& p, int grid, size_t smem, bool ws_smem, bool dots,
-                       cudaStream_t st, const pq2h::DeviceInfo& dev) {
-    if (dots) return launch_variant<GPT, false, true>(p, grid, smem, st, dev);
-    if (ws_smem) return launch_variant<GPT, true, false>(p, grid, smem, st, dev);
-    return launch_variant<GPT, false, false>(p, grid, smem, st, dev);
+                       cudaStream_t st) {
+    if (dots) return launch_variant<GPT, false, true>(p, grid, smem, st);
+    if (ws_smem) return launch_variant<GPT, true, false>(p, grid, smem, st);
+    return launch_variant<GPT, false, false>(p, grid, smem, st);
+}
+
+// Tuning knobs (environment, read once): PQ2_GEMV_CTAS_PER_SM (default 2),
+// PQ2_GEMV_RING_KB (default 96), PQ2_GEMV_THREADS (target consumer threads,
+// default 256), PQ2_GEMV_STAGE_KB (default 8).
+int env_int(const char* name, int dflt) {
+    const char* v = std::getenv(name);
+    if (!v || !*v) return dflt;
+    const int x = std::atoi(v);
+    return x > 0 ? x : dflt;
+}
+
+struct Tuning {
+    int ctas_per_sm, ring_kb, threads, stage_kb;
+};
+
+const Tuning& tuning() {
+    static const Tuning t = {env_int("PQ2_GEMV_CTAS_PER_SM", 2), env_int("PQ2_GEMV_RING_KB", 96),
+                             env_int("PQ2_GEMV_THREADS", 256), env_int("PQ2_GEMV_STAGE_KB", 8)};
+    return t;
+}
+
+size_t smem_bytes(const GemvParams& p) {
+    const int red_floats = 2 * p.chunk_stages * p.R * p.GT;
+    const size_t head = (16 * p.stages + 16 + 4 * red_floats + 127) & ~127;
+    return head + static_cast<size_t>(p.stages) * p.stage_bytes;
 }
 
 }  // namespace
@@ -236,6 +299,7 @@ namespace pq2h {
 cudaError_t launch_gemv(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
                         const __half* ws, float* y, int32_t* dots, int64_t N, int64_t K,
                         cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev) {
+    const Tuning& tu = tuning();
     GemvParams p = {};
     p.qp = qp;
     p.S = S;
@@ -249,30 +313,38 @@ cudaError_t launch_gemv(const int8_t* qp, const float* S, const int32_t* T, cons
     p.G = static_cast<int>(K / 128);
     const int gpt = p.G <= 512 ? 1 : (p.G <= 1024 ? 2 : 4);
     p.GT = (p.G + gpt - 1) / gpt;
-    p.RP = kTargetConsumers / p.GT > 0 ? kTargetConsumers / p.GT : 1;
+    const int target = tu.threads < 32 ? 32 : (tu.threads > 512 ? 512 : tu.threads);
+    p.RP = target / p.GT > 0 ? target / p.GT : 1;
     p.TC = ((p.RP * p.GT + 31) / 32) * 32;
     p.codes_row_bytes = static_cast<uint32_t>(K / 4);
     const bool ws_smem = (dots == nullptr) && (p.G % 8 == 0);
     const int row_bytes = static_cast<int>(p.codes_row_bytes) + (ws_smem ? 2 * p.G : 0);
-    const int per_rp = p.RP * row_bytes;
-    int ri = (12 * 1024 + per_rp / 2) / per_rp;
-    if (ri < 1) ri = 1;
-    p.R = p.RP * ri;
+    const int per_pair = 2 * p.RP * row_bytes;  // rows come in pairs per thread
+    int pairs = (tu.stage_kb * 1024 + per_pair / 2) / per_pair;
+    if (pairs < 1) pairs = 1;
+    p.R = 2 * p.RP * pairs;
     p.stage_bytes = static_cast<uint32_t>(((p.R * row_bytes) + 15) & ~15);
-    int stages = kRingBudget / static_cast<int>(p.stage_bytes);
-    if (stages > 16) stages = 16;
-    if (stages < 2) stages = 2;
-    p.stages = stages;
-    const int rows_per_cta = static_cast<int>((N + dev.num_sms - 1) / dev.num_sms);
+    int stages = tu.ring_kb * 1024 / static_cast<int>(p.stage_bytes);
+    p.stages = stages > 16 ? 16 : (stages < 2 ? 2 : stages);
+    const int64_t slots = static_cast<int64_t>(dev.num_sms) * tu.ctas_per_sm;
+    const int rows_per_cta = static_cast<int>((N + slots - 1) / slots);
     p.rows_per_cta = rows_per_cta;
+    // ~64 rows per row-sum chunk, never more than the CTA owns
+    int cs = (64 + p.R - 1) / p.R;
+    const int cta_stages = (rows_per_cta + p.R - 1) / p.R;
+    if (cs > cta_stages) cs = cta_stages;
+    p.chunk_stages = cs < 1 ? 1 : cs;
     const int grid = static_cast<int>((N + rows_per_cta - 1) / rows_per_cta);
     p.ctl = ctl;
-    const size_t head = ((16 * p.stages + 16 + 8 * p.R * p.GT + 127) & ~127);
-    const size_t smem = head + static_cast<size_t>(p.stages) * p.stage_bytes;
+    size_t smem = smem_bytes(p);
+    while (smem > static_cast<size_t>(dev.max_smem_optin) && p.stages > 2) {
+        --p.stages;
+        smem = smem_bytes(p);
+    }
     if (smem > static_cast<size_t>(dev.max_smem_optin)) return cudaErrorInvalidConfiguration;
-    if (gpt == 1) return launch_gpt<1>(p, grid, smem, ws_smem, dots != nullptr, st, dev);
-    if (gpt == 2) return launch_gpt<2>(p, grid, smem, ws_smem, dots != nullptr, st, dev);
-    return launch_gpt<4>(p, grid, smem, ws_smem, dots != nullptr, st, dev);
+    if (gpt == 1) return launch_gpt<1>(p, grid, smem, ws_smem, dots != nullptr, st);
+    if (gpt == 2) return launch_gpt<2>(p, grid, smem, ws_smem, dots != nullptr, st);
+    return launch_gpt<4>(p, grid, smem, ws_smem, dots != nullptr, st);
 }
 
 }  // namespace pq2h
