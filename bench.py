@@ -52,8 +52,12 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 def gemm_bytes(M, N, K):
     """Algorithmic bytes of one matmul call (each byte once): codes, weight
-    scales, quantised activations, S and T, fp32 output."""
+    scales, quantised activations, S and T, fp32 output.  For M = 1 the step
+    runs the fused quantise + GEMV kernel, whose inputs are the fp16
+    activations instead of the quantised ones."""
     G = K // 128
+    if M == 1:
+        return N * K // 4 + 2 * N * G + 2 * K + 4 * N
     return N * K // 4 + 2 * N * G + M * K + 8 * M * G + 4 * M * N
 
 
@@ -192,9 +196,15 @@ def run_matmul(pq2, p):
 
 
 def step_fn(pq2, layers, matmul_only=False):
+    """One pass: per projection, M = 1 runs pq2_matmul (the fused quantise +
+    GEMV kernel); M > 1 runs pq2_quantize_act then the matmul kernel (the
+    matmul alone when matmul_only)."""
     def fn():
         for projs in layers:
             for p in projs:
+                if p["M"] == 1:
+                    pq2.pq2_matmul(p["x"], p["codes"], p["ws"], p["y"], p["mmws"])
+                    continue
                 if not matmul_only:
                     pq2.pq2_quantize_act(p["x"], p["qp"], p["S"], p["T"])
                 run_matmul(pq2, p)
@@ -299,7 +309,7 @@ def gpu_arm(args, rank, world, dist):
         e2e = e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_layer * R, world,
                       dist, device)
 
-    launches = args.steps * reps * R * 2 * len(layer)
+    launches = args.steps * reps * R * sum(1 if M == 1 else 2 for (M, _, _, _, _) in layer)
     out = {
         "metric": f"ternary matmul {kind} ({name})",
         "value": round(value, 2), "unit": kind, "n_gpus": world, "steps": args.steps,
@@ -311,8 +321,9 @@ def gpu_arm(args, rank, world, dist):
                    "shapes": [{"M": M, "K": K, "N": N} for (M, K, N, _, _) in layer],
                    "l2": f"inputs larger than L2: {R * layer_weight_bytes / 1e6:.0f} MB of distinct "
                          f"weights per pass vs {l2 / 1e6:.0f} MB L2",
-                   "graph": "one CUDA graph per pass (quantise + matmul per projection), "
-                            "programmatic dependent launch",
+                   "graph": "one CUDA graph per pass (per projection: fused quantise+GEMV "
+                            "for M=1, quantise then matmul otherwise), programmatic dependent "
+                            "launch",
                    "arith": "int8 activations x 2-bit ternary codes, int32 group dots, fp32 sums",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,

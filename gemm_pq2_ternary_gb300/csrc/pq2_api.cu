@@ -174,9 +174,9 @@ pq2_status pq2_gemv(const int8_t* qp, const float* S, const int32_t* T, const ui
     Ctx c;
     s = get_ctx(&c);
     if (s != PQ2_OK) return s;
-    return cuda_status(pq2h::launch_gemv(qp, S, T, codes, static_cast<const __half*>(ws_f16), y,
-                                         nullptr, N, K, static_cast<cudaStream_t>(stream), c.ctl,
-                                         c.dev));
+    return cuda_status(pq2h::launch_gemv(nullptr, qp, S, T, codes,
+                                         static_cast<const __half*>(ws_f16), y, nullptr, N, K,
+                                         static_cast<cudaStream_t>(stream), c.ctl, c.dev));
 }
 
 size_t pq2_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
@@ -186,6 +186,7 @@ size_t pq2_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
         case PQ2_OP_SMALL: return (M >= 2 && M <= 16) ? 0 : SIZE_MAX;
         case PQ2_OP_PREFILL: return 0;
         case PQ2_OP_MATMUL: {
+            if (M == 1) return 0;  // fused quantise + GEMV, no scratch
             const size_t G = static_cast<size_t>(K / 128);
             const size_t act = align256(static_cast<size_t>(M) * K) +
                                2 * align256(static_cast<size_t>(M) * G * 4);
@@ -241,6 +242,18 @@ pq2_status pq2_matmul(const void* x_f16, const uint8_t* codes, const void* ws_f1
     if (M < 1 || !x_f16 || !codes || !ws_f16 || !y) return PQ2_ERR_INVALID_ARG;
     const size_t need = pq2_workspace_bytes(PQ2_OP_MATMUL, M, N, K);
     if (need == SIZE_MAX) return PQ2_ERR_UNSUPPORTED_SHAPE;
+    if (M == 1) {
+        // fused: the GEMV kernel quantises x itself
+        if (!aligned16(x_f16) || !aligned16(codes) || !aligned16(ws_f16) || !aligned16(y))
+            return PQ2_ERR_MISALIGNED;
+        Ctx c;
+        s = get_ctx(&c);
+        if (s != PQ2_OK) return s;
+        return cuda_status(pq2h::launch_gemv(static_cast<const __half*>(x_f16), nullptr, nullptr,
+                                             nullptr, codes, static_cast<const __half*>(ws_f16),
+                                             y, nullptr, N, K, static_cast<cudaStream_t>(stream),
+                                             c.ctl, c.dev));
+    }
     if (!workspace || workspace_bytes < need) return PQ2_ERR_WORKSPACE;
     if (!aligned16(workspace)) return PQ2_ERR_MISALIGNED;
     const size_t G = static_cast<size_t>(K / 128);
@@ -278,8 +291,8 @@ pq2_status pq2_group_dots(int op, const int8_t* qp, const int32_t* T, const uint
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (op == PQ2_OP_GEMV)
         return cuda_status(
-            pq2h::launch_gemv(qp, nullptr, T, codes, nullptr, nullptr, dots, N, K, st, c.ctl,
-                              c.dev));
+            pq2h::launch_gemv(nullptr, qp, nullptr, T, codes, nullptr, nullptr, dots, N, K, st,
+                              c.ctl, c.dev));
     return cuda_status(pq2h::launch_simple(qp, nullptr, T, codes, nullptr, nullptr, dots, M, N,
                                            K, st, c.ctl, c.dev));
 }

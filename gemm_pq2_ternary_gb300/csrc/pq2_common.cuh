@@ -164,6 +164,66 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     return v;
 }
 
+// Quantise one 128-value group with one warp ("Making a ternary reasoning
+// model fast in vLLM", page "From CUDA to Triton and Gluon", section "Prompt
+// processing": q int8, s fp32, t int32 per group; section "One token at a
+// time": plane order).  Lane b holds the four values of code byte b
+// (weights 4b..4b+3) and writes plane s at qg[s*32 + b].  amax/127 and x/d
+// are IEEE divisions rounded to nearest, q rounds half to even and is clamped
+// to [-127,127]; an all-zero group gives s = 0, q = 0.
+__device__ __forceinline__ void quantize_group_loaded(uint2 raw, int lane, int8_t* qg,
+                                                      float* s_out, int32_t* t_out) {
+    const __half2 h01 = *reinterpret_cast<const __half2*>(&raw.x);
+    const __half2 h23 = *reinterpret_cast<const __half2*>(&raw.y);
+    const float v[4] = {__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23)};
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float d = __fdiv_rn(amax, 127.0f);
+    int sum = 0;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        int q = 0;
+        if (amax != 0.0f) {
+            q = __float2int_rn(__fdiv_rn(v[s], d));
+            q = max(-127, min(127, q));
+        }
+        sum += q;
+        qg[s * 32 + lane] = static_cast<int8_t>(q);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) {
+        *s_out = (amax != 0.0f) ? d : 0.0f;
+        *t_out = sum;
+    }
+}
+
+__device__ __forceinline__ void quantize_group_warp(const __half* xg, int lane, int8_t* qg,
+                                                    float* s_out, int32_t* t_out) {
+    quantize_group_loaded(*reinterpret_cast<const uint2*>(xg + 4 * lane), lane, qg, s_out, t_out);
+}
+
+// All G groups of one activation row by `nwarps` warps (this one is `warp`):
+// the loads of up to 8 groups per warp are issued together before any of
+// them is quantised, so their latencies overlap.
+__device__ __forceinline__ void quantize_row_warps(const __half* x, int G, int warp, int nwarps,
+                                                   int lane, int8_t* q, float* s, int32_t* t) {
+    for (int g0 = warp; g0 < G; g0 += 8 * nwarps) {
+        uint2 raw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int g = g0 + i * nwarps;
+            if (g < G) raw[i] = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(g) * 128 + 4 * lane);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int g = g0 + i * nwarps;
+            if (g < G) quantize_group_loaded(raw[i], lane, q + g * 128, s + g, t + g);
+        }
+    }
+}
+
 // Codes-dot of one 128-weight group: 8 code words against the 32 plane-ordered
 // activation words q[s*8 + j] (plane s, word j).  Plane s of word w is
 // w & (3 << 2s) per byte, i.e. 4^s times the codes; the four plane sums are

@@ -34,6 +34,7 @@
 namespace {
 
 struct GemvParams {
+    const __half* x;   // fused path: fp16 activations [K] (qp, S, T unused)
     const int8_t* qp;
     const float* S;
     const int32_t* T;
@@ -51,8 +52,13 @@ struct GemvParams {
     int rows_per_cta;
     uint32_t stage_bytes;      // ring slot size (codes + ws, 16-aligned)
     uint32_t codes_row_bytes;  // K / 4
+    int prefetch;              // issue an L2 prefetch of the CTA's weights first
     pq2::DevCtl ctl;
 };
+
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 
 constexpr int kMaxThreads = 512 + 32;  // consumers (<= 512) + producer warp
 
@@ -77,7 +83,7 @@ __device__ __forceinline__ float group_term(const uint8_t* crow, const uint8_t* 
     return static_cast<float>(dot) * s * __half2float(wsh);
 }
 
-template <int GPT, bool WS_SMEM, bool DOTS>
+template <int GPT, bool WS_SMEM, bool DOTS, bool FUSED>
 __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -86,7 +92,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
     float* red = reinterpret_cast<float*>(smem + 16 * p.stages + 16);
     const int chunk_rows = p.chunk_stages * p.R;
     const int red_stride = chunk_rows * p.GT;  // floats per buffer
-    uint8_t* ring = smem + ((16 * p.stages + 16 + 8 * red_stride + 127) & ~127);
+    // fused path: the quantised activations live in shared memory
+    const int act_off = (16 * p.stages + 16 + 8 * red_stride + 127) & ~127;
+    int8_t* qsm = reinterpret_cast<int8_t*>(smem + act_off);
+    float* ssm = reinterpret_cast<float*>(smem + act_off + p.K);
+    int32_t* tsm = reinterpret_cast<int32_t*>(smem + act_off + p.K + 4 * p.G);
+    const int ring_off = FUSED ? ((act_off + p.K + 8 * p.G + 127) & ~127) : act_off;
+    uint8_t* ring = smem + ring_off;
 
     const int n_begin = blockIdx.x * p.rows_per_cta;
     const int n_end = min(p.N, n_begin + p.rows_per_cta);
@@ -102,6 +114,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
         }
         *abort_flag = 0;
         pq2::fence_mbar_init();
+    }
+    if (tid == p.TC && p.prefetch) {
+        // Start the weight stream before waiting for the preceding kernel.
+        // The weights are not its output in normal use, and even if they
+        // were, a prefetch into L2 (the coherence point) cannot return stale
+        // data to the copies issued after the wait.
+        const uint8_t* src = p.codes + static_cast<size_t>(n_begin) * p.codes_row_bytes;
+        uint32_t left = static_cast<uint32_t>(n_end - n_begin) * p.codes_row_bytes;
+        while (left > 0) {
+            const uint32_t b = left < 65536u ? left : 65536u;
+            bulk_prefetch_l2(src, b);
+            src += b;
+            left -= b;
+        }
     }
     __syncthreads();
     // Activations, scales and (possibly) weights may come from the preceding
@@ -154,6 +180,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
     const int RI = p.R / p.RP;  // even
     const int hswap = (tid >> 2) & 1;  // which 16-byte half of a group to read first
 
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int8_t* qsrc = p.qp;
+    const float* ssrc = p.S;
+    const int32_t* tsrc = p.T;
+    if (FUSED) {
+        // quantise the fp16 activations once per CTA (while the producer's
+        // first weight copies are in flight)
+        pq2::quantize_row_warps(p.x, p.G, warp, nwarps, lane, qsm, ssm, tsm);
+        pq2::named_bar_sync(2, p.TC);
+        qsrc = qsm;
+        ssrc = ssm;
+        tsrc = tsm;
+    }
+
     uint32_t qreg[GPT][32];
     float sg[GPT];
     int tg[GPT];
@@ -163,7 +204,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
         const int g = gi + j * p.GT;
         gval[j] = active && g < p.G;
         const int gl = gval[j] ? g : 0;
-        const uint4* src = reinterpret_cast<const uint4*>(p.qp + static_cast<size_t>(gl) * 128);
+        const uint4* src = reinterpret_cast<const uint4*>(qsrc + static_cast<size_t>(gl) * 128);
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
             // plane v/2, words 4*(v&1)..+3; stored at the half this thread reads first
@@ -173,12 +214,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
             qreg[j][4 * v + 2] = w.z;
             qreg[j][4 * v + 3] = w.w;
         }
-        sg[j] = DOTS ? 0.0f : p.S[gl];
-        tg[j] = p.T[gl];
+        sg[j] = DOTS ? 0.0f : ssrc[gl];
+        tg[j] = tsrc[gl];
     }
 
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
     bool failed = false;
 
     for (int c0 = 0; c0 < nst; c0 += p.chunk_stages) {
@@ -249,9 +288,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
     }
 }
 
-template <int GPT, bool WS_SMEM, bool DOTS>
+template <int GPT, bool WS_SMEM, bool DOTS, bool FUSED>
 cudaError_t launch_variant(const GemvParams& p, int grid, size_t smem, cudaStream_t st) {
-    auto kern = gemv_kernel<GPT, WS_SMEM, DOTS>;
+    auto kern = gemv_kernel<GPT, WS_SMEM, DOTS, FUSED>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -261,14 +300,19 @@ cudaError_t launch_variant(const GemvParams& p, int grid, size_t smem, cudaStrea
 template <int GPT>
 cudaError_t launch_gpt(const GemvParams& p, int grid, size_t smem, bool ws_smem, bool dots,
                        cudaStream_t st) {
-    if (dots) return launch_variant<GPT, false, true>(p, grid, smem, st);
-    if (ws_smem) return launch_variant<GPT, true, false>(p, grid, smem, st);
-    return launch_variant<GPT, false, false>(p, grid, smem, st);
+    if (dots) return launch_variant<GPT, false, true, false>(p, grid, smem, st);
+    if (p.x) {
+        if (ws_smem) return launch_variant<GPT, true, false, true>(p, grid, smem, st);
+        return launch_variant<GPT, false, false, true>(p, grid, smem, st);
+    }
+    if (ws_smem) return launch_variant<GPT, true, false, false>(p, grid, smem, st);
+    return launch_variant<GPT, false, false, false>(p, grid, smem, st);
 }
 
 // Tuning knobs (environment, read once): PQ2_GEMV_CTAS_PER_SM (default 2),
-// PQ2_GEMV_RING_KB (default 96), PQ2_GEMV_THREADS (target consumer threads,
-// default 256), PQ2_GEMV_STAGE_KB (default 8).
+// PQ2_GEMV_RING_KB (default 64), PQ2_GEMV_THREADS (target consumer threads,
+// default 256), PQ2_GEMV_STAGE_KB (default 4), PQ2_GEMV_PREFETCH (1 = on,
+// default 1; 2 = off).
 int env_int(const char* name, int dflt) {
     const char* v = std::getenv(name);
     if (!v || !*v) return dflt;
@@ -277,18 +321,20 @@ int env_int(const char* name, int dflt) {
 }
 
 struct Tuning {
-    int ctas_per_sm, ring_kb, threads, stage_kb;
+    int ctas_per_sm, ring_kb, threads, stage_kb, prefetch;
 };
 
 const Tuning& tuning() {
-    static const Tuning t = {env_int("PQ2_GEMV_CTAS_PER_SM", 2), env_int("PQ2_GEMV_RING_KB", 96),
-                             env_int("PQ2_GEMV_THREADS", 256), env_int("PQ2_GEMV_STAGE_KB", 8)};
+    static const Tuning t = {env_int("PQ2_GEMV_CTAS_PER_SM", 2), env_int("PQ2_GEMV_RING_KB", 64),
+                             env_int("PQ2_GEMV_THREADS", 256), env_int("PQ2_GEMV_STAGE_KB", 4),
+                             env_int("PQ2_GEMV_PREFETCH", 1) == 1 ? 1 : 0};
     return t;
 }
 
 size_t smem_bytes(const GemvParams& p) {
     const int red_floats = 2 * p.chunk_stages * p.R * p.GT;
-    const size_t head = (16 * p.stages + 16 + 4 * red_floats + 127) & ~127;
+    size_t head = (16 * p.stages + 16 + 4 * red_floats + 127) & ~127;
+    if (p.x) head = (head + p.K + 8 * p.G + 127) & ~static_cast<size_t>(127);
     return head + static_cast<size_t>(p.stages) * p.stage_bytes;
 }
 
@@ -296,11 +342,12 @@ size_t smem_bytes(const GemvParams& p) {
 
 namespace pq2h {
 
-cudaError_t launch_gemv(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
-                        const __half* ws, float* y, int32_t* dots, int64_t N, int64_t K,
-                        cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev) {
+cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const int32_t* T,
+                        const uint8_t* codes, const __half* ws, float* y, int32_t* dots, int64_t N,
+                        int64_t K, cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev) {
     const Tuning& tu = tuning();
     GemvParams p = {};
+    p.x = dots ? nullptr : x;
     p.qp = qp;
     p.S = S;
     p.T = T;
@@ -336,6 +383,7 @@ cudaError_t launch_gemv(const int8_t* qp, const float* S, const int32_t* T, cons
     p.chunk_stages = cs < 1 ? 1 : cs;
     const int grid = static_cast<int>((N + rows_per_cta - 1) / rows_per_cta);
     p.ctl = ctl;
+    p.prefetch = tu.prefetch;
     size_t smem = smem_bytes(p);
     while (smem > static_cast<size_t>(dev.max_smem_optin) && p.stages > 2) {
         --p.stages;

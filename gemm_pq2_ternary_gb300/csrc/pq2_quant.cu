@@ -3,9 +3,8 @@
 // Quantise ("Making a ternary reasoning model fast in vLLM", page "From CUDA
 // to Triton and Gluon", section "Prompt processing": one quantize kernel
 // emits q [m,k] int8, s [m,G] fp32, t [m,G] int32; section "One token at a
-// time": q in plane order).  One warp per 128-value group: lane b holds the
-// four values of code byte b (weights 4b..4b+3), so plane s of the group is
-// written by the 32 lanes as 32 consecutive bytes at s*32.
+// time": q in plane order).  One warp per 128-value group (grid-stride), the
+// per-group step shared with the fused M = 1 path (quantize_group_warp).
 //
 // Pack (same page, "One token at a time": codes 0,1,2 for -1,0,+1, four to a
 // byte, weight 4*byte+s in bits 2s).  One thread per 16 ternary values.
@@ -23,35 +22,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const __half* __restrict_
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t gi = warp; gi < groups; gi += nwarps) {
-        // group gi covers x[gi*128 .. gi*128+127] (row-major [M,K], K = 128*G)
-        const uint2 raw = *reinterpret_cast<const uint2*>(x + gi * 128 + 4 * lane);
-        const __half2 h01 = *reinterpret_cast<const __half2*>(&raw.x);
-        const __half2 h23 = *reinterpret_cast<const __half2*>(&raw.y);
-        float v[4] = {__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23)};
-        float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float d = __fdiv_rn(amax, 127.0f);
-        int sum = 0;
-        int8_t* dst = qp + gi * 128 + lane;
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            int q = 0;
-            if (amax != 0.0f) {
-                q = __float2int_rn(__fdiv_rn(v[s], d));  // round half to even
-                q = max(-127, min(127, q));
-            }
-            sum += q;
-            dst[s * 32] = static_cast<int8_t>(q);  // weight 4*lane+s -> s*32+lane
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane == 0) {
-            S[gi] = (amax != 0.0f) ? d : 0.0f;
-            T[gi] = sum;
-        }
-    }
+    for (int64_t gi = warp; gi < groups; gi += nwarps)
+        pq2::quantize_group_warp(x + gi * 128, lane, qp + gi * 128, S + gi, T + gi);
 }
 
 __global__ void __launch_bounds__(256) pack_kernel(const int8_t* __restrict__ tern,
