@@ -72,6 +72,39 @@ bool device_info(DeviceInfo* out) {
     return true;
 }
 
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(ptr);
+    }();
+    return fn;
+}
+}  // namespace
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                    uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_ctl(pq2::DevCtl* ctl) {
     DeviceInfo d;
     if (!device_info(&d)) return false;
@@ -183,7 +216,8 @@ size_t pq2_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
     if (check_nk(N, K) != PQ2_OK || M < 1) return SIZE_MAX;
     switch (op) {
         case PQ2_OP_GEMV: return M == 1 ? 0 : SIZE_MAX;
-        case PQ2_OP_SMALL: return (M >= 2 && M <= 16) ? 0 : SIZE_MAX;
+        case PQ2_OP_SMALL:
+            return (M >= 2 && M <= 16) ? pq2h::small_workspace_bytes(M, N, K) : SIZE_MAX;
         case PQ2_OP_PREFILL: return 0;
         case PQ2_OP_MATMUL: {
             if (M == 1) return 0;  // fused quantise + GEMV, no scratch
@@ -211,9 +245,9 @@ pq2_status pq2_gemm_small(const int8_t* qp, const float* S, const int32_t* T,
     Ctx c;
     s = get_ctx(&c);
     if (s != PQ2_OK) return s;
-    return cuda_status(pq2h::launch_simple(qp, S, T, codes, static_cast<const __half*>(ws_f16), y,
-                                           nullptr, M, N, K, static_cast<cudaStream_t>(stream),
-                                           c.ctl, c.dev));
+    return cuda_status(pq2h::launch_small(qp, S, T, codes, static_cast<const __half*>(ws_f16), y,
+                                          nullptr, M, N, K, workspace,
+                                          static_cast<cudaStream_t>(stream), c.ctl, c.dev));
 }
 
 pq2_status pq2_gemm_prefill(const int8_t* qp, const float* S, const int32_t* T,
@@ -293,6 +327,9 @@ pq2_status pq2_group_dots(int op, const int8_t* qp, const int32_t* T, const uint
         return cuda_status(
             pq2h::launch_gemv(nullptr, qp, nullptr, T, codes, nullptr, nullptr, dots, N, K, st,
                               c.ctl, c.dev));
+    if (op == PQ2_OP_SMALL)
+        return cuda_status(pq2h::launch_small(qp, nullptr, T, codes, nullptr, nullptr, dots, M, N,
+                                              K, workspace, st, c.ctl, c.dev));
     return cuda_status(pq2h::launch_simple(qp, nullptr, T, codes, nullptr, nullptr, dots, M, N,
                                            K, st, c.ctl, c.dev));
 }

@@ -4,12 +4,19 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "pq2_common.cuh"
 
 namespace pq2h {
+
+// 2-D tiled tensor map (no swizzle, zero fill out of range): dims
+// {inner, outer} elements, row pitch in bytes, box {box_inner, box_outer}.
+// The driver's encoder is reached through the runtime's entry-point query.
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                    uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer);
 
 cudaError_t launch_quantize(const __half* x, int8_t* qp, float* S, int32_t* T, int64_t M,
                             int64_t K, cudaStream_t st, const pq2::DevCtl& ctl,
@@ -24,6 +31,14 @@ cudaError_t launch_pack(const int8_t* tern, uint8_t* codes, int64_t N, int64_t K
 cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const int32_t* T,
                         const uint8_t* codes, const __half* ws, float* y, int32_t* dots, int64_t N,
                         int64_t K, cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev);
+
+// 2 <= M <= 16: tensor-core (mma.sync e4m3) kernel, split-K reduced in order.
+// workspace: small_workspace_bytes(M, N, K) bytes.
+size_t small_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
+                         const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
+                         int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
+                         const DeviceInfo& dev);
 
 // Plain warp-per-output kernel, any M (first correct path for M > 1).
 cudaError_t launch_simple(const int8_t* qp, const float* S, const int32_t* T,
