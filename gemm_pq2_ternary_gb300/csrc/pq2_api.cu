@@ -1,6 +1,7 @@
 // The C ABI (include/pq2.h): host-side argument checks, per-device set-up,
 // routing to the kernels, and the device error word.
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -49,6 +50,15 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 namespace pq2h {
 
+// Suspend-time hint for mbarrier waits, PQ2_WAIT_HINT_NS (read once; tuning).
+unsigned wait_hint_ns() {
+    static const unsigned v = [] {
+        const char* e = std::getenv("PQ2_WAIT_HINT_NS");
+        return e && *e ? static_cast<unsigned>(std::strtoul(e, nullptr, 10)) : 0u;
+    }();
+    return v;
+}
+
 bool device_info(DeviceInfo* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
@@ -93,7 +103,8 @@ EncodeTiledFn encode_tiled_fn() {
 }  // namespace
 
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                    uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+                    uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+                    bool swizzle128) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {inner, outer};
@@ -101,7 +112,8 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, 
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -111,6 +123,7 @@ bool make_ctl(pq2::DevCtl* ctl) {
     ctl->err = d.err;
     ctl->wait_limit_ns = g_wait_limit_ns.load();
     ctl->debug_skip_stage = g_debug_skip_stage.load();
+    ctl->wait_hint_ns = wait_hint_ns();
     return true;
 }
 
@@ -218,7 +231,7 @@ size_t pq2_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
         case PQ2_OP_GEMV: return M == 1 ? 0 : SIZE_MAX;
         case PQ2_OP_SMALL:
             return (M >= 2 && M <= 16) ? pq2h::small_workspace_bytes(M, N, K) : SIZE_MAX;
-        case PQ2_OP_PREFILL: return 0;
+        case PQ2_OP_PREFILL: return pq2h::prefill_workspace_bytes(M, N, K);
         case PQ2_OP_MATMUL: {
             if (M == 1) return 0;  // fused quantise + GEMV, no scratch
             const size_t G = static_cast<size_t>(K / 128);
@@ -260,12 +273,13 @@ pq2_status pq2_gemm_prefill(const int8_t* qp, const float* S, const int32_t* T,
     if (M > (int64_t(1) << 31) - 1) return PQ2_ERR_UNSUPPORTED_SHAPE;
     const size_t need = pq2_workspace_bytes(PQ2_OP_PREFILL, M, N, K);
     if (need > 0 && (!workspace || workspace_bytes < need)) return PQ2_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PQ2_ERR_MISALIGNED;
     Ctx c;
     s = get_ctx(&c);
     if (s != PQ2_OK) return s;
-    return cuda_status(pq2h::launch_simple(qp, S, T, codes, static_cast<const __half*>(ws_f16), y,
-                                           nullptr, M, N, K, static_cast<cudaStream_t>(stream),
-                                           c.ctl, c.dev));
+    return cuda_status(pq2h::launch_prefill(qp, S, T, codes, static_cast<const __half*>(ws_f16), y,
+                                            nullptr, M, N, K, workspace,
+                                            static_cast<cudaStream_t>(stream), c.ctl, c.dev));
 }
 
 pq2_status pq2_matmul(const void* x_f16, const uint8_t* codes, const void* ws_f16, float* y,
@@ -330,8 +344,9 @@ pq2_status pq2_group_dots(int op, const int8_t* qp, const int32_t* T, const uint
     if (op == PQ2_OP_SMALL)
         return cuda_status(pq2h::launch_small(qp, nullptr, T, codes, nullptr, nullptr, dots, M, N,
                                               K, workspace, st, c.ctl, c.dev));
-    return cuda_status(pq2h::launch_simple(qp, nullptr, T, codes, nullptr, nullptr, dots, M, N,
-                                           K, st, c.ctl, c.dev));
+    // the prefill path needs S only to prepare its token planes
+    return cuda_status(pq2h::launch_prefill(qp, nullptr, T, codes, nullptr, nullptr, dots, M, N,
+                                            K, workspace, st, c.ctl, c.dev));
 }
 
 pq2_status pq2_last_device_error(void* stream) {

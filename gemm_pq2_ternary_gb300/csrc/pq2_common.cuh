@@ -25,6 +25,7 @@ enum : unsigned {
 struct DevCtl {
     unsigned* err;          // device error word (never null)
     unsigned long long wait_limit_ns;
+    unsigned wait_hint_ns;  // suspend-time hint of mbarrier try_wait (0 = none)
     int debug_skip_stage;   // >= 0: producer withholds that stage (timeout tests)
 };
 
@@ -60,17 +61,27 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
-// try_wait with a suspend-time hint: the thread sleeps until the phase
-// completes or ~20 us pass, instead of spinning on the issue slots.
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// try_wait; with a non-zero suspend-time hint the thread may sleep until the
+// phase completes or the hint (ns) passes.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, unsigned hint_ns) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
-        : "memory");
+    if (hint_ns) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+    }
     return ok != 0;
 }
 
@@ -81,10 +92,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   const DevCtl& ctl,
                                                   volatile int* abort_flag = nullptr) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, ctl.wait_hint_ns)) return true;
     unsigned long long t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity, ctl.wait_hint_ns)) return true;
         if ((i & 3u) == 0) {
             if (abort_flag && *abort_flag) return false;
             if (globaltimer_ns() - t0 > ctl.wait_limit_ns) {

@@ -12,11 +12,13 @@
 
 namespace pq2h {
 
-// 2-D tiled tensor map (no swizzle, zero fill out of range): dims
-// {inner, outer} elements, row pitch in bytes, box {box_inner, box_outer}.
-// The driver's encoder is reached through the runtime's entry-point query.
+// 2-D tiled tensor map (zero fill out of range): dims {inner, outer}
+// elements, row pitch in bytes, box {box_inner, box_outer}; swizzle128 =
+// 128-byte swizzle (box rows of exactly 128 bytes), else none.  The driver's
+// encoder is reached through the runtime's entry-point query.
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                    uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer);
+                    uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+                    bool swizzle128);
 
 cudaError_t launch_quantize(const __half* x, int8_t* qp, float* S, int32_t* T, int64_t M,
                             int64_t K, cudaStream_t st, const pq2::DevCtl& ctl,
@@ -39,6 +41,13 @@ cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, con
                          const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
                          int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                          const DeviceInfo& dev);
+
+// Any M: tcgen05 tensor-core kernel (token planes prepared in the workspace).
+size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
+                           const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
+                           int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
+                           const DeviceInfo& dev);
 
 // Plain warp-per-output kernel, any M (first correct path for M > 1).
 cudaError_t launch_simple(const int8_t* qp, const float* S, const int32_t* T,

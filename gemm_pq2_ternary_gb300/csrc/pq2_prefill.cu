@@ -1,0 +1,502 @@
+// Prompt-processing matmul, any M (pq2_gemm_prefill), on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory).
+//
+// The method is the pages' prefill kernel ("Making a ternary reasoning model
+// fast in vLLM", page "From CUDA to Triton and Gluon", section "Prompt
+// processing: check configuration and launch costs"): 2-D output tiles,
+// per-group integer products from the planes of the codes, the -sum(q)
+// correction and the same per-group fp32 dequantise-accumulate order as the
+// M = 1 path.
+//
+// GB300 design.  tcgen05 has no int8 kind on sm_103a; kind::f8f6f4 with e4m3
+// operands is exact here:
+//  * weights (B operand, N = 128 rows per tile): plane s of code byte b is
+//    (byte >> 2s) & 3, stored as the e4m3 byte itself = c * 2^-9 (e4m3 bytes
+//    below 16 are exactly byte * 2^-9);
+//  * tokens (A operand, M = 128 rows per tile): q = 16h + l with h in
+//    [-8,7], l in [0,15]; 16h and l are exact e4m3 values, prepared once per
+//    call in two planes (hi, lo) by a small kernel;
+//  * two MMAs per k-step (hi, lo) accumulate into the same fp32 D in tensor
+//    memory: D = 2^-9 * sum(code * q), an exact small multiple of 2^-9.
+//  The k order inside a group is the plane order of the activations: k-step
+//  s of a group (32 values) is plane s, so a weight row of B is
+//  [plane0 bytes 0..31 | plane1 | plane2 | plane3], written by the expansion
+//  warps straight into the 128-byte-swizzled K-major shared layout.
+//
+// Per CTA (persistent over 128x128 output tiles, one per SM):
+//   warp 0      TMA producer: per group, the hi and lo token tiles
+//               (128 x 128 B, 128B swizzle) and the code tile (128 x 32 B)
+//   warp 1      MMA issuer (one thread): 4 k-steps x (hi, lo) per group into
+//               one of two D buffers, then tcgen05.commit
+//   warps 2-5   expansion: one weight row per thread, codes -> e4m3 B tile;
+//               also the group's weight scales for the epilogue
+//   warps 6-13  epilogue: per group, dot = D*512 - t (exact), then
+//               acc += dot * s * ws with the running fp32 accumulator in
+//               tensor memory; finally acc -> y.
+// Every mbarrier wait is bounded (device error word on expiry).
+#include "pq2_internal.h"
+
+namespace {
+
+constexpr int kTileM = 128;  // tokens per tile (MMA M)
+constexpr int kTileN = 128;  // weight rows per tile (MMA N)
+constexpr int kStages = 4;
+constexpr int kThreads = 14 * 32;
+constexpr int kEpiWarp0 = 6;
+constexpr uint32_t kTmemCols = 512;  // D0 [0,128), D1 [128,256), acc [256,384)
+
+constexpr uint32_t kATileBytes = kTileM * 128;   // one group of 128 token rows
+constexpr uint32_t kBTileBytes = kTileN * 128;   // expanded weight rows
+constexpr uint32_t kCTileBytes = kTileN * 32;    // raw code rows
+constexpr uint32_t kStageBytes = 2 * kATileBytes + kBTileBytes + kCTileBytes;  // 53248
+
+struct PrefillParams {
+    CUtensorMap tm_ahi;    // e4m3 [M][K], box {128, 128}, 128B swizzle
+    CUtensorMap tm_alo;
+    CUtensorMap tm_codes;  // uint8 [N][K/4], box {32, 128}
+    const float2* st;      // [G][M] (s, t)
+    const __half* ws;      // [N][G]
+    float* y;              // [M][N]
+    int32_t* dots;         // debug: [M][N][G]
+    int M, N, K, G;
+    int m_tiles, n_tiles;
+    pq2::DevCtl ctl;
+};
+
+// ---------------------------------------------------------------------------
+// token planes: q = 16h + l -> e4m3(16h), e4m3(l); (s, t) transposed to [G][M]
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
+    uint32_t lo, hi;
+    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
+        : "=r"(lo) : "f"(v0), "f"(v1));
+    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
+        : "=r"(hi) : "f"(v2), "f"(v3));
+    return lo | (hi << 16);
+}
+
+__global__ void __launch_bounds__(256) token_planes_kernel(const int8_t* __restrict__ qp,
+                                                           const float* __restrict__ S,
+                                                           const int32_t* __restrict__ T,
+                                                           uint32_t* __restrict__ ahi,
+                                                           uint32_t* __restrict__ alo,
+                                                           float2* __restrict__ st, int64_t M,
+                                                           int64_t K) {
+    pq2::pdl_wait();
+    pq2::pdl_launch_dependents();
+    const int64_t words = M * K / 4;
+    const int64_t G = K / 128;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < words;
+         i += stride) {
+        const uint32_t qw = reinterpret_cast<const uint32_t*>(qp)[i];
+        float h[4], l[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int q = static_cast<int8_t>((qw >> (8 * b)) & 0xFFu);
+            h[b] = static_cast<float>(16 * (q >> 4));  // 16 * floor(q / 16)
+            l[b] = static_cast<float>(q & 15);         // q - 16 * floor(q / 16)
+        }
+        ahi[i] = e4m3x4(h[0], h[1], h[2], h[3]);
+        alo[i] = e4m3x4(l[0], l[1], l[2], l[3]);
+    }
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < M * G;
+         i += stride) {
+        const int64_t m = i / G, g = i - m * G;
+        st[g * M + m] = make_float2(S ? S[i] : 0.0f, static_cast<float>(T[i]));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 helpers
+// ---------------------------------------------------------------------------
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(1) << 16;             // leading offset (unused here)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;     // stride offset
+    d |= static_cast<uint64_t>(1) << 46;             // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;             // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f8f6f4: D f32, A and B e4m3, both K-major.
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) |
+                            (static_cast<uint32_t>(kTileN >> 3) << 17) |
+                            (static_cast<uint32_t>(kTileM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            pq2::smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+            taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+        "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+        "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+        "f"(v[29]), "f"(v[30]), "f"(v[31]));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// main kernel
+// ---------------------------------------------------------------------------
+template <bool DOTS>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t full[kStages];   // TMA bytes of a stage landed
+    __shared__ uint64_t bready[kStages]; // expanded weight tile written (4 warps)
+    __shared__ uint64_t empty[kStages];  // MMAs of the stage done (commit)
+    __shared__ uint64_t dfull[2];        // D buffer holds a finished group (commit)
+    __shared__ uint64_t dempty[2];       // epilogue done with a D buffer (8 warps)
+    __shared__ float ws_sm[2][kTileN];   // weight scales per D buffer
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const uint32_t base = pq2::smem_u32(smem);
+    uint8_t* stage0 = smem + ((1024 - (base & 1023)) & 1023);
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            pq2::mbar_init(&full[i], 1);
+            pq2::mbar_init(&bready[i], 4);
+            pq2::mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            pq2::mbar_init(&dfull[i], 1);
+            pq2::mbar_init(&dempty[i], 8);
+        }
+        abort_flag = 0;
+        pq2::fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         pq2::smem_u32(&tmem_base)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pq2::pdl_wait();
+    pq2::pdl_launch_dependents();
+
+    const uint32_t tmem = tmem_base;
+    const int G = p.G;
+    const int n_tiles_total = p.m_tiles * p.n_tiles;
+    volatile int* abort_v = &abort_flag;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            int it = 0;  // global group counter (stage = it % kStages)
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
+                const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+                for (int g = 0; g < G; ++g, ++it) {
+                    const int s = it % kStages;
+                    if (it >= kStages &&
+                        !pq2::mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1, p.ctl, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    if (it == p.ctl.debug_skip_stage) continue;
+                    uint8_t* st = stage0 + static_cast<size_t>(s) * kStageBytes;
+                    pq2::mbar_arrive_expect_tx(&full[s], kStageBytes - kBTileBytes);
+                    pq2::tma_load_2d(st, &p.tm_ahi, g * 128, mt * kTileM, &full[s]);
+                    pq2::tma_load_2d(st + kATileBytes, &p.tm_alo, g * 128, mt * kTileM, &full[s]);
+                    pq2::tma_load_2d(st + 2 * kATileBytes + kBTileBytes, &p.tm_codes, g * 32,
+                                     nt * kTileN, &full[s]);
+                }
+            }
+            // drain: every armed stage must have landed before exit
+            const int issued = it;
+            for (int s = 0; s < kStages; ++s) {
+                if (issued <= s) continue;
+                int last = s + ((issued - 1 - s) / kStages) * kStages;
+                if (last == p.ctl.debug_skip_stage) last -= kStages;
+                if (last >= 0) pq2::mbar_wait_bounded(&full[s], (last / kStages) & 1, p.ctl);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
+                for (int g = 0; g < G; ++g, ++it) {
+                    const int s = it % kStages;
+                    const int db = it & 1;
+                    if (!pq2::mbar_wait_bounded(&bready[s], (it / kStages) & 1, p.ctl, abort_v) ||
+                        (it >= 2 &&
+                         !pq2::mbar_wait_bounded(&dempty[db], ((it >> 1) - 1) & 1, p.ctl, abort_v))) {
+                        ok = false;
+                        *abort_v = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = pq2::smem_u32(stage0 + static_cast<size_t>(s) * kStageBytes);
+                    const uint32_t d_tmem = tmem + db * 128;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t bdesc = sw128_desc(st + 2 * kATileBytes + 32 * k);
+                        mma_f8(d_tmem, sw128_desc(st + 32 * k), bdesc, k > 0);
+                        mma_f8(d_tmem, sw128_desc(st + kATileBytes + 32 * k), bdesc, 1);
+                    }
+                    mma_commit(&empty[s]);
+                    mma_commit(&dfull[db]);
+                }
+            }
+            // no MMA may still be running when tensor memory is released
+            if (it > 0)
+                pq2::mbar_wait_bounded(&dfull[(it - 1) & 1], ((it - 1) >> 1) & 1, p.ctl);
+        }
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------ expansion ------------------------------
+        const int r = (warp - 2) * 32 + lane;  // weight row within the tile
+        const int half = (lane >> 2) & 1;      // conflict-free order of the 2 loads
+        int it = 0;
+        bool failed = false;
+        for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x) {
+            const int nt = tile / p.m_tiles;
+            const int n = nt * kTileN + r;
+            for (int g = 0; g < G; ++g, ++it) {
+                const int s = it % kStages;
+                const int db = it & 1;
+                // weight scale of this row for the epilogue (prefetched before the waits)
+                const float wsv = (!DOTS && n < p.N) ? __half2float(p.ws[static_cast<size_t>(n) * G + g]) : 0.0f;
+                if (!failed &&
+                    (!pq2::mbar_wait_bounded(&full[s], (it / kStages) & 1, p.ctl, abort_v) ||
+                     (it >= 2 &&
+                      !pq2::mbar_wait_bounded(&dempty[db], ((it >> 1) - 1) & 1, p.ctl, abort_v)))) {
+                    failed = true;
+                    *abort_v = 1;
+                }
+                if (!failed) {
+                    uint8_t* st = stage0 + static_cast<size_t>(s) * kStageBytes;
+                    const uint8_t* crow = st + 2 * kATileBytes + kBTileBytes + r * 32;
+                    const uint4 ca = *reinterpret_cast<const uint4*>(crow + 16 * half);
+                    const uint4 cb = *reinterpret_cast<const uint4*>(crow + 16 * (half ^ 1));
+                    const uint32_t w[8] = {half ? cb.x : ca.x, half ? cb.y : ca.y,
+                                           half ? cb.z : ca.z, half ? cb.w : ca.w,
+                                           half ? ca.x : cb.x, half ? ca.y : cb.y,
+                                           half ? ca.z : cb.z, half ? ca.w : cb.w};
+                    uint8_t* brow = st + 2 * kATileBytes + r * 128;
+#pragma unroll
+                    for (int pl = 0; pl < 4; ++pl) {
+#pragma unroll
+                        for (int hc = 0; hc < 2; ++hc) {  // 16-byte chunk 2*pl + hc
+                            uint4 v;
+                            v.x = (w[4 * hc + 0] >> (2 * pl)) & 0x03030303u;
+                            v.y = (w[4 * hc + 1] >> (2 * pl)) & 0x03030303u;
+                            v.z = (w[4 * hc + 2] >> (2 * pl)) & 0x03030303u;
+                            v.w = (w[4 * hc + 3] >> (2 * pl)) & 0x03030303u;
+                            const int chunk = (2 * pl + hc) ^ (r & 7);
+                            *reinterpret_cast<uint4*>(brow + 16 * chunk) = v;
+                        }
+                    }
+                    ws_sm[db][r] = wsv;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                __syncwarp();
+                if (lane == 0) pq2::mbar_arrive(&bready[s]);
+            }
+        }
+    } else {
+        // ------------------------------ epilogue ------------------------------
+        const int ew = warp - kEpiWarp0;  // 0..7
+        const int quad = warp & 3;        // TMEM lane quadrant of this warp
+        const int col0 = (ew >> 2) * 64;  // two warps per quadrant: columns [0,64), [64,128)
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        int it = 0;
+        bool failed = false;
+        for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x) {
+            const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+            const int m = mt * kTileM + quad * 32 + lane;  // token row of this thread
+            const bool mvalid = m < p.M;
+            float2 stv = (mvalid && !failed) ? p.st[m] : make_float2(0.0f, 0.0f);  // group 0
+            for (int g = 0; g < G; ++g, ++it) {
+                const int db = it & 1;
+                // prefetch next group's (s, t) for this token
+                float2 st_next = make_float2(0.0f, 0.0f);
+                if (mvalid && g + 1 < G) st_next = p.st[static_cast<size_t>(g + 1) * p.M + m];
+                if (!failed &&
+                    !pq2::mbar_wait_bounded(&dfull[db], (it >> 1) & 1, p.ctl, abort_v)) {
+                    failed = true;
+                    *abort_v = 1;
+                }
+                if (!failed) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < 64; c += 32) {
+                        float d[32];
+                        tmem_ld32(tmem + lane_off + db * 128 + col0 + c, d);
+                        float acc[32];
+                        if (g > 0) tmem_ld32(tmem + lane_off + 256 + col0 + c, acc);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float dot = fmaf(d[j], 512.0f, -stv.y);  // exact integer
+                            if (DOTS) {
+                                const int n = nt * kTileN + col0 + c + j;
+                                if (mvalid && n < p.N)
+                                    p.dots[(static_cast<size_t>(m) * p.N + n) * G + g] =
+                                        static_cast<int>(dot);
+                            } else {
+                                const float term = dot * stv.x;
+                                acc[j] = g > 0 ? fmaf(term, ws_sm[db][col0 + c + j], acc[j])
+                                               : term * ws_sm[db][col0 + c + j];
+                            }
+                        }
+                        if (!DOTS) tmem_st32(tmem + lane_off + 256 + col0 + c, acc);
+                    }
+                    if (!DOTS) tmem_wait_st();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) pq2::mbar_arrive(&dempty[db]);
+                stv = st_next;
+            }
+            // tile done: acc -> y
+            if (!DOTS && !failed) {
+                tc_fence_after();
+                const int nb = nt * kTileN + col0;
+#pragma unroll
+                for (int c = 0; c < 64; c += 32) {
+                    float acc[32];
+                    tmem_ld32(tmem + lane_off + 256 + col0 + c, acc);
+                    tmem_wait_ld();
+                    if (mvalid) {
+                        float* yrow = p.y + static_cast<size_t>(m) * p.N + nb + c;
+                        if (nb + c + 32 <= p.N && (p.N & 3) == 0) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4)
+                                *reinterpret_cast<float4*>(yrow + j) =
+                                    make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (nb + c + j < p.N) yrow[j] = acc[j];
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // teardown: every role is done with tensor memory
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols));
+}
+
+size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+namespace pq2h {
+
+size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    (void)N;
+    return 2 * align256(static_cast<size_t>(M) * K) + align256(static_cast<size_t>(M) * (K / 128) * 8);
+}
+
+cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
+                           const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
+                           int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
+                           const DeviceInfo& dev) {
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    uint8_t* ahi = w;
+    uint8_t* alo = w + align256(static_cast<size_t>(M) * K);
+    float2* stv = reinterpret_cast<float2*>(w + 2 * align256(static_cast<size_t>(M) * K));
+    {
+        const int64_t words = M * K / 4;
+        const int64_t want = (words + 255) / 256;
+        const int grid = static_cast<int>(want < dev.num_sms * 16 ? want : dev.num_sms * 16);
+        cudaError_t e = launch(token_planes_kernel, dim3(grid), dim3(256), 0, st, true, qp, S, T,
+                               reinterpret_cast<uint32_t*>(ahi), reinterpret_cast<uint32_t*>(alo),
+                               stv, M, K);
+        if (e != cudaSuccess) return e;
+    }
+    PrefillParams p = {};
+    if (!encode_tmap_2d(&p.tm_ahi, CU_TENSOR_MAP_DATA_TYPE_UINT8, ahi, static_cast<uint64_t>(K),
+                        static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128u, kTileM, true) ||
+        !encode_tmap_2d(&p.tm_alo, CU_TENSOR_MAP_DATA_TYPE_UINT8, alo, static_cast<uint64_t>(K),
+                        static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128u, kTileM, true) ||
+        !encode_tmap_2d(&p.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes,
+                        static_cast<uint64_t>(K / 4), static_cast<uint64_t>(N),
+                        static_cast<uint64_t>(K / 4), 32u, kTileN, false))
+        return cudaErrorInvalidValue;
+    p.st = stv;
+    p.ws = ws;
+    p.y = y;
+    p.dots = dots;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.G = static_cast<int>(K / 128);
+    p.m_tiles = static_cast<int>((M + kTileM - 1) / kTileM);
+    p.n_tiles = static_cast<int>((N + kTileN - 1) / kTileN);
+    p.ctl = ctl;
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int grid = tiles < dev.num_sms ? tiles : dev.num_sms;
+    const size_t smem = 1024 + static_cast<size_t>(kStages) * kStageBytes;
+    auto kern = dots ? prefill_kernel<true> : prefill_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch(kern, dim3(grid), dim3(kThreads), smem, st, true, p);
+}
+
+}  // namespace pq2h

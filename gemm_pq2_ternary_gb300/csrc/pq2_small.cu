@@ -40,8 +40,8 @@
 
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kTilesPerWarp = 6;                       // register accumulators per warp
+constexpr int kConsumerWarps = 8;
+constexpr int kTilesPerWarp = 3;                       // register accumulators per warp
 constexpr int kBatchTiles = kConsumerWarps * kTilesPerWarp;
 constexpr int kFragBytesPerGroupTile = 4 * 2 * 32 * 8;  // planes x (hi,lo) x lanes x 8 B
 
@@ -102,6 +102,7 @@ struct SmallParams {
     uint32_t codes_stage_bytes;  // batch_rows * GC * 32
     uint32_t qp_stage_bytes;     // 16 * GC * 128
     int max_groups_per_split;
+    int swizzle;     // codes tiles stored with the 128-byte TMA swizzle (GC == 4)
     pq2::DevCtl ctl;
 };
 
@@ -125,7 +126,12 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
     float2* st_sm = reinterpret_cast<float2*>(smem + st_off);  // [groups][16] (s, t)
     const int ws_off = st_off + p.max_groups_per_split * 16 * 8;
     __half* ws_sm = reinterpret_cast<__half*>(smem + ws_off);  // [batch_rows][groups]
-    uint8_t* ring = smem + ((ws_off + p.batch_rows * p.max_groups_per_split * 2 + 127) & ~127);
+    // stages start on 1024-byte boundaries (the swizzle pattern follows the
+    // shared-memory address bits)
+    const uint32_t base_addr = pq2::smem_u32(smem);
+    const uint32_t ring_addr =
+        (base_addr + ws_off + p.batch_rows * p.max_groups_per_split * 2 + 1023) & ~1023u;
+    uint8_t* ring = smem + (ring_addr - base_addr);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -209,13 +215,24 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
         // this batch's weight scales, [row][group of the split]
         if (!DOTS) {
             pq2::named_bar_sync(1, kCT);  // previous batch done with ws_sm
+            // one warp per row, lanes over the split's groups, 4 rows in flight
             const int rows = ntile * 16;
-            for (int i = tid; i < rows * n_groups; i += kCT) {
-                const int r = i / n_groups, gl = i - r * n_groups;
-                const int n = tb0 * 16 + r;
-                ws_sm[r * p.max_groups_per_split + gl] =
-                    n < p.N ? p.ws[static_cast<size_t>(n) * p.G + g0 + gl] : __float2half(0.0f);
-            }
+            for (int r0 = warp * 4; r0 < rows; r0 += kConsumerWarps * 4)
+                for (int c0 = 0; c0 < n_groups; c0 += 32) {
+                    const int gl = c0 + lane;
+                    __half v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int n = tb0 * 16 + r0 + u;
+                        v[u] = (r0 + u < rows && n < p.N && gl < n_groups)
+                                   ? p.ws[static_cast<size_t>(n) * p.G + g0 + gl]
+                                   : __float2half(0.0f);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (r0 + u < rows && gl < n_groups)
+                            ws_sm[(r0 + u) * p.max_groups_per_split + gl] = v[u];
+                }
         }
         pq2::named_bar_sync(1, kCT);
         float acc[kTilesPerWarp][NT][4];
@@ -242,20 +259,24 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
             if (!failed) {
                 // B fragments of this stage's groups from the staged activations:
                 // frag word ((((gl*NT + nt)*4 + s)*2 + h)*32 + lane)*2 + r
-                const int nwords = gcs * NT * 4 * 32 * 2;  // (h stripped)
+                // one thread per activation word, in the staged row-major order
+                // qst[m][gl*32 + s*8 + 2*tid + r] (conflict-free reads)
+                const int words_per_row = p.GC * 32;
+                const int nwords = NT * 8 * words_per_row;
                 for (int w = tid; w < nwords; w += kCT) {
-                    const int r = w & 1;
-                    const int ln = (w >> 1) & 31;
-                    const int s = (w >> 6) & 3;
-                    const int gnt = w >> 8;  // gl * NT + nt
-                    const int nt = gnt % NT;
-                    const int gl = gnt / NT;
-                    const int m = nt * 8 + (ln >> 2);
-                    const uint32_t qw = *reinterpret_cast<const uint32_t*>(
-                        qst + m * (p.GC * 128) + gl * 128 + s * 32 + 8 * (ln & 3) + 4 * r);
+                    const int m = w / words_per_row;
+                    const int c = w - m * words_per_row;
+                    const int gl = c >> 5;
+                    if (gl >= gcs) continue;
+                    const int s = (c >> 3) & 3;
+                    const int tq2 = (c >> 1) & 3;
+                    const int r = c & 1;
+                    const uint32_t qw = reinterpret_cast<const uint32_t*>(qst)[w];
                     uint32_t hw, lw;
                     split_word(qw, (s & 1) != 0, &hw, &lw);
-                    const int base = ((gnt * 4 + s) * 2) * 64 + ln * 2 + r;
+                    const int nt = m >> 3;
+                    const int ln = ((m & 7) << 2) | tq2;
+                    const int base = (((gl * NT + nt) * 4 + s) * 2) * 64 + ln * 2 + r;
                     fst[base] = hw;
                     fst[base + 64] = lw;
                 }
@@ -288,26 +309,54 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
                         s_tok[nt][1] = st.z;
                         t_tok[nt][1] = st.w;
                     }
+                    // A fragments of this warp's tiles for this group
+                    uint32_t a[kTilesPerWarp][4][4];
+                    bool tv[kTilesPerWarp];
 #pragma unroll
                     for (int j = 0; j < kTilesPerWarp; ++j) {
                         const int tb = warp + kConsumerWarps * j;
-                        if (tb >= ntile) break;
-                        const int ra = tb * 16 + gid;
-                        const uint2 c0 = *reinterpret_cast<const uint2*>(
-                            cst + static_cast<size_t>(ra) * p.GC * 32 + gl * 32 + 8 * tq);
-                        const uint2 c1 = *reinterpret_cast<const uint2*>(
-                            cst + static_cast<size_t>(ra + 8) * p.GC * 32 + gl * 32 + 8 * tq);
+                        tv[j] = tb < ntile;
+                        const int ra = (tv[j] ? tb : 0) * 16 + gid;
+                        uint32_t oa = static_cast<uint32_t>(ra) * p.GC * 32 + gl * 32 + 8 * tq;
+                        uint32_t ob = oa + 8u * p.GC * 32;
+                        if (p.swizzle) {  // 16-byte chunk index ^= row % 8
+                            oa ^= ((oa >> 7) & 7u) << 4;
+                            ob ^= ((ob >> 7) & 7u) << 4;
+                        }
+                        const uint2 c0 = *reinterpret_cast<const uint2*>(cst + oa);
+                        const uint2 c1 = *reinterpret_cast<const uint2*>(cst + ob);
                         const uint32_t s0x = c0.x >> 4, s0y = c0.y >> 4, s1x = c1.x >> 4,
                                        s1y = c1.y >> 4;
-                        uint32_t a[4][4];
-                        a[0][0] = c0.x & 0x03030303u; a[0][1] = c1.x & 0x03030303u;
-                        a[0][2] = c0.y & 0x03030303u; a[0][3] = c1.y & 0x03030303u;
-                        a[1][0] = c0.x & 0x0C0C0C0Cu; a[1][1] = c1.x & 0x0C0C0C0Cu;
-                        a[1][2] = c0.y & 0x0C0C0C0Cu; a[1][3] = c1.y & 0x0C0C0C0Cu;
-                        a[2][0] = s0x & 0x03030303u;  a[2][1] = s1x & 0x03030303u;
-                        a[2][2] = s0y & 0x03030303u;  a[2][3] = s1y & 0x03030303u;
-                        a[3][0] = s0x & 0x0C0C0C0Cu;  a[3][1] = s1x & 0x0C0C0C0Cu;
-                        a[3][2] = s0y & 0x0C0C0C0Cu;  a[3][3] = s1y & 0x0C0C0C0Cu;
+                        a[j][0][0] = c0.x & 0x03030303u; a[j][0][1] = c1.x & 0x03030303u;
+                        a[j][0][2] = c0.y & 0x03030303u; a[j][0][3] = c1.y & 0x03030303u;
+                        a[j][1][0] = c0.x & 0x0C0C0C0Cu; a[j][1][1] = c1.x & 0x0C0C0C0Cu;
+                        a[j][1][2] = c0.y & 0x0C0C0C0Cu; a[j][1][3] = c1.y & 0x0C0C0C0Cu;
+                        a[j][2][0] = s0x & 0x03030303u;  a[j][2][1] = s1x & 0x03030303u;
+                        a[j][2][2] = s0y & 0x03030303u;  a[j][2][3] = s1y & 0x03030303u;
+                        a[j][3][0] = s0x & 0x0C0C0C0Cu;  a[j][3][1] = s1x & 0x0C0C0C0Cu;
+                        a[j][3][2] = s0y & 0x0C0C0C0Cu;  a[j][3][3] = s1y & 0x0C0C0C0Cu;
+                    }
+                    // MMAs issued tile-interleaved: consecutive MMAs are independent
+                    float d[kTilesPerWarp][NT][4];
+#pragma unroll
+                    for (int j = 0; j < kTilesPerWarp; ++j)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) d[j][nt][e] = 0.0f;
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int j = 0; j < kTilesPerWarp; ++j)
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt)
+                                    if (tv[j]) mma_e4m3(d[j][nt], a[j][s], bf[nt][s][h][0], bf[nt][s][h][1]);
+#pragma unroll
+                    for (int j = 0; j < kTilesPerWarp; ++j) {
+                        if (!tv[j]) continue;
+                        const int ra = (warp + kConsumerWarps * j) * 16 + gid;
                         float wsa = 0.0f, wsb = 0.0f;
                         if (!DOTS) {
                             wsa = __half2float(ws_sm[ra * p.max_groups_per_split + (g - g0)]);
@@ -317,17 +366,11 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
                         const int nb = na + 8;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                            for (int s = 0; s < 4; ++s) {
-                                mma_e4m3(d, a[s], bf[nt][s][0][0], bf[nt][s][0][1]);
-                                mma_e4m3(d, a[s], bf[nt][s][1][0], bf[nt][s][1][1]);
-                            }
                             // exact integer group dots, then the fp32 group term
-                            const float dot0 = fmaf(d[0], 512.0f, -t_tok[nt][0]);
-                            const float dot1 = fmaf(d[1], 512.0f, -t_tok[nt][1]);
-                            const float dot2 = fmaf(d[2], 512.0f, -t_tok[nt][0]);
-                            const float dot3 = fmaf(d[3], 512.0f, -t_tok[nt][1]);
+                            const float dot0 = fmaf(d[j][nt][0], 512.0f, -t_tok[nt][0]);
+                            const float dot1 = fmaf(d[j][nt][1], 512.0f, -t_tok[nt][1]);
+                            const float dot2 = fmaf(d[j][nt][2], 512.0f, -t_tok[nt][0]);
+                            const float dot3 = fmaf(d[j][nt][3], 512.0f, -t_tok[nt][1]);
                             if (DOTS) {
                                 const int m0 = nt * 8 + 2 * tq;
                                 const size_t G = p.G;
@@ -396,7 +439,7 @@ __global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restr
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
 struct SmallPlan {
-    int NT, KS, ctas_per_ks, n_tiles, GC, stages, batch_rows, box_rows;
+    int NT, KS, ctas_per_ks, n_tiles, GC, stages, batch_rows, box_rows, swizzle;
     uint32_t stage_bytes, codes_stage_bytes, qp_stage_bytes;
     int max_groups_per_split;
     size_t smem;
@@ -424,21 +467,22 @@ SmallPlan plan_small(int64_t M, int64_t N, int64_t K, int num_sms) {
     int GC = 4;
     if (GC > pl.max_groups_per_split) GC = pl.max_groups_per_split;
     pl.GC = GC;
+    pl.swizzle = GC == 4 ? 1 : 0;
     pl.codes_stage_bytes = static_cast<uint32_t>(pl.batch_rows * GC * 32);
     pl.qp_stage_bytes = static_cast<uint32_t>(16 * GC * 128);
-    pl.stage_bytes = pl.codes_stage_bytes + pl.qp_stage_bytes +
-                     static_cast<uint32_t>(GC * pl.NT * kFragBytesPerGroupTile);
+    pl.stage_bytes = (pl.codes_stage_bytes + pl.qp_stage_bytes +
+                      static_cast<uint32_t>(GC * pl.NT * kFragBytesPerGroupTile) + 1023u) & ~1023u;
     auto head = [&](int stages) {
         return (16 * static_cast<size_t>(stages) + 16 +
                 static_cast<size_t>(pl.max_groups_per_split) * 16 * 8 +
                 static_cast<size_t>(pl.batch_rows) * pl.max_groups_per_split * 2 + 127) &
                ~static_cast<size_t>(127);
     };
-    int stages = static_cast<int>((208 * 1024 - head(4)) / pl.stage_bytes);
+    int stages = static_cast<int>((206 * 1024 - head(4)) / pl.stage_bytes);
     if (stages > 4) stages = 4;
     if (stages < 2) stages = 2;
     pl.stages = stages;
-    pl.smem = head(stages) + static_cast<size_t>(stages) * pl.stage_bytes;
+    pl.smem = head(stages) + 1024 + static_cast<size_t>(stages) * pl.stage_bytes;
     pl.partial_bytes = KS > 1 ? align256(static_cast<size_t>(KS) * M * N * 4) : 0;
     return pl;
 }
@@ -475,11 +519,11 @@ cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, con
     if (!encode_tmap_2d(&p.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, codes,
                         static_cast<uint64_t>(K / 16), static_cast<uint64_t>(N),
                         static_cast<uint64_t>(K / 4), static_cast<uint32_t>(pl.GC * 8),
-                        static_cast<uint32_t>(pl.box_rows)))
+                        static_cast<uint32_t>(pl.box_rows), pl.swizzle != 0))
         return cudaErrorInvalidValue;
     if (!encode_tmap_2d(&p.tm_qp, CU_TENSOR_MAP_DATA_TYPE_UINT32, qp, static_cast<uint64_t>(K / 4),
                         static_cast<uint64_t>(M), static_cast<uint64_t>(K),
-                        static_cast<uint32_t>(pl.GC * 32), 16u))
+                        static_cast<uint32_t>(pl.GC * 32), 16u, false))
         return cudaErrorInvalidValue;
     p.ws = ws;
     p.S = S;
@@ -501,6 +545,7 @@ cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, con
     p.codes_stage_bytes = pl.codes_stage_bytes;
     p.qp_stage_bytes = pl.qp_stage_bytes;
     p.max_groups_per_split = pl.max_groups_per_split;
+    p.swizzle = pl.swizzle;
     p.ctl = ctl;
     cudaError_t e;
     if (pl.NT == 1)

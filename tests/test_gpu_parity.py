@@ -253,6 +253,7 @@ PREFILL_PROBLEMS = [
     inputs.Problem("prefill_m17", 17, 640, 129, "p343", "outliers", 31),
     inputs.Problem("prefill_m300", 300, 1024, 520, "uniform", "normal", 32),
     inputs.prefill(128),
+    inputs.prefill(4096),
 ]
 
 
@@ -269,9 +270,9 @@ def test_prefill_parity(pq2, prob):
         _check_sampled(pq2, c, y, count=2048)
 
 
-def test_prefill_group_dots_bit_exact(pq2):
+@pytest.mark.parametrize("prob", PREFILL_PROBLEMS[:3], ids=lambda p: p.name)
+def test_prefill_group_dots_bit_exact(pq2, prob):
     from gemm_pq2_ternary_gb300.binding import alloc_workspace, PQ2_OP_PREFILL
-    prob = PREFILL_PROBLEMS[0]
     c = Case(pq2, prob)
     dots = torch.empty((prob.M, prob.N, prob.K // 128), dtype=torch.int32, device=DEV)
     pq2.pq2_group_dots(pq2.PQ2_OP_PREFILL, c.qp_d, c.T_d, c.codes_d, dots,
