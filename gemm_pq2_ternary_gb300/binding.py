@@ -46,6 +46,8 @@ SIGNATURES = {
     "pq2_last_device_error": ([_P], _I),
     "pq2_debug_set_wait_limit_ns": ([_U64], _I),
     "pq2_debug_skip_stage": ([_I], _I),
+    "pq2_gemm_small_noalloc": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _I),
+    "pq2_gemm_small_noalloc_max_scratch": ([], _SZ),
 }
 
 
@@ -163,6 +165,18 @@ def pq2_gemm_prefill(qp, S, T, codes, ws, y, workspace=None, stream=None):
     wp, wb = _ws(workspace)
     _check(_lib.pq2_gemm_prefill(_ptr(qp), _ptr(S), _ptr(T), _ptr(codes), _ptr(ws), _ptr(y),
                                  M, N, K, wp, wb, _stream(stream)), "pq2_gemm_prefill")
+
+
+def pq2_gemm_small_noalloc(qp, S, T, codes, ws, y, stream=None):
+    """pq2_gemm_small without a workspace: its scratch is a fixed device array
+    inside the library (for callers that cannot allocate device memory)."""
+    M, N, K = _mm_shapes(qp, codes)
+    _check(_lib.pq2_gemm_small_noalloc(_ptr(qp), _ptr(S), _ptr(T), _ptr(codes), _ptr(ws), _ptr(y),
+                                       M, N, K, _stream(stream)), "pq2_gemm_small_noalloc")
+
+
+def pq2_gemm_small_noalloc_max_scratch() -> int:
+    return int(_lib.pq2_gemm_small_noalloc_max_scratch())
 
 
 def pq2_matmul(x, codes, ws, y, workspace, stream=None):

@@ -37,6 +37,7 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const
 // 2 <= M <= 16: tensor-core (mma.sync e4m3) kernel, split-K reduced in order.
 // workspace: small_workspace_bytes(M, N, K) bytes.
 size_t small_workspace_bytes(int64_t M, int64_t N, int64_t K);
+size_t small_scratch_bytes(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
                          const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
                          int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,

@@ -501,6 +501,12 @@ cudaError_t launch_main(const SmallParams& p, const SmallPlan& pl, cudaStream_t 
 
 namespace pq2h {
 
+// Exact scratch (split-K partial sums) for this shape on a device with
+// num_sms multiprocessors.
+size_t small_scratch_bytes(int64_t M, int64_t N, int64_t K, int num_sms) {
+    return plan_small(M, N, K, num_sms).partial_bytes;
+}
+
 // Device-independent upper bound: partial sums for the largest split count
 // the planner uses (8).
 size_t small_workspace_bytes(int64_t M, int64_t N, int64_t K) {

@@ -198,6 +198,29 @@ pq2_status pq2_group_dots(int op, const int8_t* qp, const int32_t* T, const uint
 pq2_status pq2_last_device_error(void* stream);
 
 /*
+ * pq2_gemm_small_noalloc -- pq2_gemm_small for callers that cannot allocate
+ * device memory (no allocator of their own, or allocation not allowed where
+ * they run): the same kernel, with its split-K scratch in a fixed 4 MiB
+ * device array that the library holds on every device it is loaded on until
+ * the process exits.  (The pages have no counterpart to this entry point;
+ * it exists for callers of this library.)
+ *   Same operands as pq2_gemm_small, no workspace.  Returns
+ *   PQ2_ERR_WORKSPACE if the shape needs more than
+ *   pq2_gemm_small_noalloc_max_scratch() bytes of scratch on this device.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) and should come before any stream capture.
+ *   All calls share the array: calls that may run at the same time on the
+ *   GPU (unordered streams) race on it.  No cudaMalloc, cudaFree or other
+ *   allocating call is made.
+ */
+pq2_status pq2_gemm_small_noalloc(const int8_t* qp, const float* S, const int32_t* T,
+                                  const uint8_t* codes, const void* ws_f16, float* y,
+                                  int64_t M, int64_t N, int64_t K, void* stream);
+
+/* Size in bytes of the fixed scratch array behind pq2_gemm_small_noalloc. */
+size_t pq2_gemm_small_noalloc_max_scratch(void);
+
+/*
  * pq2_debug_set_wait_limit_ns -- bound on every on-chip barrier wait, in
  * nanoseconds (default 2e9).  For tests of the timeout path only.
  */
