@@ -233,7 +233,7 @@ size_t pq2_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
             return (M >= 2 && M <= 16) ? pq2h::small_workspace_bytes(M, N, K) : SIZE_MAX;
         case PQ2_OP_PREFILL: return pq2h::prefill_workspace_bytes(M, N, K);
         case PQ2_OP_MATMUL: {
-            if (M == 1) return 0;  // fused quantise + GEMV, no scratch
+            if (M == 1 && pq2h::gemv_fused_supported(K)) return 0;  // fused, no scratch
             const size_t G = static_cast<size_t>(K / 128);
             const size_t act = align256(static_cast<size_t>(M) * K) +
                                2 * align256(static_cast<size_t>(M) * G * 4);
@@ -290,7 +290,7 @@ pq2_status pq2_matmul(const void* x_f16, const uint8_t* codes, const void* ws_f1
     if (M < 1 || !x_f16 || !codes || !ws_f16 || !y) return PQ2_ERR_INVALID_ARG;
     const size_t need = pq2_workspace_bytes(PQ2_OP_MATMUL, M, N, K);
     if (need == SIZE_MAX) return PQ2_ERR_UNSUPPORTED_SHAPE;
-    if (M == 1) {
+    if (M == 1 && pq2h::gemv_fused_supported(K)) {
         // fused: the GEMV kernel quantises x itself
         if (!aligned16(x_f16) || !aligned16(codes) || !aligned16(ws_f16) || !aligned16(y))
             return PQ2_ERR_MISALIGNED;

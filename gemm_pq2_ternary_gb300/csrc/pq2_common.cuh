@@ -178,6 +178,33 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
+// Shared-memory accesses by 32-bit shared address (explicit ld/st.shared, so
+// the hot loops never go through generic addressing).  Volatile: they keep
+// their order relative to the mbarrier waits and barriers.
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v));
+}
+
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -186,63 +213,83 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     return v;
 }
 
-// Quantise one 128-value group with one warp ("Making a ternary reasoning
-// model fast in vLLM", page "From CUDA to Triton and Gluon", section "Prompt
-// processing": q int8, s fp32, t int32 per group; section "One token at a
-// time": plane order).  Lane b holds the four values of code byte b
-// (weights 4b..4b+3) and writes plane s at qg[s*32 + b].  amax/127 and x/d
-// are IEEE divisions rounded to nearest, q rounds half to even and is clamped
-// to [-127,127]; an all-zero group gives s = 0, q = 0.
-__device__ __forceinline__ void quantize_group_loaded(uint2 raw, int lane, int8_t* qg,
-                                                      float* s_out, int32_t* t_out) {
-    const __half2 h01 = *reinterpret_cast<const __half2*>(&raw.x);
-    const __half2 h23 = *reinterpret_cast<const __half2*>(&raw.y);
-    const float v[4] = {__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23)};
-    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+// Quotients for the quantiser, each a product with a reciprocal corrected
+// once by its exact remainder r = x - q0*d (one fused multiply-add; the
+// correction step of Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  They are
+// used only on the quantiser's own domain and were checked exhaustively on
+// the GPU against IEEE division there:
+//   * d = amax / 127 from the fp32 value nearest 1/127: bit-identical to the
+//     correctly rounded quotient for all 31,743 positive finite fp16 amax;
+//   * x / d from the hardware reciprocal approximation of d: the same integer
+//     after round-half-even as the correctly rounded quotient, for every fp16
+//     amax and every fp16 x with |x| <= amax (503,856,639 pairs; negative x
+//     mirror positive ones).
+__device__ __forceinline__ float div_corrected(float x, float d, float y) {
+    const float q0 = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q0, d, x);
+    return __fmaf_rn(r, y, q0);
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+constexpr uint32_t kRcp127Bits = 0x3C010204u;  // fp32 nearest 1/127
+
+// Quantise one 128-value group with 8 consecutive lanes of a warp ("Making a
+// ternary reasoning model fast in vLLM", page "From CUDA to Triton and
+// Gluon", section "Prompt processing": q int8, s fp32, t int32 per group;
+// section "One token at a time": plane order).  All 32 lanes call it, four
+// groups at a time; lane j (0..7) of a group holds its values 16j..16j+15 as
+// fp16 (h[0] the first eight), i.e. code bytes 4j..4j+3, and writes plane s
+// of them as one 32-bit word at qg + s*32 + 4j.
+//   amax = max |x| (exact in fp16); d = RN(amax / 127); q = RN-even(x / d)
+// (both divisions by div_corrected, exact on this domain).
+// No clamp is needed: |x| <= amax and d >= (amax/127)(1 - 2^-24) keep
+// |x / d| below 127.5.  T = sum q.  An all-zero group gives d = 0, q = 0.
+// Nothing is written unless `store`; lane j == 0 writes s and t.
+__device__ __forceinline__ void quantize_group8(const uint4 (&h)[2], int j, bool store,
+                                                int8_t* qg, float* s_out, int32_t* t_out) {
+    const __half2* hv = reinterpret_cast<const __half2*>(h);
+    __half2 m = __habs2(hv[0]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float d = __fdiv_rn(amax, 127.0f);
-    int sum = 0;
+    for (int k = 1; k < 8; ++k) m = __hmax2(m, __habs2(hv[k]));
+    float amax = fmaxf(__low2float(m), __high2float(m));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    const bool zero = amax == 0.0f;
+    const float d = div_corrected(amax, 127.0f, __uint_as_float(kRcp127Bits));  // RN(amax/127)
+    const float y = rcp_approx(d);  // d is 0 (unused) or a normal number
+    // q by adding 1.5 * 2^23: the sum lies in [2^23, 2^24), where the add
+    // itself rounds to an integer, half to even, and the low byte of its bit
+    // pattern is q as an int8 (|x / d| < 127.5).
+    uint32_t qb[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float v = (i & 1) ? __high2float(hv[i >> 1]) : __low2float(hv[i >> 1]);
+        const float qf = zero ? 0.0f : div_corrected(v, d, y);
+        qb[i] = __float_as_uint(__fadd_rn(qf, 12582912.0f));
+    }
+    int t = 0;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-        int q = 0;
-        if (amax != 0.0f) {
-            q = __float2int_rn(__fdiv_rn(v[s], d));
-            q = max(-127, min(127, q));
-        }
-        sum += q;
-        qg[s * 32 + lane] = static_cast<int8_t>(q);
+        // bytes 4j..4j+3 of plane s are values s, s+4, s+8, s+12
+        const uint32_t lo = __byte_perm(qb[s], qb[s + 4], 0x0040);
+        const uint32_t hi = __byte_perm(qb[s + 8], qb[s + 12], 0x0040);
+        const uint32_t w = __byte_perm(lo, hi, 0x5410);
+        if (store) *reinterpret_cast<uint32_t*>(qg + s * 32 + 4 * j) = w;
+        t = __dp4a(static_cast<int>(w), 0x01010101, t);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) {
-        *s_out = (amax != 0.0f) ? d : 0.0f;
-        *t_out = sum;
-    }
-}
-
-__device__ __forceinline__ void quantize_group_warp(const __half* xg, int lane, int8_t* qg,
-                                                    float* s_out, int32_t* t_out) {
-    quantize_group_loaded(*reinterpret_cast<const uint2*>(xg + 4 * lane), lane, qg, s_out, t_out);
-}
-
-// All G groups of one activation row by `nwarps` warps (this one is `warp`):
-// the loads of up to 8 groups per warp are issued together before any of
-// them is quantised, so their latencies overlap.
-__device__ __forceinline__ void quantize_row_warps(const __half* x, int G, int warp, int nwarps,
-                                                   int lane, int8_t* q, float* s, int32_t* t) {
-    for (int g0 = warp; g0 < G; g0 += 8 * nwarps) {
-        uint2 raw[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int g = g0 + i * nwarps;
-            if (g < G) raw[i] = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(g) * 128 + 4 * lane);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int g = g0 + i * nwarps;
-            if (g < G) quantize_group_loaded(raw[i], lane, q + g * 128, s + g, t + g);
-        }
+    t += __shfl_xor_sync(0xffffffffu, t, 4);
+    t += __shfl_xor_sync(0xffffffffu, t, 2);
+    t += __shfl_xor_sync(0xffffffffu, t, 1);
+    if (store && j == 0) {
+        *s_out = zero ? 0.0f : d;
+        *t_out = t;
     }
 }
 
@@ -260,6 +307,23 @@ __device__ __forceinline__ int group_codes_dot(const uint32_t (&w)[8], const uin
         a3 = dp4a_us(w[j] & 0xC0C0C0C0u, q[3 * 8 + j], a3);
     }
     return a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6);
+}
+
+// The same group dot times 64, with 64*bias added: the plane sums are
+// combined as ((a0*4 + a1)*4 + a2)*4 + a3 (three shift-adds, exact: plane s
+// is 4^s times its codes) and the bias enters as the start value of the
+// plane-3 sum.  |result| < 2^22 for int8 activations.
+__device__ __forceinline__ int group_codes_dot64(const uint32_t (&w)[8], const uint32_t* q,
+                                                 int bias64) {
+    int a0 = 0, a1 = 0, a2 = 0, a3 = bias64;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        a0 = dp4a_us(w[j] & 0x03030303u, q[0 * 8 + j], a0);
+        a1 = dp4a_us(w[j] & 0x0C0C0C0Cu, q[1 * 8 + j], a1);
+        a2 = dp4a_us(w[j] & 0x30303030u, q[2 * 8 + j], a2);
+        a3 = dp4a_us(w[j] & 0xC0C0C0C0u, q[3 * 8 + j], a3);
+    }
+    return ((a0 * 4 + a1) * 4 + a2) * 4 + a3;
 }
 
 }  // namespace pq2

@@ -1,4 +1,4 @@
-// M = 1 decode matmul (pq2_gemv).
+// M = 1 decode matmul (pq2_gemv, and pq2_matmul's fused M = 1 path).
 //
 // The arithmetic is the pages' single-token algorithm ("Making a ternary
 // reasoning model fast in vLLM", page "From CUDA to Triton and Gluon",
@@ -9,22 +9,36 @@
 // "The win: a program just for one token": no token dimension at all.
 //
 // GB300 layout of the work (not the pages' tiling):
-//  * Persistent CTAs (up to two per SM) each own a contiguous range of output
-//    rows.  Rows are contiguous in memory (codes [N, K/4] row-major), so a
-//    stage of R rows is ONE contiguous chunk: a single 1-D bulk copy (TMA
-//    engine) per stage streams it into a shared-memory ring, completion
-//    tracked by an mbarrier.  One elected producer thread keeps the ring full.
-//  * Consumer thread (rp, gi) always works on the same 128-weight group gi of
-//    the rows it handles, so the group's 128 activation bytes, s and t live
-//    in registers for the whole kernel.  Two rows are processed at once for
-//    instruction-level parallelism.
+//  * One CTA per SM (up to 21 consumer warps), each owning a contiguous
+//    range of output rows.  Many warps per SM hide the latency of the shared
+//    loads and DP4A chains.  Programmatic dependent launch lets each CTA,
+//    before it waits for the preceding kernel, prefetch its own weight rows
+//    into L2 (the weights are not that kernel's output).
+//  * Rows are contiguous in memory (codes [N, K/4] row-major), so a stage of
+//    R rows is ONE contiguous chunk: a single 1-D bulk copy (TMA engine) per
+//    stage moves it into a shared-memory ring, completion tracked by an
+//    mbarrier.  One elected producer thread keeps the ring full.
+//  * Fused path: the fp16 activations reach shared memory by one bulk copy
+//    as well (every CTA reads the same few KB; whole-line bulk requests keep
+//    that hot spot in L2 cheap) and are quantised there (plane order,
+//    per-group S and T, eight lanes per group).  The groups of q sit 160
+//    bytes apart (128 + 32 of padding), which makes the one-time load of
+//    every thread's 128 activation bytes free of bank conflicts.  The
+//    unfused path (pq2_gemv) loads its thread's quantised group straight
+//    from global memory.
+//  * Consumer thread (rp, gi) always works on the same 128-weight group(s)
+//    gi of the rows it handles, so the group's 128 activation bytes, s and t
+//    live in registers for the whole kernel.  Two rows are processed at once
+//    where the stage has them, for instruction-level parallelism.
 //  * Per group: two 16-byte shared loads of codes, 32 mask + 32 DP4A (plane
-//    s masked in place is 4^s times the codes; the four plane sums are
-//    rescaled exactly by shifts), the -sum(q) correction, one fp32 multiply
-//    and one FMA.
+//    s masked in place is 4^s times the codes), three shift-adds that give
+//    64 * (dot(codes, q) - sum(q)) exactly (the -64 sum(q) is the start value
+//    of one plane sum), one conversion and two fp32 multiplies by s/64 and
+//    ws (s/64 is exact, so the product equals dot * s).
 //  * Each consumer warp releases a ring slot on its own (mbarrier arrive);
 //    per-thread group terms go to a shared array and are summed per row, in
-//    a fixed order, once per chunk of rows (one named barrier per chunk).
+//    a fixed order, once per chunk of rows (8 lanes per row, one named
+//    barrier per chunk).
 //  * Every mbarrier wait is bounded; on expiry the block sets the device
 //    error word, stops, and the producer waits for its copies in flight.
 #include <cstdlib>
@@ -46,13 +60,14 @@ struct GemvParams {
     int GT;            // threads per row (each owns GPT groups)
     int RP;            // rows handled side by side
     int TC;            // consumer threads (multiple of 32)
-    int R;             // rows per stage (multiple of 2*RP)
+    int R;             // rows per stage (multiple of RP)
     int stages;
     int chunk_stages;  // stages per row-sum chunk
     int rows_per_cta;
     uint32_t stage_bytes;      // ring slot size (codes + ws, 16-aligned)
     uint32_t codes_row_bytes;  // K / 4
-    int prefetch;              // issue an L2 prefetch of the CTA's weights first
+    uint32_t act_off, red_off, ring_off;  // shared-memory layout
+    int prefetch;              // L2 prefetch of the CTA's weights before the wait
     pq2::DevCtl ctl;
 };
 
@@ -60,45 +75,71 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-constexpr int kMaxThreads = 512 + 32;  // consumers (<= 512) + producer warp
+__device__ __forceinline__ void prefetch_range(const uint8_t* src, size_t bytes) {
+    while (bytes > 0) {
+        const uint32_t b = bytes < 65536u ? static_cast<uint32_t>(bytes) : 65536u;
+        bulk_prefetch_l2(src, b);
+        src += b;
+        bytes -= b;
+    }
+}
+
+// One CTA per SM; many consumer warps hide the shared-memory and DP4A
+// latencies of the group dots (the variant with one group per thread keeps to
+// <= 93 registers at 704 threads).
+constexpr int kMaxConsumersSmall = 672;
+constexpr int kMaxConsumersLarge = 512;
+constexpr uint32_t kFusedMaxK = 32768;  // fused quantise + GEMV up to this K
+constexpr int kQStride = 160;           // bytes between groups of q in shared memory
 
 // The group's 32 code bytes are read as two 16-byte halves, half `h` first
 // (h alternates every 4 lanes, which makes each 8-lane phase of the shared
 // loads hit 8 distinct bank groups).  The thread's activation words were
 // permuted the same way when they were loaded, so word i of `w` still meets
 // its own activation word.
+// crow, wsrow: shared addresses of the row's codes and (WS_SMEM) weight
+// scales in the ring.  t64 = -64 * sum(q) of the group, s64 = s / 64.
 template <bool WS_SMEM, bool DOTS>
-__device__ __forceinline__ float group_term(const uint8_t* crow, const uint8_t* wsrow_smem,
+__device__ __forceinline__ float group_term(uint32_t crow, uint32_t wsrow,
                                             const __half* wsrow_gmem, int32_t* dotrow, int g,
-                                            const uint32_t* q, int t, float s, int h) {
-    const uint4* cw = reinterpret_cast<const uint4*>(crow + g * 32);
-    const uint4 c0 = cw[h], c1 = cw[h ^ 1];
+                                            const uint32_t* q, int t64, float s64, int h) {
+    const uint32_t cw = crow + g * 32;
+    const uint4 c0 = pq2::lds_v4(cw + 16 * h), c1 = pq2::lds_v4(cw + 16 * (h ^ 1));
     const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const int dot = pq2::group_codes_dot(w, q) - t;
+    const int dot64 = pq2::group_codes_dot64(w, q, t64);
     if (DOTS) {
-        dotrow[g] = dot;
+        dotrow[g] = dot64 >> 6;  // exact: a multiple of 64
         return 0.0f;
     }
-    const __half wsh = WS_SMEM ? reinterpret_cast<const __half*>(wsrow_smem)[g] : wsrow_gmem[g];
-    return static_cast<float>(dot) * s * __half2float(wsh);
+    const float wsf =
+        WS_SMEM ? __half2float(__ushort_as_half(static_cast<unsigned short>(pq2::lds_u16(wsrow + 2 * g))))
+                : __half2float(wsrow_gmem[g]);
+    // float(dot64) exactly (|dot64| < 2^22): an integer add on the bit
+    // pattern of 1.5 * 2^23 and one subtraction, instead of a conversion
+    const float dotf = __fsub_rn(__int_as_float(0x4B400000 + dot64), 12582912.0f);
+    return dotf * s64 * wsf;
 }
 
 template <int GPT, bool WS_SMEM, bool DOTS, bool FUSED>
-__global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__((GPT == 1 ? kMaxConsumersSmall : kMaxConsumersLarge) + 32, 1)
+    gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + p.stages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + p.stages);
-    float* red = reinterpret_cast<float*>(smem + 16 * p.stages + 16);
+    uint64_t* abar = empty + p.stages;  // activations landed
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(abar + 1);
+    int8_t* qsm = reinterpret_cast<int8_t*>(smem + p.act_off);  // group g at g * kQStride
+    float* ssm = reinterpret_cast<float*>(smem + p.act_off + kQStride * p.G);
+    int32_t* tsm = reinterpret_cast<int32_t*>(smem + p.act_off + kQStride * p.G + 4 * p.G);
+    float* red = reinterpret_cast<float*>(smem + p.red_off);
+    // fused path: x is staged over the row-sum buffer (free until the first
+    // chunk's terms are written, which is after quantisation)
+    const __half* xsm = reinterpret_cast<const __half*>(smem + p.red_off);
+    uint8_t* ring = smem + p.ring_off;
+    const uint32_t ring_s = pq2::smem_u32(ring);
+    const uint32_t red_s = pq2::smem_u32(red);
     const int chunk_rows = p.chunk_stages * p.R;
     const int red_stride = chunk_rows * p.GT;  // floats per buffer
-    // fused path: the quantised activations live in shared memory
-    const int act_off = (16 * p.stages + 16 + 8 * red_stride + 127) & ~127;
-    int8_t* qsm = reinterpret_cast<int8_t*>(smem + act_off);
-    float* ssm = reinterpret_cast<float*>(smem + act_off + p.K);
-    int32_t* tsm = reinterpret_cast<int32_t*>(smem + act_off + p.K + 4 * p.G);
-    const int ring_off = FUSED ? ((act_off + p.K + 8 * p.G + 127) & ~127) : act_off;
-    uint8_t* ring = smem + ring_off;
 
     const int n_begin = blockIdx.x * p.rows_per_cta;
     const int n_end = min(p.N, n_begin + p.rows_per_cta);
@@ -112,22 +153,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
             pq2::mbar_init(&full[i], 1);
             pq2::mbar_init(&empty[i], nwarps);
         }
+        pq2::mbar_init(abar, 1);
         *abort_flag = 0;
         pq2::fence_mbar_init();
     }
     if (tid == p.TC && p.prefetch) {
-        // Start the weight stream before waiting for the preceding kernel.
-        // The weights are not its output in normal use, and even if they
-        // were, a prefetch into L2 (the coherence point) cannot return stale
-        // data to the copies issued after the wait.
-        const uint8_t* src = p.codes + static_cast<size_t>(n_begin) * p.codes_row_bytes;
-        uint32_t left = static_cast<uint32_t>(n_end - n_begin) * p.codes_row_bytes;
-        while (left > 0) {
-            const uint32_t b = left < 65536u ? left : 65536u;
-            bulk_prefetch_l2(src, b);
-            src += b;
-            left -= b;
-        }
+        // Start pulling this CTA's weights into L2 before waiting for the
+        // preceding kernel.  They are not its output in normal use; and even
+        // if they were, a prefetch into L2 (the coherence point) cannot make
+        // the copies issued after the wait return stale data.
+        const size_t rows = static_cast<size_t>(n_end - n_begin);
+        prefetch_range(p.codes + static_cast<size_t>(n_begin) * p.codes_row_bytes,
+                       rows * p.codes_row_bytes);
+        if (WS_SMEM)
+            prefetch_range(reinterpret_cast<const uint8_t*>(p.ws + static_cast<size_t>(n_begin) * p.G),
+                           rows * p.G * 2);
     }
     __syncthreads();
     // Activations, scales and (possibly) weights may come from the preceding
@@ -138,6 +178,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
     if (tid >= p.TC) {
         // ------------------------------ producer ------------------------------
         if (tid != p.TC) return;
+        if (FUSED) {
+            pq2::mbar_arrive_expect_tx(abar, 2u * p.K);
+            pq2::bulk_g2s(smem + p.red_off, p.x, 2u * p.K, abar);
+        }
         const uint64_t policy = pq2::policy_evict_first();
         int issued_end = 0;  // stages [0, issued_end) were armed, except a withheld one
         for (int i = 0; i < nst; ++i) {
@@ -170,6 +214,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
             if (last == p.ctl.debug_skip_stage) last -= p.stages;
             if (last >= 0) pq2::mbar_wait_bounded(&full[s], (last / p.stages) & 1, p.ctl);
         }
+        if (FUSED) pq2::mbar_wait_bounded(abar, 0, p.ctl);
         return;
     }
 
@@ -177,56 +222,81 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
     const int rp = tid / p.GT;
     const int gi = tid - rp * p.GT;
     const bool active = rp < p.RP;
-    const int RI = p.R / p.RP;  // even
+    const int RI = p.R / p.RP;  // rows per row slot and stage
     const int hswap = (tid >> 2) & 1;  // which 16-byte half of a group to read first
-
     const int lane = tid & 31;
     const int warp = tid >> 5;
+
+    bool failed = false;
     const int8_t* qsrc = p.qp;
+    int qstride = 128;
     const float* ssrc = p.S;
     const int32_t* tsrc = p.T;
     if (FUSED) {
-        // quantise the fp16 activations once per CTA (while the producer's
-        // first weight copies are in flight)
-        pq2::quantize_row_warps(p.x, p.G, warp, nwarps, lane, qsm, ssm, tsm);
-        pq2::named_bar_sync(2, p.TC);
+        if (!pq2::mbar_wait_bounded(abar, 0, p.ctl, abort_flag)) {
+            failed = true;
+            *abort_flag = 1;
+        }
+        // the quantiser shuffles within the warp: decide per warp
+        failed = __any_sync(0xffffffffu, failed);
+        if (!failed) {
+            // eight lanes per group, four groups per warp at a time
+            const int j = lane & 7;
+            for (int g0 = warp * 4; g0 < p.G; g0 += nwarps * 4) {
+                const int g = g0 + (lane >> 3);
+                const bool valid = g < p.G;
+                const int gl = valid ? g : g0;
+                const uint4* src = reinterpret_cast<const uint4*>(xsm + gl * 128 + 16 * j);
+                const uint4 h[2] = {src[0], src[1]};
+                pq2::quantize_group8(h, j, valid, qsm + gl * kQStride, ssm + gl, tsm + gl);
+            }
+        }
+        // everyone agrees on a failure before anything reads the activations
+        if (pq2::named_bar_any(2, p.TC, failed)) {
+            if (tid == 0) *abort_flag = 1;
+            return;
+        }
         qsrc = qsm;
+        qstride = kQStride;
         ssrc = ssm;
         tsrc = tsm;
     }
 
     uint32_t qreg[GPT][32];
-    float sg[GPT];
-    int tg[GPT];
+    float sg[GPT];  // s / 64
+    int tg[GPT];    // -64 * sum(q)
     bool gval[GPT];
 #pragma unroll
     for (int j = 0; j < GPT; ++j) {
         const int g = gi + j * p.GT;
         gval[j] = active && g < p.G;
         const int gl = gval[j] ? g : 0;
-        const uint4* src = reinterpret_cast<const uint4*>(qsrc + static_cast<size_t>(gl) * 128);
+        const uint4* src = reinterpret_cast<const uint4*>(qsrc + static_cast<size_t>(gl) * qstride);
+        const uint32_t src_s = pq2::smem_u32(qsm) + gl * kQStride;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
             // plane v/2, words 4*(v&1)..+3; stored at the half this thread reads first
-            const uint4 w = src[v ^ hswap];
+            const uint4 w = FUSED ? pq2::lds_v4(src_s + 16 * (v ^ hswap)) : src[v ^ hswap];
             qreg[j][4 * v + 0] = w.x;
             qreg[j][4 * v + 1] = w.y;
             qreg[j][4 * v + 2] = w.z;
             qreg[j][4 * v + 3] = w.w;
         }
-        sg[j] = DOTS ? 0.0f : ssrc[gl];
-        tg[j] = tsrc[gl];
+        sg[j] = DOTS ? 0.0f : ssrc[gl] * 0.015625f;  // exact scaling by 2^-6
+        tg[j] = -64 * tsrc[gl];
     }
 
-    bool failed = false;
-
+    // ring slot and phase parity advance incrementally: no integer division
+    // in the loop (it runs on the narrow conversion pipe, for every warp at
+    // the same moment)
+    int slot = 0;
+    uint32_t parity = 0;
+    uint32_t redb_s = red_s;  // row-sum buffer of the current chunk (two alternate)
     for (int c0 = 0; c0 < nst; c0 += p.chunk_stages) {
         const int c1 = min(nst, c0 + p.chunk_stages);
-        float* redb = red + ((c0 / p.chunk_stages) & 1) * red_stride;
         for (int i = c0; i < c1; ++i) {
-            const int slot = i % p.stages;
             if (!failed) {
-                if (!pq2::mbar_wait_bounded(&full[slot], (i / p.stages) & 1, p.ctl, abort_flag)) {
+                if (!pq2::mbar_wait_bounded(&full[slot], parity, p.ctl, abort_flag)) {
                     failed = true;
                     *abort_flag = 1;
                 }
@@ -234,39 +304,47 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
             if (!failed && active) {
                 const int row0 = n_begin + i * p.R;
                 const int rows = min(p.R, n_end - row0);
-                const uint8_t* stage = ring + static_cast<size_t>(slot) * p.stage_bytes;
-                const uint8_t* wsm = stage + static_cast<size_t>(p.R) * p.codes_row_bytes;
-                for (int t = 0; t < RI; t += 2) {
-                    const int ra = rp + t * p.RP;
-                    const int rb = ra + p.RP;
-                    if (ra >= rows) break;
-                    const bool hb = rb < rows;
-                    const int rbs = hb ? rb : ra;  // recompute row a when b is past the end
-                    const uint8_t* ca = stage + static_cast<size_t>(ra) * p.codes_row_bytes;
-                    const uint8_t* cb = stage + static_cast<size_t>(rbs) * p.codes_row_bytes;
-                    float acc_a = 0.0f, acc_b = 0.0f;
+                const uint32_t stage = ring_s + slot * p.stage_bytes;
+                const uint32_t wsm = stage + p.R * p.codes_row_bytes;
+                // this thread's groups of stage row r
+                auto row_term = [&](int r) {
+                    const uint32_t c = stage + r * p.codes_row_bytes;
+                    float acc = 0.0f;
 #pragma unroll
                     for (int j = 0; j < GPT; ++j) {
                         if (!gval[j]) continue;
-                        const int g = gi + j * p.GT;
-                        acc_a += group_term<WS_SMEM, DOTS>(
-                            ca, wsm + ra * p.G * 2, p.ws + static_cast<size_t>(row0 + ra) * p.G,
-                            p.dots + static_cast<size_t>(row0 + ra) * p.G, g, qreg[j], tg[j],
-                            sg[j], hswap);
-                        acc_b += group_term<WS_SMEM, DOTS>(
-                            cb, wsm + rbs * p.G * 2, p.ws + static_cast<size_t>(row0 + rbs) * p.G,
-                            p.dots + static_cast<size_t>(row0 + rbs) * p.G, g, qreg[j], tg[j],
-                            sg[j], hswap);
+                        acc += group_term<WS_SMEM, DOTS>(
+                            c, wsm + r * p.G * 2, p.ws + static_cast<size_t>(row0 + r) * p.G,
+                            p.dots + static_cast<size_t>(row0 + r) * p.G, gi + j * p.GT,
+                            qreg[j], tg[j], sg[j], hswap);
                     }
-                    if (!DOTS) {
-                        const int la = (i - c0) * p.R + ra;
-                        redb[la * p.GT + gi] = acc_a;
-                        if (hb) redb[(la + p.RP) * p.GT + gi] = acc_b;
+                    return acc;
+                };
+                // rows rp, rp + RP, ... of the stage, two at a time where possible
+                for (int t = 0; t < RI; t += 2) {
+                    const int ra = rp + t * p.RP;
+                    if (ra >= rows) break;
+                    const int rb = ra + p.RP;
+                    const int la = (i - c0) * p.R + ra;
+                    if (t + 1 < RI && rb < rows) {
+                        const float acc_a = row_term(ra);
+                        const float acc_b = row_term(rb);
+                        if (!DOTS) {
+                            pq2::sts_f32(redb_s + 4u * (la * p.GT + gi), acc_a);
+                            pq2::sts_f32(redb_s + 4u * ((la + p.RP) * p.GT + gi), acc_b);
+                        }
+                    } else {
+                        const float acc_a = row_term(ra);
+                        if (!DOTS) pq2::sts_f32(redb_s + 4u * (la * p.GT + gi), acc_a);
                     }
                 }
             }
             __syncwarp();
             if (lane == 0) pq2::mbar_arrive(&empty[slot]);
+            if (++slot == p.stages) {
+                slot = 0;
+                parity ^= 1u;
+            }
         }
         // all consumers have written this chunk's terms; agree on stopping
         const bool any_fail = pq2::named_bar_any(1, p.TC, failed);
@@ -275,16 +353,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvParams p
             break;
         }
         if (!DOTS) {
+            // row sums: 8 lanes per row, each over a fixed stride of the
+            // row's terms, then a fixed 3-step butterfly
             const int crow0 = n_begin + c0 * p.R;
             const int crows = min(n_end, n_begin + c1 * p.R) - crow0;
-            for (int r = warp; r < crows; r += nwarps) {
+            const int sub = lane & 7;
+            for (int rb = warp * 4; rb < crows; rb += nwarps * 4) {
+                const int r = rb + (lane >> 3);
                 float s = 0.0f;
-                for (int c = lane; c < p.GT; c += 32) s += redb[r * p.GT + c];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == 0) p.y[crow0 + r] = s;
+                if (r < crows)
+                    for (int c = sub; c < p.GT; c += 8) s += pq2::lds_f32(redb_s + 4u * (r * p.GT + c));
+                s += __shfl_xor_sync(0xffffffffu, s, 4);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                if (sub == 0 && r < crows) p.y[crow0 + r] = s;
             }
         }
+        redb_s = (redb_s == red_s) ? red_s + 4u * red_stride : red_s;
     }
 }
 
@@ -309,10 +394,10 @@ cudaError_t launch_gpt(const GemvParams& p, int grid, size_t smem, bool ws_smem,
     return launch_variant<GPT, false, false, false>(p, grid, smem, st);
 }
 
-// Tuning knobs (environment, read once): PQ2_GEMV_CTAS_PER_SM (default 2),
-// PQ2_GEMV_RING_KB (default 64), PQ2_GEMV_THREADS (target consumer threads,
-// default 256), PQ2_GEMV_STAGE_KB (default 4), PQ2_GEMV_PREFETCH (1 = on,
-// default 1; 2 = off).
+// Tuning knobs (environment, read once): PQ2_GEMV_CTAS_PER_SM (default 1),
+// PQ2_GEMV_RING_KB (default 160), PQ2_GEMV_STAGE_KB (default 16),
+// PQ2_GEMV_PREFETCH (1 = on; 2 = off, default: with one CTA per SM the
+// prefetch only queues ahead of the ring copies).
 int env_int(const char* name, int dflt) {
     const char* v = std::getenv(name);
     if (!v || !*v) return dflt;
@@ -321,26 +406,35 @@ int env_int(const char* name, int dflt) {
 }
 
 struct Tuning {
-    int ctas_per_sm, ring_kb, threads, stage_kb, prefetch;
+    int ctas_per_sm, ring_kb, stage_kb, prefetch;
 };
 
 const Tuning& tuning() {
-    static const Tuning t = {env_int("PQ2_GEMV_CTAS_PER_SM", 2), env_int("PQ2_GEMV_RING_KB", 64),
-                             env_int("PQ2_GEMV_THREADS", 256), env_int("PQ2_GEMV_STAGE_KB", 4),
-                             env_int("PQ2_GEMV_PREFETCH", 1) == 1 ? 1 : 0};
+    static const Tuning t = {env_int("PQ2_GEMV_CTAS_PER_SM", 1), env_int("PQ2_GEMV_RING_KB", 160),
+                             env_int("PQ2_GEMV_STAGE_KB", 16),
+                             env_int("PQ2_GEMV_PREFETCH", 2) == 1 ? 1 : 0};
     return t;
 }
 
-size_t smem_bytes(const GemvParams& p) {
-    const int red_floats = 2 * p.chunk_stages * p.R * p.GT;
-    size_t head = (16 * p.stages + 16 + 4 * red_floats + 127) & ~127;
-    if (p.x) head = (head + p.K + 8 * p.G + 127) & ~static_cast<size_t>(127);
-    return head + static_cast<size_t>(p.stages) * p.stage_bytes;
+uint32_t align128(size_t v) { return static_cast<uint32_t>((v + 127) & ~static_cast<size_t>(127)); }
+
+// Shared-memory layout: barriers | activations (q, S, T) | row-sum buffers
+// (the fused path stages fp16 x there first) | ring.
+size_t layout(GemvParams& p) {
+    p.act_off = align128(8 * (2 * p.stages + 1) + 16);
+    const size_t act = p.x ? static_cast<size_t>(kQStride + 8) * p.G : 0;
+    p.red_off = align128(p.act_off + act);
+    size_t red = 8 * static_cast<size_t>(p.chunk_stages) * p.R * p.GT;
+    if (p.x && red < 2 * static_cast<size_t>(p.K)) red = 2 * static_cast<size_t>(p.K);
+    p.ring_off = align128(p.red_off + red);
+    return p.ring_off + static_cast<size_t>(p.stages) * p.stage_bytes;
 }
 
 }  // namespace
 
 namespace pq2h {
+
+bool gemv_fused_supported(int64_t K) { return K <= kFusedMaxK; }
 
 cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const int32_t* T,
                         const uint8_t* codes, const __half* ws, float* y, int32_t* dots, int64_t N,
@@ -348,6 +442,7 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const
     const Tuning& tu = tuning();
     GemvParams p = {};
     p.x = dots ? nullptr : x;
+    if (p.x && K > kFusedMaxK) return cudaErrorInvalidValue;
     p.qp = qp;
     p.S = S;
     p.T = T;
@@ -358,36 +453,40 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
     p.G = static_cast<int>(K / 128);
-    const int gpt = p.G <= 512 ? 1 : (p.G <= 1024 ? 2 : 4);
+    const int gpt = p.G <= kMaxConsumersSmall ? 1 : (p.G <= 2 * kMaxConsumersLarge ? 2 : 4);
     p.GT = (p.G + gpt - 1) / gpt;
-    const int target = tu.threads < 32 ? 32 : (tu.threads > 512 ? 512 : tu.threads);
-    p.RP = target / p.GT > 0 ? target / p.GT : 1;
+    const int max_tc = gpt == 1 ? kMaxConsumersSmall : kMaxConsumersLarge;
+    p.RP = max_tc / p.GT > 0 ? max_tc / p.GT : 1;
     p.TC = ((p.RP * p.GT + 31) / 32) * 32;
     p.codes_row_bytes = static_cast<uint32_t>(K / 4);
     const bool ws_smem = (dots == nullptr) && (p.G % 8 == 0);
     const int row_bytes = static_cast<int>(p.codes_row_bytes) + (ws_smem ? 2 * p.G : 0);
-    const int per_pair = 2 * p.RP * row_bytes;  // rows come in pairs per thread
-    int pairs = (tu.stage_kb * 1024 + per_pair / 2) / per_pair;
-    if (pairs < 1) pairs = 1;
-    p.R = 2 * p.RP * pairs;
-    p.stage_bytes = static_cast<uint32_t>(((p.R * row_bytes) + 15) & ~15);
-    int stages = tu.ring_kb * 1024 / static_cast<int>(p.stage_bytes);
-    p.stages = stages > 16 ? 16 : (stages < 2 ? 2 : stages);
     const int64_t slots = static_cast<int64_t>(dev.num_sms) * tu.ctas_per_sm;
     const int rows_per_cta = static_cast<int>((N + slots - 1) / slots);
     p.rows_per_cta = rows_per_cta;
-    // ~64 rows per row-sum chunk, never more than the CTA owns
-    int cs = (64 + p.R - 1) / p.R;
+    // stage = RP*k rows of about stage_kb, not more than the CTA owns
+    const int per_k = p.RP * row_bytes;
+    int k = (tu.stage_kb * 1024 + per_k / 2) / per_k;
+    const int max_k = (rows_per_cta + p.RP - 1) / p.RP;
+    if (k > max_k) k = max_k;
+    if (k < 1) k = 1;
+    p.R = p.RP * k;
+    p.stage_bytes = static_cast<uint32_t>(((p.R * row_bytes) + 15) & ~15);
     const int cta_stages = (rows_per_cta + p.R - 1) / p.R;
+    int stages = tu.ring_kb * 1024 / static_cast<int>(p.stage_bytes);
+    if (stages > cta_stages) stages = cta_stages;
+    p.stages = stages > 16 ? 16 : (stages < 2 ? 2 : stages);
+    // row-sum chunk: ~12 KB of terms (at least one stage, at most the CTA's rows)
+    int cs = (12 * 1024 / (4 * p.GT)) / p.R;
     if (cs > cta_stages) cs = cta_stages;
     p.chunk_stages = cs < 1 ? 1 : cs;
     const int grid = static_cast<int>((N + rows_per_cta - 1) / rows_per_cta);
     p.ctl = ctl;
     p.prefetch = tu.prefetch;
-    size_t smem = smem_bytes(p);
+    size_t smem = layout(p);
     while (smem > static_cast<size_t>(dev.max_smem_optin) && p.stages > 2) {
         --p.stages;
-        smem = smem_bytes(p);
+        smem = layout(p);
     }
     if (smem > static_cast<size_t>(dev.max_smem_optin)) return cudaErrorInvalidConfiguration;
     if (gpt == 1) return launch_gpt<1>(p, grid, smem, ws_smem, dots != nullptr, st);

@@ -29,7 +29,9 @@ cudaError_t launch_pack(const int8_t* tern, uint8_t* codes, int64_t N, int64_t K
 
 // M == 1.  dots != nullptr selects the integer-dot debug output instead of y.
 // x != nullptr selects the fused path: the kernel quantises the fp16
-// activations itself (qp, S, T unused).
+// activations itself (qp, S, T unused); only for K where
+// gemv_fused_supported(K).
+bool gemv_fused_supported(int64_t K);
 cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const int32_t* T,
                         const uint8_t* codes, const __half* ws, float* y, int32_t* dots, int64_t N,
                         int64_t K, cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev);
@@ -49,11 +51,5 @@ cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, c
                            const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
                            int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                            const DeviceInfo& dev);
-
-// Plain warp-per-output kernel, any M (first correct path for M > 1).
-cudaError_t launch_simple(const int8_t* qp, const float* S, const int32_t* T,
-                          const uint8_t* codes, const __half* ws, float* y, int32_t* dots,
-                          int64_t M, int64_t N, int64_t K, cudaStream_t st,
-                          const pq2::DevCtl& ctl, const DeviceInfo& dev);
 
 }  // namespace pq2h

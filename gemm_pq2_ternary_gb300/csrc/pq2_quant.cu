@@ -3,8 +3,9 @@
 // Quantise ("Making a ternary reasoning model fast in vLLM", page "From CUDA
 // to Triton and Gluon", section "Prompt processing": one quantize kernel
 // emits q [m,k] int8, s [m,G] fp32, t [m,G] int32; section "One token at a
-// time": q in plane order).  One warp per 128-value group (grid-stride), the
-// per-group step shared with the fused M = 1 path (quantize_group_warp).
+// time": q in plane order).  Eight lanes per 128-value group, four groups per
+// warp (grid-stride); the per-group step is shared with the fused M = 1 path
+// (quantize_group8).
 //
 // Pack (same page, "One token at a time": codes 0,1,2 for -1,0,+1, four to a
 // byte, weight 4*byte+s in bits 2s).  One thread per 16 ternary values.
@@ -20,10 +21,17 @@ __global__ void __launch_bounds__(256) quantize_kernel(const __half* __restrict_
     pq2::pdl_wait();
     pq2::pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
+    const int j = lane & 7;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t gi = warp; gi < groups; gi += nwarps)
-        pq2::quantize_group_warp(x + gi * 128, lane, qp + gi * 128, S + gi, T + gi);
+    for (int64_t g0 = warp * 4; g0 < groups; g0 += nwarps * 4) {
+        const int64_t g = g0 + (lane >> 3);
+        const bool valid = g < groups;
+        const int64_t gl = valid ? g : g0;
+        const uint4* src = reinterpret_cast<const uint4*>(x + gl * 128 + 16 * j);
+        const uint4 h[2] = {pq2::ld_nc_v4(src), pq2::ld_nc_v4(src + 1)};
+        pq2::quantize_group8(h, j, valid, qp + gl * 128, S + gl, T + gl);
+    }
 }
 
 __global__ void __launch_bounds__(256) pack_kernel(const int8_t* __restrict__ tern,
@@ -67,7 +75,7 @@ cudaError_t launch_quantize(const __half* x, int8_t* qp, float* S, int32_t* T, i
                             const DeviceInfo& dev) {
     const int64_t groups = M * (K / 128);
     if (groups == 0) return cudaSuccess;
-    const int64_t want = (groups + 7) / 8;
+    const int64_t want = (groups + 31) / 32;  // 8 warps x 4 groups per block
     const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
     const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
     return launch(quantize_kernel, dim3(grid), dim3(256), 0, st, true, x, qp, S, T, groups, ctl);

@@ -165,7 +165,9 @@ pq2_status pq2_gemm_prefill(const int8_t* qp, const float* S, const int32_t* T,
  * pages' routing by token count ([P1] "Defaults and switches").
  *   x_f16 [M,K] fp16, codes, ws_f16 in; y [M,N] fp32 out.
  *   workspace: pq2_workspace_bytes(PQ2_OP_MATMUL, M, N, K) bytes (holds the
- *   quantised activations plus the chosen kernel's own scratch).
+ *   quantised activations plus the chosen kernel's own scratch).  For M == 1
+ *   and K <= 32768 the GEMV kernel quantises x itself (one launch) and no
+ *   workspace is needed (size 0, workspace may be NULL).
  */
 pq2_status pq2_matmul(const void* x_f16, const uint8_t* codes, const void* ws_f16, float* y,
                       int64_t M, int64_t N, int64_t K,
