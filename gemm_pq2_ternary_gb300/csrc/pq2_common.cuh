@@ -85,8 +85,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, un
     return ok != 0;
 }
 
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed, at most
-// `limit_ns` of wall time.  Returns false (and sets the device error word)
+// `limit_ns` of wall time (polling, with a short sleep between polls after
+// the first few).  Returns false (and sets the device error word)
 // if the limit ran out.  `abort_flag` (shared memory, may be null): give up
 // early, without error, once another thread of the block has set it.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
@@ -96,7 +110,42 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     unsigned long long t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity, ctl.wait_hint_ns)) return true;
+        // after a few polls, yield the scheduler between polls: a polling
+        // warp otherwise takes issue slots from the warps it waits for
+        if (i >= 8) __nanosleep(32);
         if ((i & 3u) == 0) {
+            if (abort_flag && *abort_flag) return false;
+            if (globaltimer_ns() - t0 > ctl.wait_limit_ns) {
+                atomicOr(ctl.err, DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Warp-wide wait: lane 0 polls the barrier (bounded) and the warp then
+// synchronises, which orders the other lanes after lane 0's acquire.  One
+// poller per warp instead of 32 keeps the barrier unit free for the other
+// waiters.  All 32 lanes must call it; the result is warp-uniform.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const DevCtl& ctl,
+                                               volatile int* abort_flag = nullptr) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, ctl, abort_flag);
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// Same bound, busy-polling with test_wait: for a single thread on the
+// critical path (a suspended try_wait can resume well after the phase
+// completes).
+__device__ __forceinline__ bool mbar_spin_bounded(uint64_t* bar, uint32_t parity,
+                                                  const DevCtl& ctl,
+                                                  volatile int* abort_flag = nullptr) {
+    if (mbar_test_wait(bar, parity)) return true;
+    unsigned long long t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
             if (abort_flag && *abort_flag) return false;
             if (globaltimer_ns() - t0 > ctl.wait_limit_ns) {
                 atomicOr(ctl.err, DEVERR_TIMEOUT);

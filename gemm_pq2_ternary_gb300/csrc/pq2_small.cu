@@ -1,569 +1,721 @@
-// Small-batch matmul, 2 <= M <= 16 token rows (pq2_gemm_small).
+// Small-batch matmul, 2 <= M <= 16 tokens (pq2_gemm_small), on the
+// 5th-generation tensor cores (tcgen05, operands and accumulators in tensor
+// memory).
 //
-// The pages' small-batch kernels ("Making a ternary reasoning model fast in
-// vLLM", page "From CUDA to Triton and Gluon", sections "Small batches: make
-// the register layout explicit", "Use a ring buffer for longer rows",
-// "Extend the kernels to sixteen token rows") load code bytes straight into
-// the A fragments of an m16n8k32 tensor-core MMA and extract each plane with
-// a shift and a mask; K splits are summed in the fixed order 0, 1, 2, ...
-// (section "Choose the configuration with the proxy").
+// The method is the pages' small-batch kernels ("Making a ternary reasoning
+// model fast in vLLM", page "From CUDA to Triton and Gluon", sections "Small
+// batches: make the register layout explicit" and "Extend the kernels to
+// sixteen token rows"): the planes of the code bytes go straight to the
+// tensor cores, which meet them with the int8 activations of all token rows
+// at once, one exact integer dot per (row, token, group); then the same
+// per-group -sum(q) correction and fp32 dequantise-accumulate as the M = 1
+// path.  Split partial sums are combined in a fixed order (section "Choose
+// the configuration with the proxy").
 //
-// GB300 design.  The int8 tensor path is a fraction of the fp8 one on this
-// part, so the MMA is m16n8k32 with e4m3 operands and an fp32 accumulator,
-// and stays exact:
-//  * A = 16 weight rows x 32 code bytes of one plane.  A code byte masked in
-//    place, w & 0x03030303 or w & 0x0C0C0C0C, read as e4m3 is the subnormal
-//    c * 2^-9 or the value 4c * 2^-9 (e4m3 bytes below 16 are exactly
-//    byte * 2^-9).  Planes 0,1 are masked in place, planes 2,3 after one
-//    shift by 4: five integer ops per code word.
-//  * B = 8 tokens x 32 activations of that plane.  An int8 q is split as
-//    q = 16h + l (h in [-8,7], l in [0,15]); 16h and l (planes 0,2) or 4h and
-//    l/4 (planes 1,3, which compensates the 4x of A) are exact e4m3 values.
-//    Two MMAs (high, low) per plane accumulate into the same fp32 D, so
-//    D = 2^-9 * sum(code * q) exactly (all partial sums are small integer
-//    multiples of 2^-9).
-//  * The k order inside an MMA is free as long as A and B agree: lane
-//    (gid, tid) holds code words 2tid, 2tid+1 of its rows (one 8-byte load)
-//    and the activation words 2tid, 2tid+1 of the same plane.
-//  * Per group: dot = D*512 - sum(q) (exact in fp32), then
-//    acc += dot * s * ws in fp32, as the M = 1 path.
+// GB300 design.  tcgen05 has no int8 kind on sm_103a; kind::f8f6f4 with e4m3
+// operands is exact here (as in the prefill kernel):
+//  * weights = A operand (M = 128 rows per tile), kept in TENSOR MEMORY: each
+//    thread owns one weight row (one TMEM lane) and writes plane s of its
+//    code words, (w >> 2s) & 0x03030303, as e4m3 bytes (bytes below 16 are
+//    exactly byte * 2^-9) with tcgen05.st.  No shared-memory round trip for
+//    the expanded weights;
+//  * tokens = B operand: q = 16h + l, with 16h and l exact e4m3 values.  A
+//    per-call preparation kernel writes, per group, one 32 x 128-byte tile
+//    holding the hi and the lo parts of tokens 0..15 (zero past M).  So one
+//    MMA with N = 32 per k-step gives the hi and lo partial dots side by side
+//    in D, and D_hi + D_lo = 2^-9 * dot(codes, q) exactly;
+//  * per group, 4 k-steps: the k order inside a group is the plane order of
+//    the activations, so k-step s is plane s (8 A columns);
+//  * epilogue: acc += ((D_hi + D_lo) * 512 s - s t) * ws in registers (the
+//    integer-dot debug output forms dot = (D_hi + D_lo) * 512 - t, exact), the 16 tokens of a weight row split over four warps.  The
+//    B rows are ordered [hi of tokens 0-3, lo of tokens 0-3, hi 4-7, lo 4-7,
+//    ...], so a warp's 4 tokens are 8 adjacent D columns.
 //
-// Work split: the K groups are cut into KS splits and the 16-row tiles of
-// each split are shared out evenly over num_SMs/KS persistent CTAs.  A CTA
-// streams, per stage, the code bytes of all its rows for a few groups (one
-// 1-D bulk copy per row segment) plus the prepared B fragments of those
-// groups (one bulk copy) through a shared-memory ring; four consumer warps
-// own its tiles, keep each group's B fragments in registers across their
-// tiles, and accumulate over the whole split in registers.  KS > 1 writes
-// partial sums that a second kernel adds in split order.
+// Items are (row tile, quad of 4 groups): one item's codes are a 128-row x
+// 128-byte box (whole lines for the TMA engine, 128-byte swizzle) and its
+// token tiles one 128-row box of the prepared tensor.  The items are cut
+// into contiguous, balanced ranges, one per CTA (one CTA per SM).  A CTA
+// flushes its accumulators at each row-tile boundary of its range: a tile
+// owned by a single CTA is written straight to y; otherwise each contributor
+// writes its partial sums and bumps the tile's counter, and the last one to
+// arrive sums the partials of all contributors in CTA order and writes y
+// (deterministic: the order is fixed, not the arrival order).
+//
+// Per CTA:
+//   warp 0      producer: per item, TMA loads of the code box and the token
+//               tiles, one bulk copy of the tokens' (s, t); its 32 lanes load
+//               the 128 rows' weight scales (two items ahead) into the stage
+//   warp 1      TMEM allocation; MMA issuer (one thread)
+//   warps 2-17  workers: expansion of item i (codes -> A in TMEM; the four
+//               warps of a lane quadrant take one group each), then the
+//               epilogue of item i-1 (the four warps take 4 tokens each)
+// Every mbarrier wait is bounded (device error word on expiry).
 #include "pq2_internal.h"
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kTilesPerWarp = 3;                       // register accumulators per warp
-constexpr int kBatchTiles = kConsumerWarps * kTilesPerWarp;
-constexpr int kFragBytesPerGroupTile = 4 * 2 * 32 * 8;  // planes x (hi,lo) x lanes x 8 B
+constexpr int kRows = 128;            // weight rows per tile (MMA M)
+constexpr int kTok = 16;              // token rows of B per plane (hi, lo)
+constexpr int kGQ = 4;                // groups per item
+constexpr int kStages = 4;            // TMA ring
+constexpr int kBufs = 2;              // A and D buffers in TMEM, per item
+constexpr int kWorkerWarps = 16;      // four per TMEM lane quadrant
+constexpr int kTokPerWarp = 4;        // epilogue tokens per worker warp
+constexpr int kWorkerThreads = kWorkerWarps * 32;
+constexpr int kThreads = (2 + kWorkerWarps) * 32;
+constexpr uint32_t kTmemCols = 512;   // A: 2 items x 4 groups x 32; D: 2 x 4 x 32
+constexpr uint32_t kGCols = 32;       // TMEM columns per group (A: K = 128 e4m3; D: N = 32 fp32)
+constexpr uint32_t kDCol0 = kBufs * kGQ * kGCols;  // 256
+constexpr int kMaxGrid = 256;         // CTAs per call at most (bounds the partial-sum slots)
+constexpr int kWsAhead = 2;           // items ahead the producer loads weight scales
 
-__device__ __forceinline__ uint32_t pack_e4m3x4(float v0, float v1, float v2, float v3) {
+constexpr uint32_t kCodesBytes = kRows * 128;          // 4 groups x 32 B per row, swizzled
+constexpr uint32_t kTokGroupBytes = 2 * kTok * 128;    // 32 rows x 128 B per group
+constexpr uint32_t kTokOff = kCodesBytes;
+constexpr uint32_t kStOff = kTokOff + kGQ * kTokGroupBytes;  // (s, t): 4 groups x 16 tokens
+constexpr uint32_t kWsOff = kStOff + kGQ * kTok * 8;         // ws: 4 groups x 128 rows, fp32
+constexpr uint32_t kTmaBytes = kStOff + kGQ * kTok * 8;      // bytes the TMA engine brings
+constexpr uint32_t kStageBytes = 35840;                      // multiple of 1024
+static_assert(kWsOff + kGQ * kRows * 4 <= kStageBytes, "stage layout");
+
+struct SmallParams {
+    CUtensorMap tm_codes;  // uint8 [N][K/4], box {128, 128}, 128B swizzle
+    CUtensorMap tm_tok;    // uint8 [G4 * 32][128], box {128, 128}, 128B swizzle
+    const float2* st16;    // [G4][16] (s, t) pairs, zero past M and past G
+    const __half* ws;      // [N][G]
+    float* y;              // [M][N]
+    int32_t* dots;         // debug: [M][N][G]
+    float* partial;        // [grid + n_tiles][M][128]
+    unsigned* counters;    // [n_tiles], zero on entry
+    int M, N, K, G;
+    int Q;                 // quads per row tile: ceil(G / 4)
+    int n_tiles;
+    int grid;
+    long long items;       // n_tiles * Q
+    pq2::DevCtl ctl;
+};
+
+// First item of CTA c; CTA owning item i (the inverse of the split).
+__host__ __device__ __forceinline__ long long range_begin(long long c, long long items, int grid) {
+    return c * items / grid;
+}
+__host__ __device__ __forceinline__ int owner_of(long long i, long long items, int grid) {
+    return static_cast<int>(((i + 1) * grid - 1) / items);
+}
+
+// ---------------------------------------------------------------------------
+// per-call preparation: token tiles, (s, t) table, tile counters
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
     uint32_t lo, hi;
-    // cvt ... e4m3x2.f32 d, a, b packs a into the upper byte, b into the lower
-    asm("{\n\t.reg .b16 t;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\t"
-        "cvt.u32.u16 %0, t;\n\t}"
-        : "=r"(lo)
-        : "f"(v0), "f"(v1));
-    asm("{\n\t.reg .b16 t;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\t"
-        "cvt.u32.u16 %0, t;\n\t}"
-        : "=r"(hi)
-        : "f"(v2), "f"(v3));
+    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
+        : "=r"(lo) : "f"(v0), "f"(v1));
+    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
+        : "=r"(hi) : "f"(v2), "f"(v3));
     return lo | (hi << 16);
 }
 
-// One activation word (4 int8 q, same plane s) -> its high and low e4m3
-// fragment words: q = 16h + l; planes 0,2 take (16h, l), planes 1,3 take
-// (4h, l/4).  All of these values are exact in e4m3.
-__device__ __forceinline__ void split_word(uint32_t qw, bool quarter, uint32_t* hiw,
-                                           uint32_t* low) {
-    float hv[4], lv[4];
+// tok [G4][32][128]: token m's e4m3(16h) in row 8*(m/4) + m%4 and its
+// e4m3(l) in row 8*(m/4) + 4 + m%4 (q = 16h + l, h = floor(q/16)); zero for
+// tokens >= M and groups >= G.  st16 [G4][16]: (512 s, s t) for the matmul
+// (the epilogue's term is D * 512 s - s t), or (0, t) when S is null (the
+// integer-dot debug output); zero likewise.
+__global__ void __launch_bounds__(256) small_prep_kernel(const int8_t* __restrict__ qp,
+                                                         const float* __restrict__ S,
+                                                         const int32_t* __restrict__ T,
+                                                         uint32_t* __restrict__ tok,
+                                                         float2* __restrict__ st16,
+                                                         unsigned* __restrict__ counters,
+                                                         int64_t M, int64_t K, int64_t G4,
+                                                         int n_tiles) {
+    pq2::pdl_wait();
+    pq2::pdl_launch_dependents();
+    const int64_t G = K / 128;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    // one index = one 4-byte word of one token of one group (hi and lo together)
+    const int64_t words = G4 * kTok * 32;
+    for (int64_t i = i0; i < words; i += stride) {
+        const int64_t g = i / (kTok * 32);
+        const int m = static_cast<int>((i / 32) % kTok);
+        const int wq = static_cast<int>(i % 32);
+        uint32_t hw = 0, lw = 0;
+        if (m < M && g < G) {
+            const uint32_t qw = reinterpret_cast<const uint32_t*>(qp + m * K + g * 128)[wq];
+            float h[4], l[4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const int q = static_cast<int8_t>((qw >> (8 * b)) & 0xFFu);
-        const int hq = q >> 4;  // floor(q / 16)
-        const int lq = q & 15;  // q - 16 * hq
-        hv[b] = static_cast<float>(quarter ? 4 * hq : 16 * hq);
-        lv[b] = quarter ? 0.25f * static_cast<float>(lq) : static_cast<float>(lq);
+            for (int b = 0; b < 4; ++b) {
+                const int q = static_cast<int8_t>((qw >> (8 * b)) & 0xFFu);
+                h[b] = static_cast<float>(16 * (q >> 4));  // 16 * floor(q / 16), exact in e4m3
+                l[b] = static_cast<float>(q & 15);         // q - 16 * floor(q / 16)
+            }
+            hw = e4m3x4(h[0], h[1], h[2], h[3]);
+            lw = e4m3x4(l[0], l[1], l[2], l[3]);
+        }
+        uint32_t* tg = tok + g * (2 * kTok * 32);
+        const int rh = 8 * (m / 4) + (m % 4);
+        tg[rh * 32 + wq] = hw;
+        tg[(rh + 4) * 32 + wq] = lw;
     }
-    *hiw = pack_e4m3x4(hv[0], hv[1], hv[2], hv[3]);
-    *low = pack_e4m3x4(lv[0], lv[1], lv[2], lv[3]);
+    for (int64_t i = i0; i < G4 * kTok; i += stride) {
+        const int64_t g = i / kTok, m = i - g * kTok;
+        float2 v = make_float2(0.0f, 0.0f);
+        if (m < M && g < G) {
+            const float t = static_cast<float>(T[m * G + g]);
+            v = S ? make_float2(512.0f * S[m * G + g], S[m * G + g] * t) : make_float2(0.0f, t);
+        }
+        st16[i] = v;
+    }
+    for (int64_t i = i0; i < n_tiles; i += stride) counters[i] = 0u;
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 helpers
+// ---------------------------------------------------------------------------
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(1) << 16;          // leading offset (unused here)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;  // stride offset
+    d |= static_cast<uint64_t>(1) << 46;          // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;          // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f8f6f4: D f32, A and B e4m3, K-major,
+// M = 128, N = 32 (the hi and lo token rows of one group).
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) |
+                            (static_cast<uint32_t>((2 * kTok) >> 3) << 17) |
+                            (static_cast<uint32_t>(kRows >> 4) << 24);
+
+// D (tensor memory) += A (tensor memory) x B (shared memory descriptor).
+__device__ __forceinline__ void mma_f8_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(kIdesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            pq2::smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15]));
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_cg(const float* p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
 }
 
 // ---------------------------------------------------------------------------
 // main kernel
 // ---------------------------------------------------------------------------
-struct SmallParams {
-    CUtensorMap tm_codes;  // uint32 [N][K/16], box {GC*8, box_rows}
-    CUtensorMap tm_qp;     // uint32 [M][K/4],  box {GC*32, 16}
-    const __half* ws;
-    const float* S;
-    const int32_t* T;
-    float* out;      // y (KS == 1) or partials [KS][M][N]
-    int32_t* dots;   // debug: per-group integer dots [M][N][G]
-    int M, N, K, G;
-    int KS;
-    int ctas_per_ks;
-    int n_tiles;
-    int GC;          // groups per stage
-    int stages;
-    int batch_rows;  // rows per batch (<= 16 * kBatchTiles)
-    int box_rows;    // rows per codes box (batch_rows or half of it)
-    uint32_t stage_bytes;
-    uint32_t codes_stage_bytes;  // batch_rows * GC * 32
-    uint32_t qp_stage_bytes;     // 16 * GC * 128
-    int max_groups_per_split;
-    int swizzle;     // codes tiles stored with the 128-byte TMA swizzle (GC == 4)
-    pq2::DevCtl ctl;
-};
-
-__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-template <int NT, bool DOTS>
-__global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
-    small_kernel(const __grid_constant__ SmallParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + p.stages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + p.stages);
-    const int st_off = 16 * p.stages + 16;
-    float2* st_sm = reinterpret_cast<float2*>(smem + st_off);  // [groups][16] (s, t)
-    const int ws_off = st_off + p.max_groups_per_split * 16 * 8;
-    __half* ws_sm = reinterpret_cast<__half*>(smem + ws_off);  // [batch_rows][groups]
-    // stages start on 1024-byte boundaries (the swizzle pattern follows the
-    // shared-memory address bits)
-    const uint32_t base_addr = pq2::smem_u32(smem);
-    const uint32_t ring_addr =
-        (base_addr + ws_off + p.batch_rows * p.max_groups_per_split * 2 + 1023) & ~1023u;
-    uint8_t* ring = smem + (ring_addr - base_addr);
+template <bool DOTS>
+__global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constant__ SmallParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t full[kStages];    // stage landed: TMA bytes + the producer's 32 lanes
+    __shared__ uint64_t sfree[kStages];   // stage consumed: 8 worker warps, after the item's
+                                          // epilogue (so after its MMAs, which read the tokens)
+    __shared__ uint64_t aready[kBufs];    // expanded weights written to TMEM (8 worker warps)
+    __shared__ uint64_t dfull[kBufs];     // the item's MMAs are done (commit): D holds its dots
+                                          // and its A buffer may be rewritten
+    __shared__ uint64_t dfree[kBufs];     // epilogue done reading a D buffer (8 worker warps)
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    __shared__ int last_flag;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int ks = blockIdx.x / p.ctas_per_ks;
-    const int cj = blockIdx.x - ks * p.ctas_per_ks;
-    const int t0 = static_cast<int>((static_cast<long long>(p.n_tiles) * cj) / p.ctas_per_ks);
-    const int t1 = static_cast<int>((static_cast<long long>(p.n_tiles) * (cj + 1)) / p.ctas_per_ks);
-    const int g0 = (p.G * ks) / p.KS;
-    const int g1 = (p.G * (ks + 1)) / p.KS;
-    if (t0 >= t1 || g0 >= g1) return;
-    const int n_groups = g1 - g0;
-    const int n_gstages = (n_groups + p.GC - 1) / p.GC;
-    const int batch_tiles = p.batch_rows / 16;
-    const int n_batches = (t1 - t0 + batch_tiles - 1) / batch_tiles;
-    const int total_stages = n_batches * n_gstages;
+    const uint32_t base = pq2::smem_u32(smem);
+    uint8_t* stage0 = smem + ((1024 - (base & 1023)) & 1023);
+    const uint32_t stage0_s = pq2::smem_u32(stage0);
 
     if (tid == 0) {
-        for (int i = 0; i < p.stages; ++i) {
-            pq2::mbar_init(&full[i], 1);
-            pq2::mbar_init(&empty[i], kConsumerWarps);
+        for (int i = 0; i < kStages; ++i) {
+            pq2::mbar_init(&full[i], 1 + 32);
+            pq2::mbar_init(&sfree[i], kWorkerWarps);
         }
-        *abort_flag = 0;
+        for (int i = 0; i < kBufs; ++i) {
+            pq2::mbar_init(&aready[i], kWorkerWarps);
+            pq2::mbar_init(&dfull[i], 1);
+            pq2::mbar_init(&dfree[i], kWorkerWarps);
+        }
+        abort_flag = 0;
         pq2::fence_mbar_init();
     }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         pq2::smem_u32(&tmem_base)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
     pq2::pdl_wait();
     pq2::pdl_launch_dependents();
 
-    if (warp == kConsumerWarps) {
-        // ------------------------------ producer ------------------------------
-        if (lane != 0) return;
-        const int n_boxes = p.batch_rows / p.box_rows;
-        const uint32_t tx = p.codes_stage_bytes + p.qp_stage_bytes;
-        int issued_end = 0;
-        for (int i = 0; i < total_stages; ++i) {
-            const int slot = i % p.stages;
-            if (i >= p.stages &&
-                !pq2::mbar_wait_bounded(&empty[slot], ((i / p.stages) - 1) & 1, p.ctl, abort_flag))
-                break;
-            issued_end = i + 1;
-            if (i == p.ctl.debug_skip_stage) continue;
-            const int b = i / n_gstages;
-            const int gs = i - b * n_gstages;
-            const int row0 = (t0 + b * batch_tiles) * 16;
-            const int ga = g0 + gs * p.GC;
-            uint8_t* cdst = ring + static_cast<size_t>(slot) * p.stage_bytes;
-            pq2::mbar_arrive_expect_tx(&full[slot], tx);
-            for (int bx = 0; bx < n_boxes; ++bx)
-                pq2::tma_load_2d(cdst + static_cast<size_t>(bx) * p.box_rows * p.GC * 32,
-                                 &p.tm_codes, ga * 8, row0 + bx * p.box_rows, &full[slot]);
-            pq2::tma_load_2d(cdst + p.codes_stage_bytes, &p.tm_qp, ga * 32, 0, &full[slot]);
-        }
-        for (int s = 0; s < p.stages; ++s) {
-            if (issued_end <= s) continue;
-            int last = s + ((issued_end - 1 - s) / p.stages) * p.stages;
-            if (last == p.ctl.debug_skip_stage) last -= p.stages;
-            if (last >= 0) pq2::mbar_wait_bounded(&full[s], (last / p.stages) & 1, p.ctl);
-        }
-        return;
-    }
+    const uint32_t tmem = tmem_base;
+    const int G = p.G, Q = p.Q;
+    const long long w0 = range_begin(blockIdx.x, p.items, p.grid);
+    const long long w1 = range_begin(blockIdx.x + 1, p.items, p.grid);
+    const int n = static_cast<int>(w1 - w0);
+    // (tile, quad) of the first item; later items advance it incrementally
+    // (a 64-bit division per item costs hundreds of cycles)
+    const int t_first = static_cast<int>(w0 / Q);
+    const int q_first = static_cast<int>(w0 - static_cast<long long>(t_first) * Q);
+    volatile int* abort_v = &abort_flag;
 
-    // -------------------------------- consumers -------------------------------
-    constexpr int kCT = kConsumerWarps * 32;
-    for (int i = tid; i < n_groups * 16; i += kCT) {
-        const int gl = i >> 4, m = i & 15;
-        float2 v = make_float2(0.0f, 0.0f);
-        if (m < p.M) {
-            const size_t idx = static_cast<size_t>(m) * p.G + g0 + gl;
-            v = make_float2(DOTS ? 0.0f : p.S[idx], static_cast<float>(p.T[idx]));
-        }
-        st_sm[i] = v;
-    }
-
-    const int gid = lane >> 2;
-    const int tq = lane & 3;
-    bool failed = false;
-    for (int b = 0; b < n_batches; ++b) {
-        const int tb0 = t0 + b * batch_tiles;
-        const int ntile = min(batch_tiles, t1 - tb0);
-        // this batch's weight scales, [row][group of the split]
-        if (!DOTS) {
-            pq2::named_bar_sync(1, kCT);  // previous batch done with ws_sm
-            // one warp per row, lanes over the split's groups, 4 rows in flight
-            const int rows = ntile * 16;
-            for (int r0 = warp * 4; r0 < rows; r0 += kConsumerWarps * 4)
-                for (int c0 = 0; c0 < n_groups; c0 += 32) {
-                    const int gl = c0 + lane;
-                    __half v[4];
+    if (warp == 0) {
+        // -------------------------------- producer --------------------------------
+        // Weight scales of rows 4*lane .. 4*lane+3 of an item's tile, its 4
+        // groups, are read kWsAhead items before they are stored into the
+        // item's stage, so the loads' latency overlaps (raw fp16 registers;
+        // the loop is unrolled so that each slot is a fixed register set:
+        // moving a register whose load is in flight would wait for it).
+        unsigned short wraw[kWsAhead][16];
+        auto load_ws = [&](int i, int t, int q, unsigned short (&v)[16]) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int n = tb0 * 16 + r0 + u;
-                        v[u] = (r0 + u < rows && n < p.N && gl < n_groups)
-                                   ? p.ws[static_cast<size_t>(n) * p.G + g0 + gl]
-                                   : __float2half(0.0f);
-                    }
+            for (int j = 0; j < 16; ++j) v[j] = 0;
+            if (DOTS || i >= n) return;
+            const unsigned short* wsu = reinterpret_cast<const unsigned short*>(p.ws);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (r0 + u < rows && gl < n_groups)
-                            ws_sm[(r0 + u) * p.max_groups_per_split + gl] = v[u];
+            for (int j = 0; j < 4; ++j) {
+                const int row = t * kRows + 4 * lane + j;
+                if (row >= p.N) continue;
+#pragma unroll
+                for (int gq = 0; gq < kGQ; ++gq) {
+                    const int g = q * kGQ + gq;
+                    if (g < G) v[4 * gq + j] = wsu[static_cast<size_t>(row) * G + g];
                 }
-        }
-        pq2::named_bar_sync(1, kCT);
-        float acc[kTilesPerWarp][NT][4];
-#pragma unroll
-        for (int j = 0; j < kTilesPerWarp; ++j)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[j][nt][e] = 0.0f;
-
-        for (int gs = 0; gs < n_gstages; ++gs) {
-            const int i = b * n_gstages + gs;
-            const int slot = i % p.stages;
-            if (!failed &&
-                !pq2::mbar_wait_bounded(&full[slot], (i / p.stages) & 1, p.ctl, abort_flag)) {
-                failed = true;
-                *abort_flag = 1;
             }
-            uint8_t* cst = ring + static_cast<size_t>(slot) * p.stage_bytes;
-            const uint8_t* qst = cst + p.codes_stage_bytes;
-            uint32_t* fst = reinterpret_cast<uint32_t*>(cst + p.codes_stage_bytes + p.qp_stage_bytes);
-            const int ga = g0 + gs * p.GC;
-            const int gcs = min(p.GC, g1 - ga);
+        };
+        int tl = t_first, ql = q_first;  // item of the next weight-scale load
+        int tp = t_first, qi = q_first;  // item being issued
+#pragma unroll
+        for (int k = 0; k < kWsAhead; ++k) {
+            load_ws(k, tl, ql, wraw[k]);
+            if (++ql == Q) { ql = 0; ++tl; }
+        }
+        int s = 0;
+        uint32_t ph = 0;
+        int issued = 0;
+        bool stop = false;
+        for (int it0 = 0; it0 < n && !stop; it0 += kWsAhead) {
+#pragma unroll
+            for (int k = 0; k < kWsAhead; ++k) {
+                const int it = it0 + k;
+                if (it >= n) break;
+                bool ok = true;
+                if (it >= kStages) ok = pq2::mbar_wait_warp(&sfree[s], ph ^ 1u, p.ctl, abort_v);
+                if (!ok) {
+                    stop = true;
+                    break;
+                }
+                issued = it + 1;
+                const int t = tp, q = qi;
+                if (++qi == Q) { qi = 0; ++tp; }
+                uint8_t* st = stage0 + static_cast<size_t>(s) * kStageBytes;
+                if (lane == 0 && it != p.ctl.debug_skip_stage) {
+                    pq2::mbar_arrive_expect_tx(&full[s], kTmaBytes);
+                    pq2::tma_load_2d(st, &p.tm_codes, q * 128, t * kRows, &full[s]);
+                    pq2::tma_load_2d(st + kTokOff, &p.tm_tok, 0, q * kGQ * 2 * kTok, &full[s]);
+                    pq2::bulk_g2s(st + kStOff, p.st16 + static_cast<size_t>(q) * kGQ * kTok,
+                                  kGQ * kTok * 8, &full[s]);
+                }
+                if (!DOTS) {
+                    // ws area: [group][row] fp32
+                    float* wss = reinterpret_cast<float*>(st + kWsOff);
+#pragma unroll
+                    for (int gq = 0; gq < kGQ; ++gq)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            wss[gq * kRows + 4 * lane + j] =
+                                __half2float(__ushort_as_half(wraw[k][4 * gq + j]));
+                }
+                if (it != p.ctl.debug_skip_stage) pq2::mbar_arrive(&full[s]);
+                load_ws(it + kWsAhead, tl, ql, wraw[k]);
+                if (++ql == Q) { ql = 0; ++tl; }
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        // drain: every armed stage must have landed before exit
+        if (lane == 0) {
+            for (int k = 0; k < kStages; ++k) {
+                if (issued <= k) continue;
+                int last = k + ((issued - 1 - k) / kStages) * kStages;
+                if (last == p.ctl.debug_skip_stage) last -= kStages;
+                if (last >= 0) pq2::mbar_wait_bounded(&full[k], (last / kStages) & 1, p.ctl);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            int s = 0, b = 0;
+            uint32_t ps = 0, pb = 0;
+            int done = 0;
+            for (int it = 0; it < n; ++it) {
+                if (!pq2::mbar_wait_bounded(&full[s], ps, p.ctl, abort_v) ||
+                    !pq2::mbar_wait_bounded(&aready[b], pb, p.ctl, abort_v) ||
+                    (it >= kBufs && !pq2::mbar_wait_bounded(&dfree[b], pb ^ 1u, p.ctl, abort_v))) {
+                    *abort_v = 1;
+                    break;
+                }
+                tc_fence_after();
+                // descriptor of the stage's first token tile; the start
+                // address field (bits 0..13, address >> 4) of the others is
+                // this one's plus the offset >> 4 (no carry: addresses < 256 KB)
+                const uint64_t desc0 = sw128_desc(stage0_s + s * kStageBytes + kTokOff);
+                // k-step outer, group inner: consecutive MMAs write different
+                // accumulators, so they do not wait on one another
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                    for (int gq = 0; gq < kGQ; ++gq)
+                        mma_f8_ta(tmem + kDCol0 + (b * kGQ + gq) * kGCols,
+                                  tmem + (b * kGQ + gq) * kGCols + 8 * k,
+                                  desc0 + ((gq * kTokGroupBytes + 32 * k) >> 4), k > 0);
+                }
+                mma_commit(&dfull[b]);
+                done = it + 1;
+                if (++s == kStages) { s = 0; ps ^= 1u; }
+                if (++b == kBufs) { b = 0; pb ^= 1u; }
+            }
+            // no MMA may still be running when tensor memory is released
+            if (done > 0)
+                pq2::mbar_wait_bounded(&dfull[(done - 1) % kBufs], ((done - 1) / kBufs) & 1, p.ctl);
+        }
+    } else {
+        // -------------------------------- workers --------------------------------
+        const int wi = warp - 2;          // 0..15
+        const int quad = warp & 3;        // TMEM lane quadrant of this warp
+        const int wq = wi >> 2;           // 0..3: the group it expands, its tokens 4wq..4wq+3
+        const int r = quad * 32 + lane;   // weight row within the tile
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        const int lead = (wi == 0);       // warp 2: counters and flags
+        bool failed = false;
+        float acc[kTokPerWarp];
+#pragma unroll
+        for (int j = 0; j < kTokPerWarp; ++j) acc[j] = 0.0f;
+        int xs = 0, xb = 0;               // expansion: stage, buffer
+        uint32_t xps = 0;
+        int es = 0, eb = 0;               // epilogue: stage, buffer
+        uint32_t epb = 0;
+        int te = t_first, qe = q_first;   // epilogue item
+
+        for (int step = 0; step <= n; ++step) {
+            // ---- expansion of group wq of item `step` ----
+            if (step < n) {
+                // warp-uniform waits: the tensor-memory accesses below are .sync.aligned
+                if (!failed && !pq2::mbar_wait_warp(&full[xs], xps, p.ctl, abort_v)) {
+                    failed = true;
+                    *abort_v = 1;
+                }
+                // A buffer xb was last read by the MMAs of item step-2, which
+                // this warp's own epilogue of that item (one step ago) already
+                // waited for: no further wait before rewriting it
+                if (!failed) {
+                    // 16-byte chunks 2wq, 2wq+1 of the row, 128-byte swizzled
+                    const uint32_t crow = stage0_s + xs * kStageBytes + r * 128;
+                    const uint4 lo4 = pq2::lds_v4(crow + (((2 * wq) ^ (r & 7)) << 4));
+                    const uint4 hi4 = pq2::lds_v4(crow + (((2 * wq + 1) ^ (r & 7)) << 4));
+                    const uint32_t w[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+                    // plane s of word j -> column 8s + j of the group's 32
+                    uint32_t v0[16], v1[16];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        v0[j] = w[j] & 0x03030303u;
+                        v0[8 + j] = (w[j] >> 2) & 0x03030303u;
+                        v1[j] = (w[j] >> 4) & 0x03030303u;
+                        v1[8 + j] = (w[j] >> 6) & 0x03030303u;
+                    }
+                    const uint32_t acol = tmem + lane_off + (xb * kGQ + wq) * kGCols;
+                    tmem_st16(acol, v0);
+                    tmem_st16(acol + 16, v1);
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) pq2::mbar_arrive(&aready[xb]);
+                if (++xs == kStages) { xs = 0; xps ^= 1u; }
+                if (++xb == kBufs) xb = 0;
+            }
+
+            // ---- epilogue of item `step - 1`, tokens 4wq..4wq+3 ----
+            const int e = step - 1;
+            if (e < 0) continue;
+            const int t = te, q = qe;
+            const bool tile_end = (qe + 1 == Q);
+            if (++qe == Q) { qe = 0; ++te; }
+            if (!failed && !pq2::mbar_wait_warp(&dfull[eb], epb, p.ctl, abort_v)) {
+                failed = true;
+                *abort_v = 1;
+            }
+            // D columns 8wq .. 8wq+7 of each group: hi of the 4 tokens, then lo
+            float dv[kGQ][8];
             if (!failed) {
-                // B fragments of this stage's groups from the staged activations:
-                // frag word ((((gl*NT + nt)*4 + s)*2 + h)*32 + lane)*2 + r
-                // one thread per activation word, in the staged row-major order
-                // qst[m][gl*32 + s*8 + 2*tid + r] (conflict-free reads)
-                const int words_per_row = p.GC * 32;
-                const int nwords = NT * 8 * words_per_row;
-                for (int w = tid; w < nwords; w += kCT) {
-                    const int m = w / words_per_row;
-                    const int c = w - m * words_per_row;
-                    const int gl = c >> 5;
-                    if (gl >= gcs) continue;
-                    const int s = (c >> 3) & 3;
-                    const int tq2 = (c >> 1) & 3;
-                    const int r = c & 1;
-                    const uint32_t qw = reinterpret_cast<const uint32_t*>(qst)[w];
-                    uint32_t hw, lw;
-                    split_word(qw, (s & 1) != 0, &hw, &lw);
-                    const int nt = m >> 3;
-                    const int ln = ((m & 7) << 2) | tq2;
-                    const int base = (((gl * NT + nt) * 4 + s) * 2) * 64 + ln * 2 + r;
-                    fst[base] = hw;
-                    fst[base + 64] = lw;
-                }
-            }
-            const bool any_fail = pq2::named_bar_any(1, kCT, failed);
-            if (any_fail) {
-                failed = true;
+                tc_fence_after();
+#pragma unroll
+                for (int gq = 0; gq < kGQ; ++gq)
+                    tmem_ld8(tmem + lane_off + kDCol0 + (eb * kGQ + gq) * kGCols + 8 * wq, dv[gq]);
+                tmem_wait_ld();
             } else {
-                for (int gl = 0; gl < gcs; ++gl) {
-                    const int g = ga + gl;
-                    uint32_t bf[NT][4][2][2];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
+                for (int gq = 0; gq < kGQ; ++gq)
 #pragma unroll
-                        for (int s = 0; s < 4; ++s)
+                    for (int j = 0; j < 8; ++j) dv[gq][j] = 0.0f;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) pq2::mbar_arrive(&dfree[eb]);
+            if (++eb == kBufs) { eb = 0; epb ^= 1u; }
+            const uint32_t es_s = stage0_s + es * kStageBytes;
+            const int row = t * kRows + r;
+            if (!failed) {
 #pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const uint2 v = reinterpret_cast<const uint2*>(
-                                    fst + (((gl * NT + nt) * 4 + s) * 2 + h) * 64)[lane];
-                                bf[nt][s][h][0] = v.x;
-                                bf[nt][s][h][1] = v.y;
-                            }
-                    float s_tok[NT][2], t_tok[NT][2];
+                for (int gq = 0; gq < kGQ; ++gq) {
+                    // (512 s, s t) of the 4 tokens (dots: (0, t)), weight scale of this row
+                    const uint32_t sta = es_s + kStOff + gq * kTok * 8 + wq * 32;
+                    const uint4 st01 = pq2::lds_v4(sta), st23 = pq2::lds_v4(sta + 16);
+                    const float sv[4] = {__uint_as_float(st01.x), __uint_as_float(st01.z),
+                                         __uint_as_float(st23.x), __uint_as_float(st23.z)};
+                    const float tv[4] = {__uint_as_float(st01.y), __uint_as_float(st01.w),
+                                         __uint_as_float(st23.y), __uint_as_float(st23.w)};
+                    const float wsv =
+                        DOTS ? 0.0f : pq2::lds_f32(es_s + kWsOff + 4 * (gq * kRows + r));
+                    const int g = q * kGQ + gq;
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const float4 st = *reinterpret_cast<const float4*>(
-                            &st_sm[(g - g0) * 16 + nt * 8 + 2 * tq]);
-                        s_tok[nt][0] = st.x;
-                        t_tok[nt][0] = st.y;
-                        s_tok[nt][1] = st.z;
-                        t_tok[nt][1] = st.w;
-                    }
-                    // A fragments of this warp's tiles for this group
-                    uint32_t a[kTilesPerWarp][4][4];
-                    bool tv[kTilesPerWarp];
-#pragma unroll
-                    for (int j = 0; j < kTilesPerWarp; ++j) {
-                        const int tb = warp + kConsumerWarps * j;
-                        tv[j] = tb < ntile;
-                        const int ra = (tv[j] ? tb : 0) * 16 + gid;
-                        uint32_t oa = static_cast<uint32_t>(ra) * p.GC * 32 + gl * 32 + 8 * tq;
-                        uint32_t ob = oa + 8u * p.GC * 32;
-                        if (p.swizzle) {  // 16-byte chunk index ^= row % 8
-                            oa ^= ((oa >> 7) & 7u) << 4;
-                            ob ^= ((ob >> 7) & 7u) << 4;
-                        }
-                        const uint2 c0 = *reinterpret_cast<const uint2*>(cst + oa);
-                        const uint2 c1 = *reinterpret_cast<const uint2*>(cst + ob);
-                        const uint32_t s0x = c0.x >> 4, s0y = c0.y >> 4, s1x = c1.x >> 4,
-                                       s1y = c1.y >> 4;
-                        a[j][0][0] = c0.x & 0x03030303u; a[j][0][1] = c1.x & 0x03030303u;
-                        a[j][0][2] = c0.y & 0x03030303u; a[j][0][3] = c1.y & 0x03030303u;
-                        a[j][1][0] = c0.x & 0x0C0C0C0Cu; a[j][1][1] = c1.x & 0x0C0C0C0Cu;
-                        a[j][1][2] = c0.y & 0x0C0C0C0Cu; a[j][1][3] = c1.y & 0x0C0C0C0Cu;
-                        a[j][2][0] = s0x & 0x03030303u;  a[j][2][1] = s1x & 0x03030303u;
-                        a[j][2][2] = s0y & 0x03030303u;  a[j][2][3] = s1y & 0x03030303u;
-                        a[j][3][0] = s0x & 0x0C0C0C0Cu;  a[j][3][1] = s1x & 0x0C0C0C0Cu;
-                        a[j][3][2] = s0y & 0x0C0C0C0Cu;  a[j][3][3] = s1y & 0x0C0C0C0Cu;
-                    }
-                    // MMAs issued tile-interleaved: consecutive MMAs are independent
-                    float d[kTilesPerWarp][NT][4];
-#pragma unroll
-                    for (int j = 0; j < kTilesPerWarp; ++j)
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) d[j][nt][e] = 0.0f;
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-#pragma unroll
-                            for (int j = 0; j < kTilesPerWarp; ++j)
-#pragma unroll
-                                for (int nt = 0; nt < NT; ++nt)
-                                    if (tv[j]) mma_e4m3(d[j][nt], a[j][s], bf[nt][s][h][0], bf[nt][s][h][1]);
-#pragma unroll
-                    for (int j = 0; j < kTilesPerWarp; ++j) {
-                        if (!tv[j]) continue;
-                        const int ra = (warp + kConsumerWarps * j) * 16 + gid;
-                        float wsa = 0.0f, wsb = 0.0f;
-                        if (!DOTS) {
-                            wsa = __half2float(ws_sm[ra * p.max_groups_per_split + (g - g0)]);
-                            wsb = __half2float(ws_sm[(ra + 8) * p.max_groups_per_split + (g - g0)]);
-                        }
-                        const int na = tb0 * 16 + ra;  // global rows
-                        const int nb = na + 8;
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            // exact integer group dots, then the fp32 group term
-                            const float dot0 = fmaf(d[j][nt][0], 512.0f, -t_tok[nt][0]);
-                            const float dot1 = fmaf(d[j][nt][1], 512.0f, -t_tok[nt][1]);
-                            const float dot2 = fmaf(d[j][nt][2], 512.0f, -t_tok[nt][0]);
-                            const float dot3 = fmaf(d[j][nt][3], 512.0f, -t_tok[nt][1]);
-                            if (DOTS) {
-                                const int m0 = nt * 8 + 2 * tq;
-                                const size_t G = p.G;
-                                if (m0 < p.M && na < p.N)
-                                    p.dots[(static_cast<size_t>(m0) * p.N + na) * G + g] = static_cast<int>(dot0);
-                                if (m0 + 1 < p.M && na < p.N)
-                                    p.dots[(static_cast<size_t>(m0 + 1) * p.N + na) * G + g] = static_cast<int>(dot1);
-                                if (m0 < p.M && nb < p.N)
-                                    p.dots[(static_cast<size_t>(m0) * p.N + nb) * G + g] = static_cast<int>(dot2);
-                                if (m0 + 1 < p.M && nb < p.N)
-                                    p.dots[(static_cast<size_t>(m0 + 1) * p.N + nb) * G + g] = static_cast<int>(dot3);
-                            } else {
-                                acc[j][nt][0] = fmaf(dot0 * s_tok[nt][0], wsa, acc[j][nt][0]);
-                                acc[j][nt][1] = fmaf(dot1 * s_tok[nt][1], wsa, acc[j][nt][1]);
-                                acc[j][nt][2] = fmaf(dot2 * s_tok[nt][0], wsb, acc[j][nt][2]);
-                                acc[j][nt][3] = fmaf(dot3 * s_tok[nt][1], wsb, acc[j][nt][3]);
-                            }
+                    for (int j = 0; j < kTokPerWarp; ++j) {
+                        // D_hi + D_lo = 2^-9 dot(codes, q): exact (both multiples of 2^-9)
+                        const float d = dv[gq][j] + dv[gq][4 + j];
+                        if (DOTS) {
+                            const int m = 4 * wq + j;
+                            const float dot = fmaf(d, 512.0f, -tv[j]);  // exact integer
+                            if (m < p.M && row < p.N && g < G)
+                                p.dots[(static_cast<size_t>(m) * p.N + row) * G + g] =
+                                    static_cast<int>(dot);
+                        } else {
+                            // (dot(codes, q) - t) * s = d * 512 s - s t
+                            acc[j] = fmaf(fmaf(d, sv[j], -tv[j]), wsv, acc[j]);
                         }
                     }
                 }
             }
             __syncwarp();
-            if (lane == 0) pq2::mbar_arrive(&empty[slot]);
-        }
-        if (failed) continue;  // keep the barrier schedule; nothing is written
-        if (!DOTS) {
-            float* out = p.out + static_cast<size_t>(ks) * p.M * p.N;
+            if (lane == 0) pq2::mbar_arrive(&sfree[es]);  // the item's stage is consumed
+            if (++es == kStages) es = 0;
+
+            // ---- end of this CTA's part of row tile t: flush ----
+            const bool seg_end = (e == n - 1) || tile_end;
+            if (!seg_end) continue;
+            if (pq2::named_bar_any(1, kWorkerThreads, failed)) {
+                if (lead && lane == 0) *abort_v = 1;
+                break;
+            }
+            if (!DOTS) {
+                const int c_lo = owner_of(static_cast<long long>(t) * Q, p.items, p.grid);
+                const int c_hi = owner_of(static_cast<long long>(t + 1) * Q - 1, p.items, p.grid);
+                if (c_lo == c_hi) {
+                    // the whole tile is this CTA's: straight to y
+                    if (row < p.N) {
 #pragma unroll
-            for (int j = 0; j < kTilesPerWarp; ++j) {
-                const int tb = warp + kConsumerWarps * j;
-                if (tb >= ntile) break;
-                const int na = (tb0 + tb) * 16 + gid;
-                const int nb = na + 8;
+                        for (int j = 0; j < kTokPerWarp; ++j) {
+                            const int m = 4 * wq + j;
+                            if (m < p.M) p.y[static_cast<size_t>(m) * p.N + row] = acc[j];
+                        }
+                    }
+                } else {
+                    float* part = p.partial + static_cast<size_t>(blockIdx.x + t) * p.M * kRows;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int m0 = nt * 8 + 2 * tq;
-                    if (m0 < p.M) {
-                        if (na < p.N) out[static_cast<size_t>(m0) * p.N + na] = acc[j][nt][0];
-                        if (nb < p.N) out[static_cast<size_t>(m0) * p.N + nb] = acc[j][nt][2];
+                    for (int j = 0; j < kTokPerWarp; ++j) {
+                        const int m = 4 * wq + j;
+                        if (m < p.M) part[static_cast<size_t>(m) * kRows + r] = acc[j];
                     }
-                    if (m0 + 1 < p.M) {
-                        if (na < p.N) out[static_cast<size_t>(m0 + 1) * p.N + na] = acc[j][nt][1];
-                        if (nb < p.N) out[static_cast<size_t>(m0 + 1) * p.N + nb] = acc[j][nt][3];
+                    __threadfence();
+                    pq2::named_bar_sync(2, kWorkerThreads);
+                    if (lead && lane == 0) {
+                        const unsigned old = atomicAdd(&p.counters[t], 1u);
+                        last_flag = (old == static_cast<unsigned>(c_hi - c_lo)) ? 1 : 0;
                     }
+                    pq2::named_bar_sync(2, kWorkerThreads);
+                    if (last_flag) {
+                        __threadfence();
+                        // per contributor, in CTA order, the loads are issued
+                        // together (one L2 round trip each)
+                        float sum[kTokPerWarp];
+#pragma unroll
+                        for (int j = 0; j < kTokPerWarp; ++j) sum[j] = 0.0f;
+                        for (int c = c_lo; c <= c_hi; ++c) {
+                            const float* pc = p.partial + static_cast<size_t>(c + t) * p.M * kRows + r;
+                            float v[kTokPerWarp];
+#pragma unroll
+                            for (int j = 0; j < kTokPerWarp; ++j) {
+                                const int m = 4 * wq + j;
+                                v[j] = m < p.M ? ld_cg(pc + static_cast<size_t>(m) * kRows) : 0.0f;
+                            }
+#pragma unroll
+                            for (int j = 0; j < kTokPerWarp; ++j) sum[j] += v[j];
+                        }
+                        if (row < p.N) {
+#pragma unroll
+                            for (int j = 0; j < kTokPerWarp; ++j) {
+                                const int m = 4 * wq + j;
+                                if (m < p.M) p.y[static_cast<size_t>(m) * p.N + row] = sum[j];
+                            }
+                        }
+                    }
+                    // last_flag is rewritten at the next flush only after
+                    // every worker has passed the first barrier there
                 }
+#pragma unroll
+                for (int j = 0; j < kTokPerWarp; ++j) acc[j] = 0.0f;
             }
         }
     }
-}
 
-// y[i] = sum over splits in order 0, 1, ..., KS-1 of P[split][i]
-__global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restrict__ P,
-                                                            float* __restrict__ y, int64_t n,
-                                                            int KS) {
-    pq2::pdl_wait();
-    pq2::pdl_launch_dependents();
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-         i += stride) {
-        float s = P[i];
-        for (int k = 1; k < KS; ++k) s += P[static_cast<int64_t>(k) * n + i];
-        y[i] = s;
-    }
+    // teardown: every role is done with tensor memory
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols));
 }
 
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
-struct SmallPlan {
-    int NT, KS, ctas_per_ks, n_tiles, GC, stages, batch_rows, box_rows, swizzle;
-    uint32_t stage_bytes, codes_stage_bytes, qp_stage_bytes;
-    int max_groups_per_split;
-    size_t smem;
-    size_t partial_bytes;
+struct SmallLayout {
+    int grid, n_tiles, Q;
+    long long items;
+    int64_t G4;
+    size_t tok, st16, counters, partial, total;  // byte offsets / total
 };
 
-SmallPlan plan_small(int64_t M, int64_t N, int64_t K, int num_sms) {
-    SmallPlan pl = {};
-    const int G = static_cast<int>(K / 128);
-    pl.NT = M <= 8 ? 1 : 2;
-    pl.n_tiles = static_cast<int>((N + 15) / 16);
-    // fewest K splits (<= 8) that still give every CTA >= 12 tiles of work
-    int KS = 1;
-    while (KS < 8 && static_cast<long long>(pl.n_tiles) * KS < 12LL * num_sms && G / (2 * KS) >= 2)
-        KS *= 2;
-    if (KS > G) KS = G;
-    pl.KS = KS;
-    pl.ctas_per_ks = num_sms / KS > 0 ? num_sms / KS : 1;
-    pl.max_groups_per_split = (G + KS - 1) / KS;
-    const int tiles_per_cta = (pl.n_tiles + pl.ctas_per_ks - 1) / pl.ctas_per_ks;
-    const int bt = tiles_per_cta < kBatchTiles ? tiles_per_cta : kBatchTiles;
-    pl.batch_rows = bt * 16;
-    // a TMA box holds at most 256 rows: one box, or two equal halves
-    pl.box_rows = pl.batch_rows <= 256 ? pl.batch_rows : pl.batch_rows / 2;
-    int GC = 4;
-    if (GC > pl.max_groups_per_split) GC = pl.max_groups_per_split;
-    pl.GC = GC;
-    pl.swizzle = GC == 4 ? 1 : 0;
-    pl.codes_stage_bytes = static_cast<uint32_t>(pl.batch_rows * GC * 32);
-    pl.qp_stage_bytes = static_cast<uint32_t>(16 * GC * 128);
-    pl.stage_bytes = (pl.codes_stage_bytes + pl.qp_stage_bytes +
-                      static_cast<uint32_t>(GC * pl.NT * kFragBytesPerGroupTile) + 1023u) & ~1023u;
-    auto head = [&](int stages) {
-        return (16 * static_cast<size_t>(stages) + 16 +
-                static_cast<size_t>(pl.max_groups_per_split) * 16 * 8 +
-                static_cast<size_t>(pl.batch_rows) * pl.max_groups_per_split * 2 + 127) &
-               ~static_cast<size_t>(127);
-    };
-    int stages = static_cast<int>((206 * 1024 - head(4)) / pl.stage_bytes);
-    if (stages > 4) stages = 4;
-    if (stages < 2) stages = 2;
-    pl.stages = stages;
-    pl.smem = head(stages) + 1024 + static_cast<size_t>(stages) * pl.stage_bytes;
-    pl.partial_bytes = KS > 1 ? align256(static_cast<size_t>(KS) * M * N * 4) : 0;
-    return pl;
-}
-
-template <int NT, bool DOTS>
-cudaError_t launch_main(const SmallParams& p, const SmallPlan& pl, cudaStream_t st) {
-    auto kern = small_kernel<NT, DOTS>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(pl.smem));
-    if (e != cudaSuccess) return e;
-    return pq2h::launch(kern, dim3(pl.KS * pl.ctas_per_ks), dim3((kConsumerWarps + 1) * 32), pl.smem,
-                        st, true, p);
+SmallLayout layout_small(int64_t M, int64_t N, int64_t K, int num_sms) {
+    SmallLayout l = {};
+    const int64_t G = K / 128;
+    l.Q = static_cast<int>((G + kGQ - 1) / kGQ);
+    l.G4 = static_cast<int64_t>(l.Q) * kGQ;
+    l.n_tiles = static_cast<int>((N + kRows - 1) / kRows);
+    l.items = static_cast<long long>(l.n_tiles) * l.Q;
+    long long grid = num_sms < kMaxGrid ? num_sms : kMaxGrid;
+    if (grid > l.items) grid = l.items;
+    l.grid = static_cast<int>(grid);
+    size_t off = 0;
+    l.tok = off;
+    off += align256(static_cast<size_t>(l.G4) * kTokGroupBytes);
+    l.st16 = off;
+    off += align256(static_cast<size_t>(l.G4) * kTok * 8);
+    l.counters = off;
+    off += align256(static_cast<size_t>(l.n_tiles) * 4);
+    l.partial = off;
+    // one [M][128] slot per (CTA c, tile t) pair, at index c + t
+    off += align256(static_cast<size_t>(l.grid + l.n_tiles) * M * kRows * 4);
+    l.total = off;
+    return l;
 }
 
 }  // namespace
 
 namespace pq2h {
 
-// Exact scratch (split-K partial sums) for this shape on a device with
-// num_sms multiprocessors.
 size_t small_scratch_bytes(int64_t M, int64_t N, int64_t K, int num_sms) {
-    return plan_small(M, N, K, num_sms).partial_bytes;
+    return layout_small(M, N, K, num_sms).total;
 }
 
-// Device-independent upper bound: partial sums for the largest split count
-// the planner uses (8).
+// Device-independent: the size for the largest grid any device gets.
 size_t small_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    (void)K;
-    return align256(static_cast<size_t>(8) * M * N * 4);
+    return small_scratch_bytes(M, N, K, kMaxGrid);
 }
 
 cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
                          const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
                          int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                          const DeviceInfo& dev) {
-    const SmallPlan pl = plan_small(M, N, K, dev.num_sms);
-    if (pl.smem > static_cast<size_t>(dev.max_smem_optin)) return cudaErrorInvalidConfiguration;
-    float* partial = static_cast<float*>(workspace);
+    if (M < 1 || M > kTok) return cudaErrorInvalidValue;
+    const SmallLayout l = layout_small(M, N, K, dev.num_sms);
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    uint32_t* tok = reinterpret_cast<uint32_t*>(w + l.tok);
+    float2* st16 = reinterpret_cast<float2*>(w + l.st16);
+    unsigned* counters = reinterpret_cast<unsigned*>(w + l.counters);
+    {
+        const int64_t words = l.G4 * kTok * 32;
+        const int64_t want = (words + 255) / 256;
+        const int grid = static_cast<int>(want < dev.num_sms * 4 ? want : dev.num_sms * 4);
+        cudaError_t e = launch(small_prep_kernel, dim3(grid), dim3(256), 0, st, true, qp, S, T, tok,
+                               st16, counters, M, K, l.G4, l.n_tiles);
+        if (e != cudaSuccess) return e;
+    }
     SmallParams p = {};
-    if (!encode_tmap_2d(&p.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, codes,
-                        static_cast<uint64_t>(K / 16), static_cast<uint64_t>(N),
-                        static_cast<uint64_t>(K / 4), static_cast<uint32_t>(pl.GC * 8),
-                        static_cast<uint32_t>(pl.box_rows), pl.swizzle != 0))
+    if (!encode_tmap_2d(&p.tm_tok, CU_TENSOR_MAP_DATA_TYPE_UINT8, tok, 128u,
+                        static_cast<uint64_t>(l.G4) * 2 * kTok, 128u, 128u, kRows, true) ||
+        !encode_tmap_2d(&p.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes,
+                        static_cast<uint64_t>(K / 4), static_cast<uint64_t>(N),
+                        static_cast<uint64_t>(K / 4), 128u, kRows, true))
         return cudaErrorInvalidValue;
-    if (!encode_tmap_2d(&p.tm_qp, CU_TENSOR_MAP_DATA_TYPE_UINT32, qp, static_cast<uint64_t>(K / 4),
-                        static_cast<uint64_t>(M), static_cast<uint64_t>(K),
-                        static_cast<uint32_t>(pl.GC * 32), 16u, false))
-        return cudaErrorInvalidValue;
+    p.st16 = st16;
     p.ws = ws;
-    p.S = S;
-    p.T = T;
-    p.out = (pl.KS > 1 && !dots) ? partial : y;
+    p.y = y;
     p.dots = dots;
+    p.partial = reinterpret_cast<float*>(w + l.partial);
+    p.counters = counters;
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
     p.G = static_cast<int>(K / 128);
-    p.KS = pl.KS;
-    p.ctas_per_ks = pl.ctas_per_ks;
-    p.n_tiles = pl.n_tiles;
-    p.GC = pl.GC;
-    p.stages = pl.stages;
-    p.batch_rows = pl.batch_rows;
-    p.box_rows = pl.box_rows;
-    p.stage_bytes = pl.stage_bytes;
-    p.codes_stage_bytes = pl.codes_stage_bytes;
-    p.qp_stage_bytes = pl.qp_stage_bytes;
-    p.max_groups_per_split = pl.max_groups_per_split;
-    p.swizzle = pl.swizzle;
+    p.Q = l.Q;
+    p.n_tiles = l.n_tiles;
+    p.grid = l.grid;
+    p.items = l.items;
     p.ctl = ctl;
-    cudaError_t e;
-    if (pl.NT == 1)
-        e = dots ? launch_main<1, true>(p, pl, st) : launch_main<1, false>(p, pl, st);
-    else
-        e = dots ? launch_main<2, true>(p, pl, st) : launch_main<2, false>(p, pl, st);
-    if (e != cudaSuccess || dots || pl.KS == 1) return e;
-    const int64_t n = M * N;
-    const int64_t want = (n + 255) / 256;
-    const int grid = static_cast<int>(want < dev.num_sms * 8 ? want : dev.num_sms * 8);
-    return launch(reduce_splits_kernel, dim3(grid), dim3(256), 0, st, true,
-                  static_cast<const float*>(partial), y, n, pl.KS);
+    const size_t smem = 1024 + static_cast<size_t>(kStages) * kStageBytes;
+    auto kern = dots ? small_kernel<true> : small_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch(kern, dim3(l.grid), dim3(kThreads), smem, st, true, p);
 }
 
 }  // namespace pq2h
