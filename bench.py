@@ -85,6 +85,47 @@ def workload_spec(args):
     raise SystemExit(f"unknown workload {w}")
 
 
+# Sources whose compiled code a workload's dominant kernel comes from; the
+# DRAM traffic recorded in profiles/dram_traffic.txt is used only while their
+# hash matches the one recorded with it.
+KERNEL_SOURCES = {
+    "gemv": ["pq2_gemv.cu", "pq2_common.cuh"],
+    "small": ["pq2_small.cu", "pq2_common.cuh"],
+    "prefill": ["pq2_prefill.cu", "pq2_common.cuh"],
+}
+
+
+def kernel_family(layer):
+    M = layer[0][0]
+    return "gemv" if M == 1 else ("small" if M <= 16 else "prefill")
+
+
+def sources_hash(family):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[family]:
+        with open(os.path.join(ROOT, "gemm_pq2_ternary_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, family):
+    """DRAM bytes per launch of the dominant kernel from one ncu capture
+    (profiles/dram_traffic.txt: workload, kernel family, sources hash, bytes),
+    or None when absent or when the kernel's sources changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = sources_hash(family)
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == workload \
+                    and parts[1] == family and parts[2] == want:
+                return int(parts[3])
+    return None
+
+
 def per_layer_units(layer, kind):
     """Algorithmic bytes (GB/s workloads) or int8-equivalent ops (TOPS) of one
     layer, and the dominant kernel's share."""
@@ -296,12 +337,14 @@ def gpu_arm(args, rank, world, dist):
     if kind == "GB/s":
         achieved = per_launch / (mm_per_launch_ms * 1e-3) * 1e-9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": None,
+                "frac": round(achieved / hbm, 4),
+                "traffic": recorded_traffic(name, kernel_family(layer)),
                 "peak_source": f"{peak_src}: MEASURED_PEAKS.json hbm_gbs (copy)"}
     else:
         achieved = per_launch / (mm_per_launch_ms * 1e-3) * 1e-12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
-                "frac": round(achieved / bf16, 4), "traffic": None,
+                "frac": round(achieved / bf16, 4),
+                "traffic": recorded_traffic(name, kernel_family(layer)),
                 "peak_source": f"{peak_src}: MEASURED_PEAKS.json bf16_tflops (burst)"}
 
     e2e = None
