@@ -373,6 +373,181 @@ __global__ void __launch_bounds__((GPT == 1 ? kMaxConsumersSmall : kMaxConsumers
     }
 }
 
+// ---------------------------------------------------------------------------
+// Direct variant (one group per thread, rows of a CTA that fit its row-sum
+// buffer): no shared-memory ring.  Right after the wait every consumer thread
+// issues 16-byte global loads for the code words and weight scales of its
+// next kLookahead rows, so all of a CTA's weight requests are in flight at
+// once and overlap the activation copy and quantisation; each later row's
+// loads go out kLookahead rows ahead of its dot.  (Measured on GB300: a 55 KB
+// per-SM weight slice landed about 1 us sooner this way than through bulk
+// copies into a ring.)
+// ---------------------------------------------------------------------------
+constexpr int kLookahead = 4;
+constexpr int kDirectConsumers = 480;  // <= 128 registers: the look-ahead slots stay in registers
+constexpr size_t kDirectMaxSmem = 160 * 1024;  // else the ring variant (row sums in chunks)
+
+template <bool DOTS, bool FUSED>
+__global__ void __launch_bounds__(kDirectConsumers + 32, 1) gemv_direct_kernel(const GemvParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* abar = reinterpret_cast<uint64_t*>(smem);  // activations landed (fused)
+    int8_t* qsm = reinterpret_cast<int8_t*>(smem + p.act_off);  // group g at g * kQStride
+    float* ssm = reinterpret_cast<float*>(smem + p.act_off + kQStride * p.G);
+    int32_t* tsm = reinterpret_cast<int32_t*>(smem + p.act_off + kQStride * p.G + 4 * p.G);
+    float* red = reinterpret_cast<float*>(smem + p.red_off);
+    // fused path: x is staged over the row-sum buffer (quantised before any
+    // term is written there)
+    const __half* xsm = reinterpret_cast<const __half*>(smem + p.red_off);
+
+    const int n_begin = blockIdx.x * p.rows_per_cta;
+    const int rows = min(p.N, n_begin + p.rows_per_cta) - n_begin;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = p.TC >> 5;
+    if (FUSED && tid == 0) {
+        pq2::mbar_init(abar, 1);
+        pq2::fence_mbar_init();
+    }
+    __syncthreads();
+    // activations, scales and (possibly) weights may come from the preceding
+    // kernel: wait for it before reading any of them
+    pq2::pdl_wait();
+    pq2::pdl_launch_dependents();
+    if (rows <= 0) return;
+    if (tid >= p.TC) {
+        if (FUSED && tid == p.TC) {
+            pq2::mbar_arrive_expect_tx(abar, 2u * p.K);
+            pq2::bulk_g2s(smem + p.red_off, p.x, 2u * p.K, abar);
+            pq2::mbar_wait_bounded(abar, 0, p.ctl);  // no copy in flight at exit
+        }
+        return;
+    }
+
+    const int rp = tid / p.GT;
+    const int gi = tid - rp * p.GT;
+    const bool active = rp < p.RP;
+    const int hswap = (tid >> 2) & 1;
+    const int nk = active && rp < rows ? (rows - rp + p.RP - 1) / p.RP : 0;  // my rows
+    const uint8_t* cbase = p.codes + static_cast<size_t>(n_begin + rp) * p.codes_row_bytes + gi * 32;
+    const size_t cstep = static_cast<size_t>(p.RP) * p.codes_row_bytes;
+    const unsigned short* wbase =
+        reinterpret_cast<const unsigned short*>(p.ws) + static_cast<size_t>(n_begin + rp) * p.G + gi;
+    const size_t wstep = static_cast<size_t>(p.RP) * p.G;
+    // fixed register slots (loops unrolled by kLookahead; nothing is moved
+    // or spilled between a load and its use, so the loads stay in flight)
+    uint4 c0[kLookahead], c1[kLookahead];
+    unsigned short wr[kLookahead];
+#pragma unroll
+    for (int j = 0; j < kLookahead; ++j) {
+        c0[j] = make_uint4(0u, 0u, 0u, 0u);
+        c1[j] = c0[j];
+        wr[j] = 0;
+        if (j < nk) {
+            const uint8_t* cw = cbase + j * cstep;
+            c0[j] = pq2::ld_nc_v4(cw + 16 * hswap);
+            c1[j] = pq2::ld_nc_v4(cw + 16 * (hswap ^ 1));
+            if (!DOTS) wr[j] = wbase[j * wstep];
+        }
+    }
+
+    // activations: quantised here (fused) or read as they are
+    const int8_t* qsrc = p.qp;
+    int qstride = 128;
+    const float* ssrc = p.S;
+    const int32_t* tsrc = p.T;
+    if (FUSED) {
+        bool failed = !pq2::mbar_wait_bounded(abar, 0, p.ctl);
+        // the quantiser shuffles within the warp: decide per warp
+        failed = __any_sync(0xffffffffu, failed);
+        if (!failed) {
+            const int j = lane & 7;
+            for (int g0 = warp * 4; g0 < p.G; g0 += nwarps * 4) {
+                const int g = g0 + (lane >> 3);
+                const bool valid = g < p.G;
+                const int gl = valid ? g : g0;
+                const uint4* src = reinterpret_cast<const uint4*>(xsm + gl * 128 + 16 * j);
+                const uint4 h[2] = {src[0], src[1]};
+                pq2::quantize_group8(h, j, valid, qsm + gl * kQStride, ssm + gl, tsm + gl);
+            }
+        }
+        if (pq2::named_bar_any(2, p.TC, failed)) return;
+        qsrc = qsm;
+        qstride = kQStride;
+        ssrc = ssm;
+        tsrc = tsm;
+    }
+    const int gl = active ? gi : 0;
+    uint32_t q[32];
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(qsrc + static_cast<size_t>(gl) * qstride);
+        const uint32_t src_s = pq2::smem_u32(qsm) + gl * kQStride;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            // plane v/2, words 4*(v&1)..+3; stored at the half this thread reads first
+            const uint4 w = FUSED ? pq2::lds_v4(src_s + 16 * (v ^ hswap)) : src[v ^ hswap];
+            q[4 * v + 0] = w.x;
+            q[4 * v + 1] = w.y;
+            q[4 * v + 2] = w.z;
+            q[4 * v + 3] = w.w;
+        }
+    }
+    const float s64 = DOTS ? 0.0f : ssrc[gl] * 0.015625f;  // exact scaling by 2^-6
+    const int t64 = -64 * tsrc[gl];
+
+    // rows rp, rp + RP, ...: the dot of row k, then the loads of row k + kLookahead
+    const uint32_t red_s = pq2::smem_u32(red);
+    for (int k0 = 0; k0 < nk; k0 += kLookahead) {
+#pragma unroll
+        for (int j = 0; j < kLookahead; ++j) {
+            const int k = k0 + j;
+            if (k >= nk) break;
+            const uint32_t w[8] = {c0[j].x, c0[j].y, c0[j].z, c0[j].w,
+                                   c1[j].x, c1[j].y, c1[j].z, c1[j].w};
+            const int dot64 = pq2::group_codes_dot64(w, q, t64);
+            const int r = rp + k * p.RP;
+            if (DOTS) {
+                p.dots[static_cast<size_t>(n_begin + r) * p.G + gi] = dot64 >> 6;  // exact
+            } else {
+                // float(dot64) exactly (|dot64| < 2^22) by the 1.5 * 2^23 bit trick
+                const float dotf = __fsub_rn(__int_as_float(0x4B400000 + dot64), 12582912.0f);
+                pq2::sts_f32(red_s + 4u * (r * p.GT + gi),
+                             dotf * s64 * __half2float(__ushort_as_half(wr[j])));
+            }
+            if (k + kLookahead < nk) {
+                const uint8_t* cw = cbase + (k + kLookahead) * cstep;
+                c0[j] = pq2::ld_nc_v4(cw + 16 * hswap);
+                c1[j] = pq2::ld_nc_v4(cw + 16 * (hswap ^ 1));
+                if (!DOTS) wr[j] = wbase[(k + kLookahead) * wstep];
+            }
+        }
+    }
+    if (DOTS) return;
+    pq2::named_bar_sync(1, p.TC);
+    // row sums: 8 lanes per row, each over a fixed stride of the row's terms,
+    // then a fixed 3-step butterfly (the same order as the ring variant)
+    const int sub = lane & 7;
+    for (int rb = warp * 4; rb < rows; rb += nwarps * 4) {
+        const int r = rb + (lane >> 3);
+        float sum = 0.0f;
+        if (r < rows)
+            for (int c = sub; c < p.GT; c += 8) sum += pq2::lds_f32(red_s + 4u * (r * p.GT + c));
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        if (sub == 0 && r < rows) p.y[n_begin + r] = sum;
+    }
+}
+
+template <bool DOTS, bool FUSED>
+cudaError_t launch_direct(const GemvParams& p, int grid, size_t smem, cudaStream_t st) {
+    auto kern = gemv_direct_kernel<DOTS, FUSED>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return pq2h::launch(kern, dim3(grid), dim3(p.TC + 32), smem, st, true, p);
+}
+
 template <int GPT, bool WS_SMEM, bool DOTS, bool FUSED>
 cudaError_t launch_variant(const GemvParams& p, int grid, size_t smem, cudaStream_t st) {
     auto kern = gemv_kernel<GPT, WS_SMEM, DOTS, FUSED>;
@@ -395,9 +570,11 @@ cudaError_t launch_gpt(const GemvParams& p, int grid, size_t smem, bool ws_smem,
 }
 
 // Tuning knobs (environment, read once): PQ2_GEMV_CTAS_PER_SM (default 1),
-// PQ2_GEMV_RING_KB (default 160), PQ2_GEMV_STAGE_KB (default 16),
+// PQ2_GEMV_THREADS (consumer threads at most, default and cap 672 for one
+// group per thread), PQ2_GEMV_RING_KB (default 160), PQ2_GEMV_STAGE_KB (default 16),
 // PQ2_GEMV_PREFETCH (1 = on; 2 = off, default: with one CTA per SM the
-// prefetch only queues ahead of the ring copies).
+// prefetch only queues ahead of the ring copies), PQ2_GEMV_DIRECT (1 = the
+// direct variant where it applies, default; 2 = always the ring variant).
 int env_int(const char* name, int dflt) {
     const char* v = std::getenv(name);
     if (!v || !*v) return dflt;
@@ -406,13 +583,16 @@ int env_int(const char* name, int dflt) {
 }
 
 struct Tuning {
-    int ctas_per_sm, ring_kb, stage_kb, prefetch;
+    int ctas_per_sm, threads, ring_kb, stage_kb, prefetch, direct;
 };
 
 const Tuning& tuning() {
-    static const Tuning t = {env_int("PQ2_GEMV_CTAS_PER_SM", 1), env_int("PQ2_GEMV_RING_KB", 160),
+    static const Tuning t = {env_int("PQ2_GEMV_CTAS_PER_SM", 1),
+                             env_int("PQ2_GEMV_THREADS", kMaxConsumersSmall),
+                             env_int("PQ2_GEMV_RING_KB", 160),
                              env_int("PQ2_GEMV_STAGE_KB", 16),
-                             env_int("PQ2_GEMV_PREFETCH", 2) == 1 ? 1 : 0};
+                             env_int("PQ2_GEMV_PREFETCH", 2) == 1 ? 1 : 0,
+                             env_int("PQ2_GEMV_DIRECT", 1) == 1 ? 1 : 0};
     return t;
 }
 
@@ -455,7 +635,8 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const
     p.G = static_cast<int>(K / 128);
     const int gpt = p.G <= kMaxConsumersSmall ? 1 : (p.G <= 2 * kMaxConsumersLarge ? 2 : 4);
     p.GT = (p.G + gpt - 1) / gpt;
-    const int max_tc = gpt == 1 ? kMaxConsumersSmall : kMaxConsumersLarge;
+    int max_tc = gpt == 1 ? kMaxConsumersSmall : kMaxConsumersLarge;
+    if (tu.threads >= 32 && tu.threads < max_tc) max_tc = tu.threads;
     p.RP = max_tc / p.GT > 0 ? max_tc / p.GT : 1;
     p.TC = ((p.RP * p.GT + 31) / 32) * 32;
     p.codes_row_bytes = static_cast<uint32_t>(K / 4);
@@ -483,6 +664,28 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const
     const int grid = static_cast<int>((N + rows_per_cta - 1) / rows_per_cta);
     p.ctl = ctl;
     p.prefetch = tu.prefetch;
+    // (the stage-withholding test hook needs the ring variant's waits)
+    if (gpt == 1 && tu.direct && ctl.debug_skip_stage < 0) {
+        // direct variant: at most kDirectConsumers threads; shared memory is
+        // barrier | activations (fused) | row-sum buffer for all of the CTA's
+        // rows (the fused path stages x there first)
+        GemvParams d = p;
+        const int dtc = max_tc < kDirectConsumers ? max_tc : kDirectConsumers;
+        d.RP = dtc / d.GT > 0 ? dtc / d.GT : 1;
+        d.TC = ((d.RP * d.GT + 31) / 32) * 32;
+        if (d.TC <= kDirectConsumers) {
+            d.act_off = 128;
+            d.red_off = align128(d.act_off + (d.x ? static_cast<size_t>(kQStride + 8) * d.G : 0));
+            size_t red = static_cast<size_t>(rows_per_cta) * d.GT * 4;
+            if (d.x && red < 2 * static_cast<size_t>(d.K)) red = 2 * static_cast<size_t>(d.K);
+            const size_t dsmem = d.red_off + red;
+            if (dsmem <= kDirectMaxSmem && dsmem <= static_cast<size_t>(dev.max_smem_optin)) {
+                if (dots) return launch_direct<true, false>(d, grid, dsmem, st);
+                if (d.x) return launch_direct<false, true>(d, grid, dsmem, st);
+                return launch_direct<false, false>(d, grid, dsmem, st);
+            }
+        }
+    }
     size_t smem = layout(p);
     while (smem > static_cast<size_t>(dev.max_smem_optin) && p.stages > 2) {
         --p.stages;
