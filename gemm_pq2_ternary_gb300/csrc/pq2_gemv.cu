@@ -8,7 +8,19 @@
 // of dot * s * ws; and, from page "Chasing llama.cpp at batch one", section
 // "The win: a program just for one token": no token dimension at all.
 //
-// GB300 layout of the work (not the pages' tiling):
+// GB300 layout of the work (not the pages' tiling).  Two variants share the
+// arithmetic and the row-sum order, so they give bit-identical y:
+//  * Direct variant (gemv_direct_kernel, the default wherever a CTA's row
+//    sums fit in shared memory): one CTA per SM, up to 15 consumer warps.
+//    Right after the dependency wait every thread issues 16-byte
+//    non-coherent global loads for the codes and weight scales of its next
+//    four rows into fixed register slots, so all of a CTA's weight requests
+//    are in flight while the activations are copied and quantised; each
+//    later row is requested four rows ahead of its dot.  No ring, no
+//    per-stage barrier: at 8 MB per call the ring's data movement and
+//    synchronisation, not the arithmetic, set the time.
+//  * Ring variant (gemv_kernel: very long rows, or more rows per CTA than the
+//    shared row-sum array holds), described by the rest of this list.
 //  * One CTA per SM (up to 21 consumer warps), each owning a contiguous
 //    range of output rows.  Many warps per SM hide the latency of the shared
 //    loads and DP4A chains.  Programmatic dependent launch lets each CTA,
