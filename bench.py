@@ -227,6 +227,12 @@ def build_layers(args, layer, R, device):
     return layers, X, Y
 
 
+def weight_flags(pq2, args):
+    """The step's weights are uploaded once and never written again, so the
+    calls may declare them static (PQ2_WEIGHTS_STATIC) unless --weights default."""
+    return pq2.PQ2_WEIGHTS_STATIC if args.weights == "static" else 0
+
+
 def run_matmul(pq2, p):
     if p["op"] == pq2.PQ2_OP_GEMV:
         pq2.pq2_gemv(p["qp"], p["S"], p["T"], p["codes"], p["ws"], p["y"])
@@ -236,15 +242,15 @@ def run_matmul(pq2, p):
         pq2.pq2_gemm_prefill(p["qp"], p["S"], p["T"], p["codes"], p["ws"], p["y"], p["wsp"])
 
 
-def step_fn(pq2, layers, matmul_only=False):
-    """One pass: per projection, M = 1 runs pq2_matmul (the fused quantise +
+def step_fn(pq2, layers, matmul_only=False, flags=0):
+    """One pass: per projection, M = 1 runs pq2_matmul_ex (the fused quantise +
     GEMV kernel); M > 1 runs pq2_quantize_act then the matmul kernel (the
     matmul alone when matmul_only)."""
     def fn():
         for projs in layers:
             for p in projs:
                 if p["M"] == 1:
-                    pq2.pq2_matmul(p["x"], p["codes"], p["ws"], p["y"], p["mmws"])
+                    pq2.pq2_matmul_ex(p["x"], p["codes"], p["ws"], p["y"], flags, p["mmws"])
                     continue
                 if not matmul_only:
                     pq2.pq2_quantize_act(p["x"], p["qp"], p["S"], p["T"])
@@ -292,8 +298,9 @@ def gpu_arm(args, rank, world, dist):
     layers, X, Y = build_layers(args, layer, R, device)
 
     stream = torch.cuda.Stream(device)
-    g_step = capture(torch, step_fn(pq2, layers), stream)
-    g_mm = capture(torch, step_fn(pq2, layers, matmul_only=True), stream)
+    flags = weight_flags(pq2, args)
+    g_step = capture(torch, step_fn(pq2, layers, flags=flags), stream)
+    g_mm = capture(torch, step_fn(pq2, layers, matmul_only=True, flags=flags), stream)
     assert pq2.pq2_last_device_error(stream) == pq2.PQ2_OK
 
     # A step replays the R-layer graph `reps` times, so the timed region
@@ -368,6 +375,9 @@ def gpu_arm(args, rank, world, dist):
                             "for M=1, quantise then matmul otherwise), programmatic dependent "
                             "launch",
                    "arith": "int8 activations x 2-bit ternary codes, int32 group dots, fp32 sums",
+                   "weights": ("static: M = 1 calls pass PQ2_WEIGHTS_STATIC (weights uploaded once; "
+                               "each call may read them before the preceding call ends)"
+                               if args.weights == "static" else "default ordering"),
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "matmul_us_per_launch": round(mm_per_launch_ms * 1e3, 3),
@@ -379,10 +389,11 @@ def gpu_arm(args, rank, world, dist):
 
 
 def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dist, device):
-    """The same metric through pq2_matmul (the public call, eager) with host
+    """The same metric through pq2_matmul_ex (the public call, eager) with host
     buffers: every pass copies all activations in from pinned host memory
     and all outputs back, inside the timed region (CUDA events on the
     stream)."""
+    flags = weight_flags(pq2, args)
     Xh = [x.cpu().pin_memory() for x in X]
     Yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in Y]
     h2d = sum(x.numel() * x.element_size() for x in Xh)
@@ -393,7 +404,7 @@ def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dis
         for x, xh in zip(X, Xh):
             x.copy_(xh, non_blocking=True)
         for p in projs:
-            pq2.pq2_matmul(p["x"], p["codes"], p["ws"], p["y"], p["mmws"])
+            pq2.pq2_matmul_ex(p["x"], p["codes"], p["ws"], p["y"], flags, p["mmws"])
         for y, yh in zip(Y, Yh):
             yh.copy_(y, non_blocking=True)
 
@@ -418,7 +429,7 @@ def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dis
     return {"value": round(units_pass * world / dt * scale, 2), "unit": kind,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(dt * 1e3, 4),
-            "step": "one pass over all projections: copy in, pq2_matmul each, copy out"}
+            "step": "one pass over all projections: copy in, pq2_matmul_ex each, copy out"}
 
 
 # ---------------------------------------------------------------------------
@@ -502,6 +513,9 @@ def main():
     ap.add_argument("--projections", type=int, default=0, help="weight sets per step (0: auto)")
     ap.add_argument("--reps", type=int, default=0,
                     help="passes over the R weight sets per step (0: auto, >= 1.5 s timed)")
+    ap.add_argument("--weights", default="static", choices=["static", "default"],
+                    help="static: M = 1 calls pass PQ2_WEIGHTS_STATIC (weights read before the "
+                         "preceding call ends); default: plain pq2_matmul ordering")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -27,11 +27,14 @@ PQ2_OP_SMALL = 1
 PQ2_OP_PREFILL = 2
 PQ2_OP_MATMUL = 3
 
+PQ2_WEIGHTS_STATIC = 1
+
 SIZE_MAX = ctypes.c_size_t(-1).value
 
 # Exported names and argument types (every one declared in include/pq2.h,
 # plus the undocumented test hook pq2_debug_skip_stage).
 _P, _I64, _SZ, _I, _U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint64
+_U32 = ctypes.c_uint32
 SIGNATURES = {
     "pq2_status_string": ([_I], ctypes.c_char_p),
     "pq2_version": ([], ctypes.c_char_p),
@@ -41,6 +44,7 @@ SIGNATURES = {
     "pq2_gemm_small": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _I),
     "pq2_gemm_prefill": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _I),
     "pq2_matmul": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _I),
+    "pq2_matmul_ex": ([_P, _P, _P, _P, _I64, _I64, _I64, _U32, _P, _SZ, _P], _I),
     "pq2_workspace_bytes": ([_I, _I64, _I64, _I64], _SZ),
     "pq2_group_dots": ([_I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _SZ, _P], _I),
     "pq2_last_device_error": ([_P], _I),
@@ -185,6 +189,14 @@ def pq2_matmul(x, codes, ws, y, workspace, stream=None):
     wp, wb = _ws(workspace)
     _check(_lib.pq2_matmul(_ptr(x), _ptr(codes), _ptr(ws), _ptr(y), M, N, K, wp, wb,
                            _stream(stream)), "pq2_matmul")
+
+
+def pq2_matmul_ex(x, codes, ws, y, flags, workspace, stream=None):
+    M, K = x.shape
+    N = codes.shape[0]
+    wp, wb = _ws(workspace)
+    _check(_lib.pq2_matmul_ex(_ptr(x), _ptr(codes), _ptr(ws), _ptr(y), M, N, K, flags, wp, wb,
+                              _stream(stream)), "pq2_matmul_ex")
 
 
 def pq2_group_dots(op, qp, T, codes, dots, workspace=None, stream=None):

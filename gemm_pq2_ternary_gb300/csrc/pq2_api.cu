@@ -285,6 +285,13 @@ pq2_status pq2_gemm_prefill(const int8_t* qp, const float* S, const int32_t* T,
 pq2_status pq2_matmul(const void* x_f16, const uint8_t* codes, const void* ws_f16, float* y,
                       int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
                       void* stream) {
+    return pq2_matmul_ex(x_f16, codes, ws_f16, y, M, N, K, 0u, workspace, workspace_bytes, stream);
+}
+
+pq2_status pq2_matmul_ex(const void* x_f16, const uint8_t* codes, const void* ws_f16, float* y,
+                         int64_t M, int64_t N, int64_t K, uint32_t flags, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    if (flags & ~PQ2_WEIGHTS_STATIC) return PQ2_ERR_INVALID_ARG;
     pq2_status s = check_nk(N, K);
     if (s != PQ2_OK) return s;
     if (M < 1 || !x_f16 || !codes || !ws_f16 || !y) return PQ2_ERR_INVALID_ARG;
@@ -300,7 +307,7 @@ pq2_status pq2_matmul(const void* x_f16, const uint8_t* codes, const void* ws_f1
         return cuda_status(pq2h::launch_gemv(static_cast<const __half*>(x_f16), nullptr, nullptr,
                                              nullptr, codes, static_cast<const __half*>(ws_f16),
                                              y, nullptr, N, K, static_cast<cudaStream_t>(stream),
-                                             c.ctl, c.dev));
+                                             c.ctl, c.dev, (flags & PQ2_WEIGHTS_STATIC) != 0));
     }
     if (!workspace || workspace_bytes < need) return PQ2_ERR_WORKSPACE;
     if (!aligned16(workspace)) return PQ2_ERR_MISALIGNED;

@@ -79,7 +79,10 @@ struct GemvParams {
     uint32_t stage_bytes;      // ring slot size (codes + ws, 16-aligned)
     uint32_t codes_row_bytes;  // K / 4
     uint32_t act_off, red_off, ring_off;  // shared-memory layout
+    uint32_t ws_off;                      // staged variant: weight scales
     int prefetch;              // L2 prefetch of the CTA's weights before the wait
+    int trigger;               // staged variant: 0 trigger dependents after the wait,
+                               // 1 after the activations are quantised, 2 after the dots
     pq2::DevCtl ctl;
 };
 
@@ -560,6 +563,198 @@ cudaError_t launch_direct(const GemvParams& p, int grid, size_t smem, cudaStream
     return pq2h::launch(kern, dim3(grid), dim3(p.TC + 32), smem, st, true, p);
 }
 
+// ---------------------------------------------------------------------------
+// Staged variant (gemv_staged_kernel): for weights the caller declares static
+// (not written by the work that precedes the call on its stream).  The CTA's
+// whole weight slice is copied into shared memory BEFORE the dependency wait,
+// one bulk copy per code row plus one for the weight scales.  Two CTAs fit on
+// an SM, so under programmatic dependent launch the next call's CTA stages
+// its slice while this one computes: the weight stream of call i+1 overlaps
+// the quantisation, dots and row sums of call i.
+// Work split: 48 teams of 8 lanes.  A team quantises one group into its own
+// shared slot (no barrier across warps), then lane j of the team computes the
+// group's terms for rows j, j+8, ... (or, when groups are fewer than teams,
+// for rows j, j+8*tpg, ... across the tpg teams given the same group).  Code
+// rows sit 16 bytes further apart than K/4, so the eight rows an 8-lane phase
+// reads fall on eight distinct 16-byte bank groups.  Terms, their order and
+// the row sums are those of the other variants: y is bit-identical.
+// ---------------------------------------------------------------------------
+constexpr int kStagedThreads = 384;
+constexpr int kStagedTeams = kStagedThreads / 8;
+constexpr uint32_t kStagedPad = 16;             // extra bytes between staged code rows
+constexpr size_t kStagedMaxSmem = 100 * 1024;   // two CTAs per SM
+constexpr size_t kStagedMinSlice = 16 * 1024;   // smaller per-CTA slices: the direct variant
+
+__device__ __forceinline__ uint4 ld_cg_v4(const void* ptr) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
+}
+
+__global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const GemvParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* wbar = reinterpret_cast<uint64_t*>(smem);  // the weight slice has landed
+    const int n_begin = blockIdx.x * p.rows_per_cta;
+    const int rows = min(p.N, n_begin + p.rows_per_cta) - n_begin;
+    const int tid = threadIdx.x;
+    const uint32_t rowb = p.codes_row_bytes;
+    const uint32_t rs = rowb + kStagedPad;
+    if (tid == 0) {
+        pq2::mbar_init(wbar, 1);
+        pq2::fence_mbar_init();
+    }
+    __syncthreads();
+    const bool ws_bulk = p.G % 8 == 0;  // then every slice of scales is 16-byte aligned
+    if (rows > 0) {
+        if (tid == 0)
+            pq2::mbar_arrive_expect_tx(
+                wbar, static_cast<uint32_t>(rows) * (rowb + (ws_bulk ? 2u * p.G : 0u)));
+        __syncthreads();
+        for (int r = tid; r < rows; r += kStagedThreads)
+            pq2::bulk_g2s(smem + p.ring_off + r * rs,
+                          p.codes + static_cast<size_t>(n_begin + r) * rowb, rowb, wbar);
+        const unsigned short* wsg = reinterpret_cast<const unsigned short*>(p.ws) +
+                                    static_cast<size_t>(n_begin) * p.G;
+        if (ws_bulk) {
+            if (tid == kStagedThreads - 1)
+                pq2::bulk_g2s(smem + p.ws_off, wsg, static_cast<uint32_t>(rows) * p.G * 2u, wbar);
+        } else {
+            unsigned short* wss = reinterpret_cast<unsigned short*>(smem + p.ws_off);
+            for (int i = tid; i < rows * p.G; i += kStagedThreads) wss[i] = wsg[i];
+            __syncthreads();
+        }
+    }
+    // x comes from the preceding kernel: wait for it before reading it
+    pq2::pdl_wait();
+    if (p.trigger == 0 || rows <= 0) pq2::pdl_launch_dependents();
+    if (rows <= 0) return;
+
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    bool failed = false;
+    const int team = tid >> 3;
+    const int j = tid & 7;
+    const int tpg = p.G < kStagedTeams ? kStagedTeams / p.G : 1;  // teams per group
+    const int gstep = kStagedTeams / tpg;                         // groups per pass
+    const int gslot = team / tpg;
+    const int li = (team - gslot * tpg) * 8 + j;  // lane index within the group's lanes
+    const int lstep = 8 * tpg;
+    const bool tactive = gslot < gstep;
+    int8_t* qslot = reinterpret_cast<int8_t*>(smem + p.act_off) + team * kQStride;
+    float* sslot = reinterpret_cast<float*>(smem + p.act_off + kQStride * kStagedTeams) + team;
+    int32_t* tslot = reinterpret_cast<int32_t*>(smem + p.act_off + (kQStride + 4) * kStagedTeams) + team;
+    const uint32_t qslot_s = pq2::smem_u32(qslot);
+    const uint32_t codes_s = pq2::smem_u32(smem + p.ring_off);
+    const uint32_t ws_s = pq2::smem_u32(smem + p.ws_off);
+    const uint32_t red_s = pq2::smem_u32(smem + p.red_off);
+    const int passes = (p.G + gstep - 1) / gstep;  // uniform over the CTA
+    for (int pass = 0; pass < passes; ++pass) {
+        const int g = gslot + pass * gstep;
+        const bool valid = tactive && g < p.G;
+        const int gl = valid ? g : 0;
+        {
+            const __half* src = p.x + static_cast<size_t>(gl) * 128 + 16 * j;
+            const uint4 h[2] = {ld_cg_v4(src), ld_cg_v4(src + 8)};
+            pq2::quantize_group8(h, j, valid, qslot, sslot, tslot);
+        }
+        if (pass == 0 && p.trigger == 1) pq2::pdl_launch_dependents();
+        __syncwarp();
+        uint32_t q[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            const uint4 w = pq2::lds_v4(qslot_s + 16 * v);
+            q[4 * v + 0] = w.x;
+            q[4 * v + 1] = w.y;
+            q[4 * v + 2] = w.z;
+            q[4 * v + 3] = w.w;
+        }
+        const float s64 = pq2::lds_f32(pq2::smem_u32(sslot)) * 0.015625f;  // exact scaling by 2^-6
+        const int t64 = -64 * *tslot;
+        // the weights were requested before the dependency wait; by now they
+        // have usually landed (every warp waits on its own; a warp whose wait
+        // runs out computes nothing and the CTA writes no y)
+        if (pass == 0) failed = !pq2::mbar_wait_warp(wbar, 0, p.ctl);
+        const int nk = !failed && valid && li < rows ? (rows - li + lstep - 1) / lstep : 0;
+        const uint32_t cs = codes_s + li * rs + gl * 32;
+        const uint32_t cstep = lstep * rs;
+        const uint32_t wsa = ws_s + 2u * (li * p.G + gl);
+        const uint32_t wstep = 2u * lstep * p.G;
+        // rows li, li + lstep, ...: the next row's codes and scale are requested
+        // before this row's dot
+        uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
+        uint32_t wv = 0;
+        if (nk > 0) {
+            c0 = pq2::lds_v4(cs);
+            c1 = pq2::lds_v4(cs + 16);
+            wv = pq2::lds_u16(wsa);
+        }
+        for (int k = 0; k < nk; ++k) {
+            uint4 n0 = c0, n1 = c1;
+            uint32_t nw = wv;
+            if (k + 1 < nk) {
+                const uint32_t a = cs + (k + 1) * cstep;
+                n0 = pq2::lds_v4(a);
+                n1 = pq2::lds_v4(a + 16);
+                nw = pq2::lds_u16(wsa + (k + 1) * wstep);
+            }
+            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            const int dot64 = pq2::group_codes_dot64(w, q, t64);
+            // float(dot64) exactly (|dot64| < 2^22) by the 1.5 * 2^23 bit trick
+            const float dotf = __fsub_rn(__int_as_float(0x4B400000 + dot64), 12582912.0f);
+            const float wsf = __half2float(__ushort_as_half(static_cast<unsigned short>(wv)));
+            pq2::sts_f32(red_s + 4u * ((li + k * lstep) * p.G + g), dotf * s64 * wsf);
+            c0 = n0;
+            c1 = n1;
+            wv = nw;
+        }
+        __syncwarp();  // the slot is rewritten by the next pass
+    }
+    if (p.trigger == 2) pq2::pdl_launch_dependents();
+    if (__syncthreads_or(failed)) {
+        if (tid == 0) pq2::mbar_wait_bounded(wbar, 0, p.ctl);  // no copy in flight at exit
+        return;
+    }
+    // row sums: 8 lanes per row, each over a fixed stride of the row's terms,
+    // then a fixed 3-step butterfly (the same order as the other variants)
+    const int sub = lane & 7;
+    constexpr int nwarps = kStagedThreads / 32;
+    for (int rb = warp * 4; rb < rows; rb += nwarps * 4) {
+        const int r = rb + (lane >> 3);
+        float sum = 0.0f;
+        if (r < rows)
+            for (int c = sub; c < p.G; c += 8) sum += pq2::lds_f32(red_s + 4u * (r * p.G + c));
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        if (sub == 0 && r < rows) p.y[n_begin + r] = sum;
+    }
+}
+
+// Shared memory of the staged variant: barrier | codes rows (padded) | weight
+// scales | per-team activation slots (q, s, t) | terms.  0 if it does not fit.
+size_t staged_layout(GemvParams& p) {
+    const size_t rows = static_cast<size_t>(p.rows_per_cta);
+    p.ring_off = 128;
+    const size_t codes = rows * (p.codes_row_bytes + kStagedPad);
+    p.ws_off = static_cast<uint32_t>((p.ring_off + codes + 127) & ~static_cast<size_t>(127));
+    const size_t wsz = rows * p.G * 2;
+    p.act_off = static_cast<uint32_t>((p.ws_off + wsz + 127) & ~static_cast<size_t>(127));
+    const size_t act = static_cast<size_t>(kQStride + 8) * kStagedTeams;
+    p.red_off = static_cast<uint32_t>((p.act_off + act + 127) & ~static_cast<size_t>(127));
+    const size_t total = p.red_off + rows * p.G * 4;
+    if (rows * p.codes_row_bytes < kStagedMinSlice) return 0;
+    return total <= kStagedMaxSmem ? total : 0;
+}
+
+cudaError_t launch_staged(const GemvParams& p, int grid, size_t smem, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_staged_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return pq2h::launch(gemv_staged_kernel, dim3(grid), dim3(kStagedThreads), smem, st, true, p);
+}
+
 template <int GPT, bool WS_SMEM, bool DOTS, bool FUSED>
 cudaError_t launch_variant(const GemvParams& p, int grid, size_t smem, cudaStream_t st) {
     auto kern = gemv_kernel<GPT, WS_SMEM, DOTS, FUSED>;
@@ -586,7 +781,10 @@ cudaError_t launch_gpt(const GemvParams& p, int grid, size_t smem, bool ws_smem,
 // group per thread), PQ2_GEMV_RING_KB (default 160), PQ2_GEMV_STAGE_KB (default 16),
 // PQ2_GEMV_PREFETCH (1 = on; 2 = off, default: with one CTA per SM the
 // prefetch only queues ahead of the ring copies), PQ2_GEMV_DIRECT (1 = the
-// direct variant where it applies, default; 2 = always the ring variant).
+// direct variant where it applies, default; 2 = always the ring variant),
+// PQ2_GEMV_TRIGGER (staged variant: 1 = let the next kernel launch right
+// after the wait, default; 2 = after the activations are quantised; 3 =
+// after the dots).
 int env_int(const char* name, int dflt) {
     const char* v = std::getenv(name);
     if (!v || !*v) return dflt;
@@ -595,7 +793,7 @@ int env_int(const char* name, int dflt) {
 }
 
 struct Tuning {
-    int ctas_per_sm, threads, ring_kb, stage_kb, prefetch, direct;
+    int ctas_per_sm, threads, ring_kb, stage_kb, prefetch, direct, trigger;
 };
 
 const Tuning& tuning() {
@@ -604,7 +802,8 @@ const Tuning& tuning() {
                              env_int("PQ2_GEMV_RING_KB", 160),
                              env_int("PQ2_GEMV_STAGE_KB", 16),
                              env_int("PQ2_GEMV_PREFETCH", 2) == 1 ? 1 : 0,
-                             env_int("PQ2_GEMV_DIRECT", 1) == 1 ? 1 : 0};
+                             env_int("PQ2_GEMV_DIRECT", 1) == 1 ? 1 : 0,
+                             env_int("PQ2_GEMV_TRIGGER", 1) - 1};
     return t;
 }
 
@@ -630,7 +829,8 @@ bool gemv_fused_supported(int64_t K) { return K <= kFusedMaxK; }
 
 cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const int32_t* T,
                         const uint8_t* codes, const __half* ws, float* y, int32_t* dots, int64_t N,
-                        int64_t K, cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev) {
+                        int64_t K, cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev,
+                        bool weights_static) {
     const Tuning& tu = tuning();
     GemvParams p = {};
     p.x = dots ? nullptr : x;
@@ -676,7 +876,14 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const
     const int grid = static_cast<int>((N + rows_per_cta - 1) / rows_per_cta);
     p.ctl = ctl;
     p.prefetch = tu.prefetch;
+    p.trigger = tu.trigger;
     // (the stage-withholding test hook needs the ring variant's waits)
+    if (weights_static && p.x && ctl.debug_skip_stage < 0) {
+        GemvParams sp = p;
+        const size_t ssmem = staged_layout(sp);
+        if (ssmem > 0 && ssmem <= static_cast<size_t>(dev.max_smem_optin))
+            return launch_staged(sp, grid, ssmem, st);
+    }
     if (gpt == 1 && tu.direct && ctl.debug_skip_stage < 0) {
         // direct variant: at most kDirectConsumers threads; shared memory is
         // barrier | activations (fused) | row-sum buffer for all of the CTA's

@@ -30,13 +30,17 @@ cudaError_t launch_pack(const int8_t* tern, uint8_t* codes, int64_t N, int64_t K
 // M == 1.  dots != nullptr selects the integer-dot debug output instead of y.
 // x != nullptr selects the fused path: the kernel quantises the fp16
 // activations itself (qp, S, T unused); only for K where
-// gemv_fused_supported(K).
+// gemv_fused_supported(K).  weights_static (fused path only): codes and ws
+// are not written by the work preceding the launch on `st`, so the kernel may
+// read them before its dependency wait.
 bool gemv_fused_supported(int64_t K);
 cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const int32_t* T,
                         const uint8_t* codes, const __half* ws, float* y, int32_t* dots, int64_t N,
-                        int64_t K, cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev);
+                        int64_t K, cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev,
+                        bool weights_static = false);
 
-// 2 <= M <= 16: tensor-core (mma.sync e4m3) kernel, split-K reduced in order.
+// 2 <= M <= 16: tcgen05 kernel with the weights expanded into tensor memory,
+// split-K partial sums reduced in a fixed order.
 // workspace: small_workspace_bytes(M, N, K) bytes.
 size_t small_workspace_bytes(int64_t M, int64_t N, int64_t K);
 size_t small_scratch_bytes(int64_t M, int64_t N, int64_t K, int num_sms);

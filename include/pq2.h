@@ -173,6 +173,29 @@ pq2_status pq2_matmul(const void* x_f16, const uint8_t* codes, const void* ws_f1
                       int64_t M, int64_t N, int64_t K,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* Flags of pq2_matmul_ex. */
+#define PQ2_WEIGHTS_STATIC 1u
+
+/*
+ * pq2_matmul_ex -- pq2_matmul with flags.  (The pages have no counterpart to
+ * the flag; it lets a decode loop overlap one call's weight stream with the
+ * preceding call's arithmetic.)
+ *   flags: 0 or PQ2_WEIGHTS_STATIC; other bits give PQ2_ERR_INVALID_ARG.
+ *   PQ2_WEIGHTS_STATIC: the caller promises that codes and ws_f16 are not
+ *     written by any operation enqueued on `stream` before this call that may
+ *     still be running when it starts (typically: weights packed or copied
+ *     once, then many calls).  The M == 1 fused kernel may then read them
+ *     before the preceding kernel on the stream has finished (programmatic
+ *     dependent launch).  x_f16 is still read only after that kernel is
+ *     done.  If the promise is broken, y is undefined.  Results are
+ *     bit-identical to pq2_matmul.  Paths other than the M == 1 fused one
+ *     ignore the flag.
+ *   Other arguments, workspace and errors as pq2_matmul.
+ */
+pq2_status pq2_matmul_ex(const void* x_f16, const uint8_t* codes, const void* ws_f16, float* y,
+                         int64_t M, int64_t N, int64_t K, uint32_t flags,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * pq2_workspace_bytes -- scratch bytes `op` needs for this shape (0 if none,
  * SIZE_MAX if the shape is not supported).

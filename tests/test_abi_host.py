@@ -100,6 +100,15 @@ def test_matmul_rejects_small_workspace(lib):
     assert st == b.PQ2_ERR_WORKSPACE
 
 
+def test_matmul_ex_rejects_unknown_flags(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    st = lib.pq2_matmul_ex(_p(FAKE), _p(FAKE), _p(FAKE), _p(FAKE), 1, 64, 128, 2, None, 0, None)
+    assert st == b.PQ2_ERR_INVALID_ARG
+    st = lib.pq2_matmul_ex(_p(FAKE), _p(FAKE), _p(FAKE), _p(FAKE), 4, 64, 128,
+                           b.PQ2_WEIGHTS_STATIC, _p(FAKE), 16, None)
+    assert st == b.PQ2_ERR_WORKSPACE
+
+
 def test_group_dots_rejects_bad_op(lib):
     from gemm_pq2_ternary_gb300 import binding as b
     st = lib.pq2_group_dots(7, _p(FAKE), _p(FAKE), _p(FAKE), 1, 8, 128, _p(FAKE), None, 0, None)

@@ -41,3 +41,96 @@ def test_fused_gemv_parity(prob):
     tol = oracle.fp32_tolerance(ref, A, prob.K // 128)
     err = np.abs(got - ref)
     assert np.all(err <= tol), f"max err {err.max()}"
+
+
+# Shapes for the static-weights path (staged where a CTA's weight slice is at
+# least 16 KB; PR1 and static_n1 stay on the direct variant): G < 48 groups
+# (several teams per group),
+# G not a multiple of 8 (scales staged by plain loads), G > 48 (two passes,
+# the second with only some teams busy), ragged N (short last CTA).
+STATIC_PROBS = [inputs.PR1, inputs.DECODE,
+                inputs.Problem("static_g8", 1, 1024, 10000, "p343", "outliers", 60),
+                inputs.Problem("static_g13", 1, 128 * 13, 6000, "p343", "outliers", 61),
+                inputs.Problem("static_g50", 1, 128 * 50, 2000, "uniform", "outliers", 62),
+                inputs.Problem("static_g96", 1, 128 * 96, 1000, "p343", "normal", 63),
+                inputs.Problem("static_n1", 1, 2048, 1, "uniform", "normal", 64)]
+
+
+def _oracle_check(prob, tern, ws, x, y):
+    oqp, oS, oT = oracle.quantize_act(x)
+    ref, A = oracle.matmul(oqp, oS, oracle.pack(tern), ws)
+    tol = oracle.fp32_tolerance(ref, A, prob.K // 128)
+    err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= tol), f"max err {err.max()}"
+
+
+@pytest.mark.parametrize("prob", STATIC_PROBS, ids=lambda p: p.name)
+def test_static_weights_match_default_path(prob):
+    """PQ2_WEIGHTS_STATIC (weights staged before the dependency wait) gives
+    bit-identical y to pq2_matmul, and y matches the oracle."""
+    from gemm_pq2_ternary_gb300 import binding as pq2
+    tern, ws, x = inputs.generate(prob)
+    codes, ws_d = pq2.pack(torch.from_numpy(tern).cuda(), torch.from_numpy(ws).cuda())
+    xd = torch.from_numpy(x).cuda()
+    torch.cuda.synchronize()  # the weights are complete before the static calls
+    y0 = torch.full((1, prob.N), float("nan"), device="cuda")
+    y1 = torch.full((1, prob.N), float("nan"), device="cuda")
+    pq2.pq2_matmul(xd, codes, ws_d, y0, None)
+    pq2.pq2_matmul_ex(xd, codes, ws_d, y1, pq2.PQ2_WEIGHTS_STATIC, None)
+    torch.cuda.synchronize()
+    assert pq2.pq2_last_device_error() == pq2.PQ2_OK
+    assert torch.equal(y0, y1)
+    if prob.N * prob.K <= 16 * 1024 * 1024:
+        _oracle_check(prob, tern, ws, x, y1)
+
+
+def test_static_weights_back_to_back():
+    """Several static-weight calls queued without synchronisation, eagerly and
+    replayed from a CUDA graph: each call's weights are read while the
+    previous call may still run, and its x only after that call is done (each
+    x is written by the kernel just before it)."""
+    from gemm_pq2_ternary_gb300 import binding as pq2
+    n_calls = 6
+    probs = [inputs.Problem(f"chain{i}", 1, 6144 if i % 2 == 0 else 4096,
+                            5120 if i % 2 == 0 else 4096, "p343", "outliers", 70 + i)
+             for i in range(n_calls)]
+    data = [inputs.generate(p) for p in probs]
+    dev = [pq2.pack(torch.from_numpy(t).cuda(), torch.from_numpy(w).cuda()) for t, w, _ in data]
+    xs = [torch.from_numpy(x).cuda() for _, _, x in data]
+    xs_live = [torch.empty_like(x) for x in xs]
+    torch.cuda.synchronize()
+    want = []
+    for (codes, ws_d), x, p in zip(dev, xs, probs):
+        y = torch.empty((1, p.N), device="cuda")
+        pq2.pq2_matmul(x, codes, ws_d, y, None)
+        want.append(y)
+    torch.cuda.synchronize()
+
+    def chain(outs):
+        for i, ((codes, ws_d), p) in enumerate(zip(dev, probs)):
+            xs_live[i].copy_(xs[i])  # x written by the kernel right before the call
+            pq2.pq2_matmul_ex(xs_live[i], codes, ws_d, outs[i], pq2.PQ2_WEIGHTS_STATIC, None)
+
+    outs = [torch.full((1, p.N), float("nan"), device="cuda") for p in probs]
+    chain(outs)
+    torch.cuda.synchronize()
+    assert pq2.pq2_last_device_error() == pq2.PQ2_OK
+    for a, b in zip(outs, want):
+        assert torch.equal(a, b)
+
+    gouts = [torch.full((1, p.N), float("nan"), device="cuda") for p in probs]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            chain(gouts)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        for o in gouts:
+            o.fill_(float("nan"))
+        g.replay()
+    torch.cuda.synchronize()
+    assert pq2.pq2_last_device_error() == pq2.PQ2_OK
+    for a, b in zip(gouts, want):
+        assert torch.equal(a, b)
