@@ -155,6 +155,17 @@ __device__ __forceinline__ bool mbar_spin_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// Warp-wide busy-polling wait (lane 0 spins with test_wait, the warp then
+// synchronises): for warps on the critical path of a pipeline, where a
+// sleeping poller would wake up late.  All 32 lanes must call it.
+__device__ __forceinline__ bool mbar_spin_warp(uint64_t* bar, uint32_t parity, const DevCtl& ctl,
+                                               volatile int* abort_flag = nullptr) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_spin_bounded(bar, parity, ctl, abort_flag);
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 // 1-D bulk copy global -> shared, completion counted on an mbarrier.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,

@@ -27,12 +27,16 @@
 //   warp 0      TMA producer: per group, the hi and lo token tiles
 //               (128 x 128 B, 128B swizzle) and the code tile (128 x 32 B)
 //   warp 1      MMA issuer (one thread): 4 k-steps x (hi, lo) per group into
-//               one of two D buffers, then tcgen05.commit
+//               one of four D buffers, then tcgen05.commit
 //   warps 2-5   expansion: one weight row per thread, codes -> e4m3 B tile;
-//               also the group's weight scales for the epilogue
+//               also the group's weight scales for the epilogue (a ring of
+//               their own, released by the epilogue, so the expansion never
+//               waits for the epilogue of the previous group)
 //   warps 6-13  epilogue: per group, dot = D*512 - t (exact), then
 //               acc += dot * s * ws with the running fp32 accumulator in
-//               tensor memory; finally acc -> y.
+//               registers (64 columns per thread); finally acc -> y.
+// Four D buffers (all 512 columns of tensor memory) give the MMAs three
+// groups of slack on the epilogue.
 // Every mbarrier wait is bounded (device error word on expiry).
 #include "pq2_internal.h"
 
@@ -41,9 +45,10 @@ namespace {
 constexpr int kTileM = 128;  // tokens per tile (MMA M)
 constexpr int kTileN = 128;  // weight rows per tile (MMA N)
 constexpr int kStages = 4;
+constexpr int kDBufs = 4;            // D buffers in tensor memory, 128 columns each
 constexpr int kThreads = 14 * 32;
 constexpr int kEpiWarp0 = 6;
-constexpr uint32_t kTmemCols = 512;  // D0 [0,128), D1 [128,256), acc [256,384)
+constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kATileBytes = kTileM * 128;   // one group of 128 token rows
 constexpr uint32_t kBTileBytes = kTileN * 128;   // expanded weight rows
@@ -164,23 +169,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
-            taddr),
-        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
-        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
-        "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
-        "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
-        "f"(v[29]), "f"(v[30]), "f"(v[31]));
-}
-
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -192,9 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     __shared__ uint64_t full[kStages];   // TMA bytes of a stage landed
     __shared__ uint64_t bready[kStages]; // expanded weight tile written (4 warps)
     __shared__ uint64_t empty[kStages];  // MMAs of the stage done (commit)
-    __shared__ uint64_t dfull[2];        // D buffer holds a finished group (commit)
-    __shared__ uint64_t dempty[2];       // epilogue done with a D buffer (8 warps)
-    __shared__ float ws_sm[2][kTileN];   // weight scales per D buffer
+    __shared__ uint64_t wsfree[kStages]; // epilogue done with a slot of ws_sm (8 warps)
+    __shared__ uint64_t dfull[kDBufs];   // D buffer holds a finished group (commit)
+    __shared__ uint64_t dempty[kDBufs];  // epilogue done with a D buffer (8 warps)
+    __shared__ float ws_sm[kStages][kTileN];  // weight scales per stage
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -209,8 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             pq2::mbar_init(&full[i], 1);
             pq2::mbar_init(&bready[i], 4);
             pq2::mbar_init(&empty[i], 1);
+            pq2::mbar_init(&wsfree[i], 8);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kDBufs; ++i) {
             pq2::mbar_init(&dfull[i], 1);
             pq2::mbar_init(&dempty[i], 8);
         }
@@ -274,10 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
                 for (int g = 0; g < G; ++g, ++it) {
                     const int s = it % kStages;
-                    const int db = it & 1;
-                    if (!pq2::mbar_wait_bounded(&bready[s], (it / kStages) & 1, p.ctl, abort_v) ||
-                        (it >= 2 &&
-                         !pq2::mbar_wait_bounded(&dempty[db], ((it >> 1) - 1) & 1, p.ctl, abort_v))) {
+                    const int db = it % kDBufs;
+                    // busy polling: this thread is on the critical path (a
+                    // sleeping poller wakes up hundreds of cycles late)
+                    if (!pq2::mbar_spin_bounded(&bready[s], (it / kStages) & 1, p.ctl, abort_v) ||
+                        (it >= kDBufs &&
+                         !pq2::mbar_spin_bounded(&dempty[db], ((it / kDBufs) - 1) & 1, p.ctl,
+                                                 abort_v))) {
                         ok = false;
                         *abort_v = 1;
                         break;
@@ -297,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
             // no MMA may still be running when tensor memory is released
             if (it > 0)
-                pq2::mbar_wait_bounded(&dfull[(it - 1) & 1], ((it - 1) >> 1) & 1, p.ctl);
+                pq2::mbar_wait_bounded(&dfull[(it - 1) % kDBufs], ((it - 1) / kDBufs) & 1, p.ctl);
         }
     } else if (warp < kEpiWarp0) {
         // ------------------------------ expansion ------------------------------
@@ -310,13 +305,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const int n = nt * kTileN + r;
             for (int g = 0; g < G; ++g, ++it) {
                 const int s = it % kStages;
-                const int db = it & 1;
                 // weight scale of this row for the epilogue (prefetched before the waits)
                 const float wsv = (!DOTS && n < p.N) ? __half2float(p.ws[static_cast<size_t>(n) * G + g]) : 0.0f;
+                // ws_sm[s] was last read by the epilogue of group it - kStages
                 if (!failed &&
                     (!pq2::mbar_wait_bounded(&full[s], (it / kStages) & 1, p.ctl, abort_v) ||
-                     (it >= 2 &&
-                      !pq2::mbar_wait_bounded(&dempty[db], ((it >> 1) - 1) & 1, p.ctl, abort_v)))) {
+                     (it >= kStages &&
+                      !pq2::mbar_wait_bounded(&wsfree[s], ((it / kStages) - 1) & 1, p.ctl,
+                                              abort_v)))) {
                     failed = true;
                     *abort_v = 1;
                 }
@@ -343,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                             *reinterpret_cast<uint4*>(brow + 16 * chunk) = v;
                         }
                     }
-                    ws_sm[db][r] = wsv;
+                    ws_sm[s][r] = wsv;
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
                 __syncwarp();
@@ -362,25 +358,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
             const int m = mt * kTileM + quad * 32 + lane;  // token row of this thread
             const bool mvalid = m < p.M;
+            float acc[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
             float2 stv = (mvalid && !failed) ? p.st[m] : make_float2(0.0f, 0.0f);  // group 0
             for (int g = 0; g < G; ++g, ++it) {
-                const int db = it & 1;
+                const int s = it % kStages;
+                const int db = it % kDBufs;
                 // prefetch next group's (s, t) for this token
                 float2 st_next = make_float2(0.0f, 0.0f);
                 if (mvalid && g + 1 < G) st_next = p.st[static_cast<size_t>(g + 1) * p.M + m];
                 if (!failed &&
-                    !pq2::mbar_wait_bounded(&dfull[db], (it >> 1) & 1, p.ctl, abort_v)) {
+                    !pq2::mbar_wait_bounded(&dfull[db], (it / kDBufs) & 1, p.ctl, abort_v)) {
                     failed = true;
                     *abort_v = 1;
                 }
                 if (!failed) {
                     tc_fence_after();
+                    const float* wsr = ws_sm[s] + col0;
 #pragma unroll
                     for (int c = 0; c < 64; c += 32) {
                         float d[32];
                         tmem_ld32(tmem + lane_off + db * 128 + col0 + c, d);
-                        float acc[32];
-                        if (g > 0) tmem_ld32(tmem + lane_off + 256 + col0 + c, acc);
                         tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
@@ -391,42 +390,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                                     p.dots[(static_cast<size_t>(m) * p.N + n) * G + g] =
                                         static_cast<int>(dot);
                             } else {
+                                // the first group's term seeds the sum (0 + x would
+                                // turn a -0 term into +0)
                                 const float term = dot * stv.x;
-                                acc[j] = g > 0 ? fmaf(term, ws_sm[db][col0 + c + j], acc[j])
-                                               : term * ws_sm[db][col0 + c + j];
+                                acc[c + j] = g > 0 ? fmaf(term, wsr[c + j], acc[c + j])
+                                                   : term * wsr[c + j];
                             }
                         }
-                        if (!DOTS) tmem_st32(tmem + lane_off + 256 + col0 + c, acc);
                     }
-                    if (!DOTS) tmem_wait_st();
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) pq2::mbar_arrive(&dempty[db]);
+                if (lane == 0) {
+                    pq2::mbar_arrive(&dempty[db]);
+                    pq2::mbar_arrive(&wsfree[s]);
+                }
                 stv = st_next;
             }
             // tile done: acc -> y
-            if (!DOTS && !failed) {
-                tc_fence_after();
+            if (!DOTS && !failed && mvalid) {
                 const int nb = nt * kTileN + col0;
+                float* yrow = p.y + static_cast<size_t>(m) * p.N + nb;
+                if (nb + 64 <= p.N && (p.N & 3) == 0) {
 #pragma unroll
-                for (int c = 0; c < 64; c += 32) {
-                    float acc[32];
-                    tmem_ld32(tmem + lane_off + 256 + col0 + c, acc);
-                    tmem_wait_ld();
-                    if (mvalid) {
-                        float* yrow = p.y + static_cast<size_t>(m) * p.N + nb + c;
-                        if (nb + c + 32 <= p.N && (p.N & 3) == 0) {
+                    for (int j = 0; j < 64; j += 4)
+                        *reinterpret_cast<float4*>(yrow + j) =
+                            make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                } else {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 4)
-                                *reinterpret_cast<float4*>(yrow + j) =
-                                    make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (nb + c + j < p.N) yrow[j] = acc[j];
-                        }
-                    }
+                    for (int j = 0; j < 64; ++j)
+                        if (nb + j < p.N) yrow[j] = acc[j];
                 }
             }
         }

@@ -397,9 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
             uint32_t ps = 0, pb = 0;
             int done = 0;
             for (int it = 0; it < n; ++it) {
-                if (!pq2::mbar_wait_bounded(&full[s], ps, p.ctl, abort_v) ||
-                    !pq2::mbar_wait_bounded(&aready[b], pb, p.ctl, abort_v) ||
-                    (it >= kBufs && !pq2::mbar_wait_bounded(&dfree[b], pb ^ 1u, p.ctl, abort_v))) {
+                if (!pq2::mbar_spin_bounded(&full[s], ps, p.ctl, abort_v) ||
+                    !pq2::mbar_spin_bounded(&aready[b], pb, p.ctl, abort_v) ||
+                    (it >= kBufs && !pq2::mbar_spin_bounded(&dfree[b], pb ^ 1u, p.ctl, abort_v))) {
                     *abort_v = 1;
                     break;
                 }
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
             // ---- expansion of group wq of item `step` ----
             if (step < n) {
                 // warp-uniform waits: the tensor-memory accesses below are .sync.aligned
-                if (!failed && !pq2::mbar_wait_warp(&full[xs], xps, p.ctl, abort_v)) {
+                if (!failed && !pq2::mbar_spin_warp(&full[xs], xps, p.ctl, abort_v)) {
                     failed = true;
                     *abort_v = 1;
                 }
@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
             const int t = te, q = qe;
             const bool tile_end = (qe + 1 == Q);
             if (++qe == Q) { qe = 0; ++te; }
-            if (!failed && !pq2::mbar_wait_warp(&dfull[eb], epb, p.ctl, abort_v)) {
+            if (!failed && !pq2::mbar_spin_warp(&dfull[eb], epb, p.ctl, abort_v)) {
                 failed = true;
                 *abort_v = 1;
             }
