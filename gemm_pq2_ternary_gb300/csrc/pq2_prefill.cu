@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     __shared__ uint64_t wsfree[kStages]; // epilogue done with a slot of ws_sm (8 warps)
     __shared__ uint64_t dfull[kDBufs];   // D buffer holds a finished group (commit)
     __shared__ uint64_t dempty[kDBufs];  // epilogue done with a D buffer (8 warps)
-    __shared__ float ws_sm[kStages][kTileN];  // weight scales per stage
+    __shared__ __align__(16) float ws_sm[kStages][kTileN];  // weight scales per stage
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -375,7 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 }
                 if (!failed) {
                     tc_fence_after();
-                    const float* wsr = ws_sm[s] + col0;
+                    // the 64 weight scales of this thread's columns: 16-byte
+                    // broadcast loads (every lane reads the same address)
+                    const float4* ws4 = reinterpret_cast<const float4*>(ws_sm[s] + col0);
 #pragma unroll
                     for (int c = 0; c < 64; c += 32) {
                         float d[32];
@@ -393,8 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                                 // the first group's term seeds the sum (0 + x would
                                 // turn a -0 term into +0)
                                 const float term = dot * stv.x;
-                                acc[c + j] = g > 0 ? fmaf(term, wsr[c + j], acc[c + j])
-                                                   : term * wsr[c + j];
+                                const float4 w4 = ws4[(c + j) >> 2];
+                                const float wj = (j & 3) == 0 ? w4.x
+                                               : (j & 3) == 1 ? w4.y
+                                               : (j & 3) == 2 ? w4.z : w4.w;
+                                acc[c + j] = g > 0 ? fmaf(term, wj, acc[c + j]) : term * wj;
                             }
                         }
                     }
