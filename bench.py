@@ -404,7 +404,7 @@ def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dis
         for x, xh in zip(X, Xh):
             x.copy_(xh, non_blocking=True)
         for p in projs:
-            pq2.pq2_matmul_ex(p["x"], p["codes"], p["ws"], p["y"], flags, p["mmws"])
+            pq2.pq2_matmul_ex(p["x"], p["codes"], p["ws"], p["y"], flags, p["mmws"], stream)
         for y, yh in zip(Y, Yh):
             yh.copy_(y, non_blocking=True)
 

@@ -5,6 +5,8 @@
 // parameters every kernel gets (device error word, wait limit).
 #pragma once
 
+#include <atomic>
+
 #include <cstdint>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -405,6 +407,32 @@ bool device_info(DeviceInfo* out);
 
 // Fills the launch control block for the current device.
 bool make_ctl(pq2::DevCtl* ctl);
+
+// Raises a kernel's dynamic shared-memory limit to at least `smem` on the
+// current device, calling the driver only the first time a larger size is
+// needed (the attribute call costs microseconds, a launch a few).  One
+// SmemLimit per kernel instantiation (a function-local static).
+constexpr int kSmemLimitDevices = 64;
+struct SmemLimit {
+    std::atomic<int> bytes[kSmemLimitDevices];
+};
+
+template <typename Kern>
+cudaError_t ensure_smem(SmemLimit& lim, Kern kern, size_t smem) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSmemLimitDevices)
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem));
+    const int want = static_cast<int>(smem);
+    if (lim.bytes[dev].load(std::memory_order_acquire) >= want) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+    if (e != cudaSuccess) return e;
+    int cur = lim.bytes[dev].load(std::memory_order_relaxed);
+    while (cur < want && !lim.bytes[dev].compare_exchange_weak(cur, want, std::memory_order_release))
+        ;
+    return cudaSuccess;
+}
 
 // Launches are done with cudaLaunchKernelEx, with programmatic stream
 // serialisation allowed (the kernels call griddepcontrol.wait before

@@ -557,8 +557,8 @@ __global__ void __launch_bounds__(kDirectConsumers + 32, 1) gemv_direct_kernel(c
 template <bool DOTS, bool FUSED>
 cudaError_t launch_direct(const GemvParams& p, int grid, size_t smem, cudaStream_t st) {
     auto kern = gemv_direct_kernel<DOTS, FUSED>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static pq2h::SmemLimit lim;
+    cudaError_t e = pq2h::ensure_smem(lim, kern, smem);
     if (e != cudaSuccess) return e;
     return pq2h::launch(kern, dim3(grid), dim3(p.TC + 32), smem, st, true, p);
 }
@@ -749,8 +749,8 @@ size_t staged_layout(GemvParams& p) {
 }
 
 cudaError_t launch_staged(const GemvParams& p, int grid, size_t smem, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_staged_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static pq2h::SmemLimit lim;
+    cudaError_t e = pq2h::ensure_smem(lim, gemv_staged_kernel, smem);
     if (e != cudaSuccess) return e;
     return pq2h::launch(gemv_staged_kernel, dim3(grid), dim3(kStagedThreads), smem, st, true, p);
 }
@@ -758,8 +758,8 @@ cudaError_t launch_staged(const GemvParams& p, int grid, size_t smem, cudaStream
 template <int GPT, bool WS_SMEM, bool DOTS, bool FUSED>
 cudaError_t launch_variant(const GemvParams& p, int grid, size_t smem, cudaStream_t st) {
     auto kern = gemv_kernel<GPT, WS_SMEM, DOTS, FUSED>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static pq2h::SmemLimit lim;
+    cudaError_t e = pq2h::ensure_smem(lim, kern, smem);
     if (e != cudaSuccess) return e;
     return pq2h::launch(kern, dim3(grid), dim3(p.TC + 32), smem, st, true, p);
 }

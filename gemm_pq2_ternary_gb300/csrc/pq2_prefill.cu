@@ -491,8 +491,8 @@ cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, c
     const int grid = tiles < dev.num_sms ? tiles : dev.num_sms;
     const size_t smem = 1024 + static_cast<size_t>(kStages) * kStageBytes;
     auto kern = dots ? prefill_kernel<true> : prefill_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static SmemLimit lim[2];
+    cudaError_t e = ensure_smem(lim[dots ? 1 : 0], kern, smem);
     if (e != cudaSuccess) return e;
     return launch(kern, dim3(grid), dim3(kThreads), smem, st, true, p);
 }

@@ -712,8 +712,8 @@ cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, con
     p.ctl = ctl;
     const size_t smem = 1024 + static_cast<size_t>(kStages) * kStageBytes;
     auto kern = dots ? small_kernel<true> : small_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static SmemLimit lim[2];
+    cudaError_t e = ensure_smem(lim[dots ? 1 : 0], kern, smem);
     if (e != cudaSuccess) return e;
     return launch(kern, dim3(l.grid), dim3(kThreads), smem, st, true, p);
 }
