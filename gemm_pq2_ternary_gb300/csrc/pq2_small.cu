@@ -46,7 +46,9 @@
 //               tiles, one bulk copy of the tokens' (s, t); its 32 lanes load
 //               the 128 rows' weight scales (two items ahead) into the stage
 //   warp 1      TMEM allocation; MMA issuer (one thread)
-//   warps 2-17  workers: expansion of item i (codes -> A in TMEM; the four
+//   warp 2      second MMA issuer (one thread): the item's groups are split
+//               between the two
+//   warps 3-18  workers: expansion of item i (codes -> A in TMEM; the four
 //               warps of a lane quadrant take one group each), then the
 //               epilogue of item i-1 (the four warps take 4 tokens each)
 // Every mbarrier wait is bounded (device error word on expiry).
@@ -60,9 +62,14 @@ constexpr int kGQ = 4;                // groups per item
 constexpr int kStages = 4;            // TMA ring
 constexpr int kBufs = 2;              // A and D buffers in TMEM, per item
 constexpr int kWorkerWarps = 16;      // four per TMEM lane quadrant
+#ifndef PQ2_SMALL_ISSUERS
+#define PQ2_SMALL_ISSUERS 2
+#endif
+constexpr int kIssuers = PQ2_SMALL_ISSUERS;  // MMA-issuing warps (1, 2 or 4), groups split among them
+constexpr int kWorker0 = 1 + kIssuers;       // first worker warp
 constexpr int kTokPerWarp = 4;        // epilogue tokens per worker warp
 constexpr int kWorkerThreads = kWorkerWarps * 32;
-constexpr int kThreads = (2 + kWorkerWarps) * 32;
+constexpr int kThreads = (kWorker0 + kWorkerWarps) * 32;
 constexpr uint32_t kTmemCols = 512;   // A: 2 items x 4 groups x 32; D: 2 x 4 x 32
 constexpr uint32_t kGCols = 32;       // TMEM columns per group (A: K = 128 e4m3; D: N = 32 fp32)
 constexpr uint32_t kDCol0 = kBufs * kGQ * kGCols;  // 256
@@ -276,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         }
         for (int i = 0; i < kBufs; ++i) {
             pq2::mbar_init(&aready[i], kWorkerWarps);
-            pq2::mbar_init(&dfull[i], 1);
+            pq2::mbar_init(&dfull[i], kIssuers);  // one commit per issuer
             pq2::mbar_init(&dfree[i], kWorkerWarps);
         }
         abort_flag = 0;
@@ -390,8 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
                 if (last >= 0) pq2::mbar_wait_bounded(&full[k], (last / kStages) & 1, p.ctl);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------ MMA issuer ------------------------------
+    } else if (warp < kWorker0) {
+        // ------------------------------ MMA issuers ------------------------------
+        // Each issuer takes kGQ / kIssuers of the item's groups: a warp that
+        // issues tcgen05.mma is held for tens of cycles per instruction, far
+        // longer than a small (N = 32) MMA keeps the tensor pipe busy.
+        const int gq0 = (warp - 1) * (kGQ / kIssuers);
         if (lane == 0) {
             int s = 0, b = 0;
             uint32_t ps = 0, pb = 0;
@@ -413,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
 #pragma unroll
-                    for (int gq = 0; gq < kGQ; ++gq)
+                    for (int gq = gq0; gq < gq0 + kGQ / kIssuers; ++gq)
                         mma_f8_ta(tmem + kDCol0 + (b * kGQ + gq) * kGCols,
                                   tmem + (b * kGQ + gq) * kGCols + 8 * k,
                                   desc0 + ((gq * kTokGroupBytes + 32 * k) >> 4), k > 0);
@@ -429,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
         }
     } else {
         // -------------------------------- workers --------------------------------
-        const int wi = warp - 2;          // 0..15
+        const int wi = warp - kWorker0;   // 0..15
         const int quad = warp & 3;        // TMEM lane quadrant of this warp
         const int wq = wi >> 2;           // 0..3: the group it expands, its tokens 4wq..4wq+3
         const int r = quad * 32 + lane;   // weight row within the tile

@@ -134,3 +134,21 @@ def test_static_weights_back_to_back():
     assert pq2.pq2_last_device_error() == pq2.PQ2_OK
     for a, b in zip(gouts, want):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("prob", [inputs.mlp_gate_up(1), inputs.mlp_down(1)], ids=lambda p: p.name)
+def test_static_weights_fall_back_where_slices_are_too_large(prob):
+    """Where a CTA's weight slice does not fit the staged kernel, the flag
+    changes nothing: y is bit-identical to pq2_matmul."""
+    from gemm_pq2_ternary_gb300 import binding as pq2
+    tern, ws, x = inputs.generate(prob)
+    codes, ws_d = pq2.pack(torch.from_numpy(tern).cuda(), torch.from_numpy(ws).cuda())
+    xd = torch.from_numpy(x).cuda()
+    torch.cuda.synchronize()
+    y0 = torch.full((1, prob.N), float("nan"), device="cuda")
+    y1 = torch.full((1, prob.N), float("nan"), device="cuda")
+    pq2.pq2_matmul(xd, codes, ws_d, y0, None)
+    pq2.pq2_matmul_ex(xd, codes, ws_d, y1, pq2.PQ2_WEIGHTS_STATIC, None)
+    torch.cuda.synchronize()
+    assert pq2.pq2_last_device_error() == pq2.PQ2_OK
+    assert torch.equal(y0, y1)
