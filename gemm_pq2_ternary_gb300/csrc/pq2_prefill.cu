@@ -26,8 +26,12 @@
 // Per CTA (persistent over 128x128 output tiles, one per SM):
 //   warp 0      TMA producer: per group, the hi and lo token tiles
 //               (128 x 128 B, 128B swizzle) and the code tile (128 x 32 B)
-//   warp 1      MMA issuer (one thread): 4 k-steps x (hi, lo) per group into
-//               one of four D buffers, then tcgen05.commit
+//   warps 1, 14 MMA issuers (one thread each; warp 1 the even groups, warp 14
+//               the odd ones): 4 k-steps x (hi, lo) per group into one of
+//               four D buffers, then tcgen05.commit.  A warp that issues
+//               tcgen05.mma is held for tens of cycles per instruction; two
+//               issuers keep the tensor pipe fed.  Even and odd groups use
+//               disjoint stages and D buffers, so the two share no barrier.
 //   warps 2-5   expansion: one weight row per thread, codes -> e4m3 B tile;
 //               also the group's weight scales for the epilogue (a ring of
 //               their own, released by the epilogue, so the expansion never
@@ -46,8 +50,11 @@ constexpr int kTileM = 128;  // tokens per tile (MMA M)
 constexpr int kTileN = 128;  // weight rows per tile (MMA N)
 constexpr int kStages = 4;
 constexpr int kDBufs = 4;            // D buffers in tensor memory, 128 columns each
-constexpr int kThreads = 14 * 32;
 constexpr int kEpiWarp0 = 6;
+constexpr int kIssuer2 = 14;         // second MMA issuer (odd groups)
+static_assert(kStages % 2 == 0 && kDBufs % 2 == 0,
+              "even and odd groups must use disjoint stages and D buffers");
+constexpr int kThreads = 15 * 32;
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kATileBytes = kTileM * 128;   // one group of 128 token rows
@@ -258,13 +265,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 if (last >= 0) pq2::mbar_wait_bounded(&full[s], (last / kStages) & 1, p.ctl);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------ MMA issuer ------------------------------
+    } else if (warp == 1 || warp == kIssuer2) {
+        // ------------------------------ MMA issuers ------------------------------
+        const int parity = warp == 1 ? 0 : 1;
         if (lane == 0) {
             int it = 0;
+            int last = -1;  // last group this issuer committed
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
                 for (int g = 0; g < G; ++g, ++it) {
+                    if ((it & 1) != parity) continue;
                     const int s = it % kStages;
                     const int db = it % kDBufs;
                     // busy polling: this thread is on the critical path (a
@@ -288,13 +298,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     }
                     mma_commit(&empty[s]);
                     mma_commit(&dfull[db]);
+                    last = it;
                 }
             }
             // no MMA may still be running when tensor memory is released
-            if (it > 0)
-                pq2::mbar_wait_bounded(&dfull[(it - 1) % kDBufs], ((it - 1) / kDBufs) & 1, p.ctl);
+            if (last >= 0)
+                pq2::mbar_wait_bounded(&dfull[last % kDBufs], (last / kDBufs) & 1, p.ctl);
         }
-    } else if (warp < kEpiWarp0) {
+    } else if (warp < kEpiWarp0) {  // warps 2-5
         // ------------------------------ expansion ------------------------------
         const int r = (warp - 2) * 32 + lane;  // weight row within the tile
         const int half = (lane >> 2) & 1;      // conflict-free order of the 2 loads
@@ -346,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 if (lane == 0) pq2::mbar_arrive(&bready[s]);
             }
         }
-    } else {
+    } else if (warp < kIssuer2) {
         // ------------------------------ epilogue ------------------------------
         const int ew = warp - kEpiWarp0;  // 0..7
         const int quad = warp & 3;        // TMEM lane quadrant of this warp
