@@ -81,6 +81,7 @@ struct GemvParams {
     uint32_t act_off, red_off, ring_off;  // shared-memory layout
     uint32_t ws_off;                      // staged variant: weight scales
     int prefetch;              // L2 prefetch of the CTA's weights before the wait
+    int prefetch_x;            // fused paths: L2 prefetch of x before the wait
     int trigger;               // staged variant: 0 trigger dependents after the wait,
                                // 1 after the activations are quantised, 2 after the dots
     pq2::DevCtl ctl;
@@ -398,7 +399,10 @@ __global__ void __launch_bounds__((GPT == 1 ? kMaxConsumersSmall : kMaxConsumers
 // per-SM weight slice landed about 1 us sooner this way than through bulk
 // copies into a ring.)
 // ---------------------------------------------------------------------------
-constexpr int kLookahead = 4;
+#ifndef PQ2_GEMV_LOOKAHEAD
+#define PQ2_GEMV_LOOKAHEAD 4
+#endif
+constexpr int kLookahead = PQ2_GEMV_LOOKAHEAD;
 constexpr int kDirectConsumers = 480;  // <= 128 registers: the look-ahead slots stay in registers
 constexpr size_t kDirectMaxSmem = 160 * 1024;  // else the ring variant (row sums in chunks)
 
@@ -426,7 +430,10 @@ __global__ void __launch_bounds__(kDirectConsumers + 32, 1) gemv_direct_kernel(c
     }
     __syncthreads();
     // activations, scales and (possibly) weights may come from the preceding
-    // kernel: wait for it before reading any of them
+    // kernel: wait for it before reading any of them.  (An L2 prefetch of x
+    // before the wait is only a hint: a write by that kernel still lands in
+    // L2.)
+    if (FUSED && tid == p.TC && p.prefetch_x) bulk_prefetch_l2(p.x, 2u * p.K);
     pq2::pdl_wait();
     pq2::pdl_launch_dependents();
     if (rows <= 0) return;
@@ -626,7 +633,11 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
             __syncthreads();
         }
     }
-    // x comes from the preceding kernel: wait for it before reading it
+    // x may come from the preceding kernel: it is read only after the wait.
+    // An L2 prefetch of it before the wait is only a hint (a write by that
+    // kernel still lands in L2), and takes the round trip to HBM off the path
+    // when x is final already.
+    if (tid == 32 && p.prefetch_x) bulk_prefetch_l2(p.x, 2u * p.K);
     pq2::pdl_wait();
     if (p.trigger == 0 || rows <= 0) pq2::pdl_launch_dependents();
     if (rows <= 0) return;
@@ -784,7 +795,9 @@ cudaError_t launch_gpt(const GemvParams& p, int grid, size_t smem, bool ws_smem,
 // direct variant where it applies, default; 2 = always the ring variant),
 // PQ2_GEMV_TRIGGER (staged variant: 1 = let the next kernel launch right
 // after the wait, default; 2 = after the activations are quantised; 3 =
-// after the dots).
+// after the dots), PQ2_GEMV_PREFETCH_X (fused paths: 1 = L2 prefetch of x
+// before the wait, default; 2 = none).  Compile-time: PQ2_GEMV_LOOKAHEAD
+// (direct variant, rows of loads in flight per thread, default 4).
 int env_int(const char* name, int dflt) {
     const char* v = std::getenv(name);
     if (!v || !*v) return dflt;
@@ -793,7 +806,7 @@ int env_int(const char* name, int dflt) {
 }
 
 struct Tuning {
-    int ctas_per_sm, threads, ring_kb, stage_kb, prefetch, direct, trigger;
+    int ctas_per_sm, threads, ring_kb, stage_kb, prefetch, direct, trigger, prefetch_x;
 };
 
 const Tuning& tuning() {
@@ -803,7 +816,8 @@ const Tuning& tuning() {
                              env_int("PQ2_GEMV_STAGE_KB", 16),
                              env_int("PQ2_GEMV_PREFETCH", 2) == 1 ? 1 : 0,
                              env_int("PQ2_GEMV_DIRECT", 1) == 1 ? 1 : 0,
-                             env_int("PQ2_GEMV_TRIGGER", 1) - 1};
+                             env_int("PQ2_GEMV_TRIGGER", 1) - 1,
+                             env_int("PQ2_GEMV_PREFETCH_X", 1) == 1 ? 1 : 0};
     return t;
 }
 
@@ -877,6 +891,7 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const
     p.ctl = ctl;
     p.prefetch = tu.prefetch;
     p.trigger = tu.trigger;
+    p.prefetch_x = tu.prefetch_x;
     // (the stage-withholding test hook needs the ring variant's waits)
     if (weights_static && p.x && ctl.debug_skip_stage < 0) {
         GemvParams sp = p;
