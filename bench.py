@@ -15,6 +15,7 @@ Workloads (--workload):
   mlp      M=--m (1 or 16): gate/up 5120 -> 34816, quantise the synthetic
            intermediate h, down 17408 -> 5120
   prefill  M=--m (128 or 4096), 5120 -> 17408
+  lmhead   M=1, K=5120 -> N=248320 (an lm_head-scale decode GEMV)
 
 --impl reference runs the CPU oracle (the method's plain definition) on the
 host cores on a bounded sample of the same workload, as the baseline arm.
@@ -79,6 +80,8 @@ def workload_spec(args):
     if w == "mlp":
         return f"mlp_pair_m{args.m}", [(args.m, 5120, 34816, "uniform", "normal"),
                                        (args.m, 17408, 5120, "uniform", "normal")], "GB/s"
+    if w == "lmhead":
+        return "lmhead_gemv_m1_k5120_n248320", [(1, 5120, 248320, "uniform", "normal")], "GB/s"
     if w == "prefill":
         return f"prefill_m{args.m}_k5120_n17408", [(args.m, 5120, 17408, "uniform", "normal")], \
             "TOPS"
@@ -507,7 +510,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pq2", choices=["pq2", "reference"])
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "pr1", "small", "mlp", "prefill"])
+                    choices=["decode", "pr1", "small", "mlp", "prefill", "lmhead"])
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--shape", default="5120,17408")
     ap.add_argument("--projections", type=int, default=0, help="weight sets per step (0: auto)")
