@@ -36,6 +36,8 @@ def _lib():
             "pq2o_codes_dots": [p, p, i64, i64, i64, p],
             "pq2o_matmul_rows": [p, p, p, p, i64, i64, i64, i64, i64, p, p],
             "pq2o_matmul_entries": [p, p, p, p, i64, i64, i64, i64, p, p, p, p],
+            "pq2o_exp": [p, i64, p],
+            "pq2o_swiglu": [p, i64, i64, p],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -180,3 +182,29 @@ def fp32_tolerance(ref, A, G):
     n = G + 2
     gamma = n * u / (1.0 - n * u)
     return 1e-3 * np.abs(ref) + gamma * A
+
+
+def exp_f32(x: np.ndarray) -> np.ndarray:
+    """The oracle's fp32 exp (Cody-Waite reduction + Taylor polynomial)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty_like(x)
+    _check(_lib().pq2o_exp(_ptr(x), x.size, _ptr(y)), "exp")
+    return y
+
+
+FP16_MAX = 65504.0
+
+
+def swiglu(gu: np.ndarray) -> np.ndarray:
+    """h = fp16(silu(gate) * up) of a gate/up output gu float32 [M, 2I]
+    (gate = first half, up = second half).  The fp32 product is clamped to
+    +-65504 and rounded to fp16 (IEEE round-half-even, numpy's conversion),
+    i.e. fp16 conversion that saturates instead of overflowing."""
+    gu = np.ascontiguousarray(gu, dtype=np.float32)
+    M, I2 = gu.shape
+    if I2 % 2:
+        raise ValueError("gu must have an even number of columns")
+    I = I2 // 2
+    h = np.empty((M, I), dtype=np.float32)
+    _check(_lib().pq2o_swiglu(_ptr(gu), M, I, _ptr(h)), "swiglu")
+    return np.clip(h, -FP16_MAX, FP16_MAX).astype(np.float16)

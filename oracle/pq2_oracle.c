@@ -38,6 +38,9 @@
  *                      dot(codes,q) - sum(q) ([P1] "One token at a time").
  *   pq2o_codes_dots    sum of code[n,k]*q[m,k] per group (no offset), for the
  *                      identity dot(codes,q) - sum(q) = sum((code-1)*q).
+ *   pq2o_swiglu        h = silu(gate) * up of a gate/up output (an assumed
+ *                      activation: the pages do not define it), with exp by
+ *                      a stated method (pq2o_exp); see the function.
  *   pq2o_matmul        y[m,n] = sum_g dot_g[m,n] * s[m,g] * ws[n,g], every
  *                      product and sum in float64, plus the magnitude
  *                      A[m,n] = sum_g |dot_g * s * ws| used by the
@@ -286,5 +289,66 @@ int pq2o_matmul_entries(const int8_t* qp, const float* S, const uint8_t* codes,
         y[i] = sum;
         if (A) A[i] = mag;
     }
+    return PQ2O_OK;
+}
+
+/*
+ * SwiGLU of the MLP's gate/up output, the activation between the two
+ * projections of a decode MLP.  The pages do not define it; SURVEY's next row
+ * names it as assumed.  This oracle takes the plain reading:
+ *   gate = gu[m, 0..I), up = gu[m, I..2I);  h = silu(gate) * up,
+ *   silu(g) = g / (1 + exp(-g)),
+ * every step one IEEE fp32 operation in this order (the caller rounds h to
+ * fp16, saturating at +-65504, before quantising it).
+ * exp is computed by a stated method rather than libm's expf, so that a
+ * kernel that follows the same steps gets the same bits: Cody and Waite's
+ * argument reduction (W. J. Cody, W. Waite, "Software Manual for the
+ * Elementary Functions", 1980): n = rint(x log2 e), r = x - n ln2 with ln2
+ * split in two fp32 parts (each subtraction one fused multiply-add), then the
+ * degree-7 Taylor polynomial of e^r (coefficients 1/i!, Horner with fused
+ * multiply-adds), then the exact scaling by 2^n.  x is clamped to [-87, 88]
+ * first (e^x stays a normal fp32 number).
+ */
+static float pq2o_exp_cw(float x) {
+    if (x < -87.0f) x = -87.0f;
+    if (x > 88.0f) x = 88.0f;
+    const float log2e = 0x1.715476p+0f;
+    const float ln2_hi = 0x1.62e430p-1f;
+    const float ln2_lo = -0x1.05c610p-29f;
+    const float n = rintf(x * log2e);
+    float r = fmaf(-n, ln2_hi, x);
+    r = fmaf(-n, ln2_lo, r);
+    float p = 0x1.a01a02p-13f;         /* 1/7! */
+    p = fmaf(p, r, 0x1.6c16c2p-10f);   /* 1/6! */
+    p = fmaf(p, r, 0x1.111112p-7f);    /* 1/5! */
+    p = fmaf(p, r, 0x1.555556p-5f);    /* 1/4! */
+    p = fmaf(p, r, 0x1.555556p-3f);    /* 1/3! */
+    p = fmaf(p, r, 0x1.0p-1f);         /* 1/2! */
+    p = fmaf(p, r, 1.0f);              /* 1/1! */
+    p = fmaf(p, r, 1.0f);              /* 1/0! */
+    return ldexpf(p, (int)n);          /* exact: the result is a normal number */
+}
+
+/* y[i] = the exp above, for the pin tests. */
+int pq2o_exp(const float* x, int64_t count, float* y) {
+    if (count < 0) return PQ2O_BAD_SHAPE;
+    for (int64_t i = 0; i < count; ++i) y[i] = pq2o_exp_cw(x[i]);
+    return PQ2O_OK;
+}
+
+/*
+ * gu  float32 [M, 2I]  (gate | up)
+ * h   float32 [M, I]   silu(gate) * up in fp32
+ */
+int pq2o_swiglu(const float* gu, int64_t M, int64_t I, float* h) {
+    if (M < 0 || I < 0) return PQ2O_BAD_SHAPE;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < I; ++k) {
+            const float g = gu[m * 2 * I + k];
+            const float u = gu[m * 2 * I + I + k];
+            const float e = pq2o_exp_cw(-g);
+            const float s = g / (1.0f + e);
+            h[m * I + k] = s * u;
+        }
     return PQ2O_OK;
 }
