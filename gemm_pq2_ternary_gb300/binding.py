@@ -26,6 +26,7 @@ PQ2_OP_GEMV = 0
 PQ2_OP_SMALL = 1
 PQ2_OP_PREFILL = 2
 PQ2_OP_MATMUL = 3
+PQ2_OP_SWIGLU_DOWN = 4
 
 PQ2_WEIGHTS_STATIC = 1
 
@@ -45,6 +46,8 @@ SIGNATURES = {
     "pq2_gemm_prefill": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _I),
     "pq2_matmul": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _I),
     "pq2_matmul_ex": ([_P, _P, _P, _P, _I64, _I64, _I64, _U32, _P, _SZ, _P], _I),
+    "pq2_quantize_swiglu": ([_P, _I64, _I64, _P, _P, _P, _P], _I),
+    "pq2_mlp_down_swiglu": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _I),
     "pq2_workspace_bytes": ([_I, _I64, _I64, _I64], _SZ),
     "pq2_group_dots": ([_I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _SZ, _P], _I),
     "pq2_last_device_error": ([_P], _I),
@@ -197,6 +200,21 @@ def pq2_matmul_ex(x, codes, ws, y, flags, workspace, stream=None):
     wp, wb = _ws(workspace)
     _check(_lib.pq2_matmul_ex(_ptr(x), _ptr(codes), _ptr(ws), _ptr(y), M, N, K, flags, wp, wb,
                               _stream(stream)), "pq2_matmul_ex")
+
+
+def pq2_quantize_swiglu(gu, qp, S, T, stream=None):
+    """gu [M, 2I] fp32 (gate | up) -> qp, S, T of h = fp16(silu(gate) * up)."""
+    M, I2 = gu.shape
+    _check(_lib.pq2_quantize_swiglu(_ptr(gu), M, I2 // 2, _ptr(qp), _ptr(S), _ptr(T),
+                                    _stream(stream)), "pq2_quantize_swiglu")
+
+
+def pq2_mlp_down_swiglu(gu, codes, ws, y, workspace, stream=None):
+    M, I2 = gu.shape
+    N = codes.shape[0]
+    wp, wb = _ws(workspace)
+    _check(_lib.pq2_mlp_down_swiglu(_ptr(gu), _ptr(codes), _ptr(ws), _ptr(y), M, N, I2 // 2,
+                                    wp, wb, _stream(stream)), "pq2_mlp_down_swiglu")
 
 
 def pq2_group_dots(op, qp, T, codes, dots, workspace=None, stream=None):

@@ -175,6 +175,22 @@ pq2_status pq2_quantize_act(const void* x_f16, int64_t M, int64_t K, int8_t* qp,
                                              static_cast<cudaStream_t>(stream), c.ctl, c.dev));
 }
 
+pq2_status pq2_quantize_swiglu(const float* gu, int64_t M, int64_t I, int8_t* qp, float* S,
+                               int32_t* T, void* stream) {
+    if (M < 0 || I < 1) return PQ2_ERR_INVALID_ARG;
+    if (I % 128 != 0 || I > PQ2_MAX_K) return PQ2_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return PQ2_OK;
+    if (!gu || !qp || !S || !T) return PQ2_ERR_INVALID_ARG;
+    if (!aligned16(gu) || !aligned16(qp) || !aligned16(S) || !aligned16(T))
+        return PQ2_ERR_MISALIGNED;
+    Ctx c;
+    pq2_status s = get_ctx(&c);
+    if (s != PQ2_OK) return s;
+    return cuda_status(pq2h::launch_quantize_swiglu(gu, qp, S, T, M, I,
+                                                    static_cast<cudaStream_t>(stream), c.ctl,
+                                                    c.dev));
+}
+
 pq2_status pq2_pack_weights(const int8_t* tern, const void* ws_f16, int64_t N, int64_t K,
                             uint8_t* codes, void* ws_out, void* stream) {
     pq2_status s = check_nk(N, K);
@@ -232,8 +248,10 @@ size_t pq2_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
         case PQ2_OP_SMALL:
             return (M >= 2 && M <= 16) ? pq2h::small_workspace_bytes(M, N, K) : SIZE_MAX;
         case PQ2_OP_PREFILL: return pq2h::prefill_workspace_bytes(M, N, K);
+        case PQ2_OP_SWIGLU_DOWN:  // K is the intermediate size I
         case PQ2_OP_MATMUL: {
-            if (M == 1 && pq2h::gemv_fused_supported(K)) return 0;  // fused, no scratch
+            if (op == PQ2_OP_MATMUL && M == 1 && pq2h::gemv_fused_supported(K))
+                return 0;  // fused, no scratch
             const size_t G = static_cast<size_t>(K / 128);
             const size_t act = align256(static_cast<size_t>(M) * K) +
                                2 * align256(static_cast<size_t>(M) * G * 4);
@@ -327,6 +345,35 @@ pq2_status pq2_matmul_ex(const void* x_f16, const uint8_t* codes, const void* ws
         return pq2_gemm_small(qp, S, T, codes, ws_f16, y, M, N, K, rest ? w : nullptr, rest,
                               stream);
     return pq2_gemm_prefill(qp, S, T, codes, ws_f16, y, M, N, K, rest ? w : nullptr, rest,
+                            stream);
+}
+
+pq2_status pq2_mlp_down_swiglu(const float* gu, const uint8_t* codes, const void* ws_f16, float* y,
+                               int64_t M, int64_t N, int64_t I, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    pq2_status s = check_nk(N, I);
+    if (s != PQ2_OK) return s;
+    if (M < 1 || !gu || !codes || !ws_f16 || !y) return PQ2_ERR_INVALID_ARG;
+    const size_t need = pq2_workspace_bytes(PQ2_OP_SWIGLU_DOWN, M, N, I);
+    if (need == SIZE_MAX) return PQ2_ERR_UNSUPPORTED_SHAPE;
+    if (!workspace || workspace_bytes < need) return PQ2_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PQ2_ERR_MISALIGNED;
+    const size_t G = static_cast<size_t>(I / 128);
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    int8_t* qp = reinterpret_cast<int8_t*>(w);
+    w += align256(static_cast<size_t>(M) * I);
+    float* S = reinterpret_cast<float*>(w);
+    w += align256(static_cast<size_t>(M) * G * 4);
+    int32_t* T = reinterpret_cast<int32_t*>(w);
+    w += align256(static_cast<size_t>(M) * G * 4);
+    const size_t rest = need - static_cast<size_t>(w - static_cast<uint8_t*>(workspace));
+    s = pq2_quantize_swiglu(gu, M, I, qp, S, T, stream);
+    if (s != PQ2_OK) return s;
+    if (M == 1) return pq2_gemv(qp, S, T, codes, ws_f16, y, N, I, stream);
+    if (M <= 16)
+        return pq2_gemm_small(qp, S, T, codes, ws_f16, y, M, N, I, rest ? w : nullptr, rest,
+                              stream);
+    return pq2_gemm_prefill(qp, S, T, codes, ws_f16, y, M, N, I, rest ? w : nullptr, rest,
                             stream);
 }
 

@@ -24,6 +24,12 @@ cudaError_t launch_quantize(const __half* x, int8_t* qp, float* S, int32_t* T, i
                             int64_t K, cudaStream_t st, const pq2::DevCtl& ctl,
                             const DeviceInfo& dev);
 
+// gu [M, 2I] fp32 (gate | up) -> quantised h = fp16(silu(gate) * up), as
+// launch_quantize does for fp16 activations.
+cudaError_t launch_quantize_swiglu(const float* gu, int8_t* qp, float* S, int32_t* T, int64_t M,
+                                   int64_t I, cudaStream_t st, const pq2::DevCtl& ctl,
+                                   const DeviceInfo& dev);
+
 cudaError_t launch_pack(const int8_t* tern, uint8_t* codes, int64_t N, int64_t K,
                         cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev);
 

@@ -26,8 +26,9 @@
 //    in D, and D_hi + D_lo = 2^-9 * dot(codes, q) exactly;
 //  * per group, 4 k-steps: the k order inside a group is the plane order of
 //    the activations, so k-step s is plane s (8 A columns);
-//  * epilogue: acc += ((D_hi + D_lo) * 512 s - s t) * ws in registers (the
-//    integer-dot debug output forms dot = (D_hi + D_lo) * 512 - t, exact), the 16 tokens of a weight row split over four warps.  The
+//  * epilogue: dot = (D_hi + D_lo) * 512 - t (an exact integer), then
+//    acc += dot * s * ws in registers (the integer-dot debug output writes
+//    dot itself); the 16 tokens of a weight row split over four warps.  The
 //    B rows are ordered [hi of tokens 0-3, lo of tokens 0-3, hi 4-7, lo 4-7,
 //    ...], so a warp's 4 tokens are 8 adjacent D columns.
 //
@@ -124,9 +125,8 @@ __device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v
 
 // tok [G4][32][128]: token m's e4m3(16h) in row 8*(m/4) + m%4 and its
 // e4m3(l) in row 8*(m/4) + 4 + m%4 (q = 16h + l, h = floor(q/16)); zero for
-// tokens >= M and groups >= G.  st16 [G4][16]: (512 s, s t) for the matmul
-// (the epilogue's term is D * 512 s - s t), or (0, t) when S is null (the
-// integer-dot debug output); zero likewise.
+// tokens >= M and groups >= G.  st16 [G4][16]: (s, t), or (0, t) when S is
+// null (the integer-dot debug output); zero likewise.
 __global__ void __launch_bounds__(256) small_prep_kernel(const int8_t* __restrict__ qp,
                                                          const float* __restrict__ S,
                                                          const int32_t* __restrict__ T,
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(256) small_prep_kernel(const int8_t* __restric
         float2 v = make_float2(0.0f, 0.0f);
         if (m < M && g < G) {
             const float t = static_cast<float>(T[m * G + g]);
-            v = S ? make_float2(512.0f * S[m * G + g], S[m * G + g] * t) : make_float2(0.0f, t);
+            v = make_float2(S ? S[m * G + g] : 0.0f, t);
         }
         st16[i] = v;
     }
@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
             if (!failed) {
 #pragma unroll
                 for (int gq = 0; gq < kGQ; ++gq) {
-                    // (512 s, s t) of the 4 tokens (dots: (0, t)), weight scale of this row
+                    // (s, t) of the 4 tokens (dots: (0, t)), weight scale of this row
                     const uint32_t sta = es_s + kStOff + gq * kTok * 8 + wq * 32;
                     const uint4 st01 = pq2::lds_v4(sta), st23 = pq2::lds_v4(sta + 16);
                     const float sv[4] = {__uint_as_float(st01.x), __uint_as_float(st01.z),
@@ -548,8 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
                                 p.dots[(static_cast<size_t>(m) * p.N + row) * G + g] =
                                     static_cast<int>(dot);
                         } else {
-                            // (dot(codes, q) - t) * s = d * 512 s - s t
-                            acc[j] = fmaf(fmaf(d, sv[j], -tv[j]), wsv, acc[j]);
+                            // the exact integer dot first, then its scales (an
+                            // fma with a rounded s t could cancel catastrophically
+                            // when t is much larger than dot(codes, q) - t)
+                            const float dot = fmaf(d, 512.0f, -tv[j]);
+                            acc[j] = fmaf(dot * sv[j], wsv, acc[j]);
                         }
                     }
                 }

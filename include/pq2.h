@@ -73,7 +73,8 @@ enum {
     PQ2_OP_GEMV = 0,     /* pq2_gemv            (M == 1)            */
     PQ2_OP_SMALL = 1,    /* pq2_gemm_small      (2 <= M <= 16)      */
     PQ2_OP_PREFILL = 2,  /* pq2_gemm_prefill    (M >= 1)            */
-    PQ2_OP_MATMUL = 3    /* pq2_matmul          (M >= 1, from fp16) */
+    PQ2_OP_MATMUL = 3,   /* pq2_matmul          (M >= 1, from fp16) */
+    PQ2_OP_SWIGLU_DOWN = 4 /* pq2_mlp_down_swiglu (M >= 1; K = I)     */
 };
 
 /* Largest K any entry point accepts (G <= 2048 groups). */
@@ -101,6 +102,28 @@ const char* pq2_version(void);
  */
 pq2_status pq2_quantize_act(const void* x_f16, int64_t M, int64_t K,
                             int8_t* qp, float* S, int32_t* T, void* stream);
+
+/*
+ * pq2_quantize_swiglu -- the activation between the two projections of a
+ * decode MLP, fused with the quantisation of pq2_quantize_act.  The pages
+ * link the MLP's gate/up and down projections ([P1] "Choose the
+ * configuration with the proxy": replayed gate -> down pairs) but do not
+ * define the activation; this is the plain SwiGLU reading:
+ *   gate = gu[m, 0..I), up = gu[m, I..2I);  h = silu(gate) * up,
+ *   silu(g) = g / (1 + exp(-g)),
+ * every step one fp32 operation with round-to-nearest, exp computed by Cody
+ * and Waite's argument reduction and a degree-7 Taylor polynomial (a fixed
+ * sequence of fused multiply-adds, so a CPU restatement gets the same bits);
+ * h is rounded to fp16, saturating at +-65504, then quantised exactly as
+ * pq2_quantize_act quantises x.
+ *   gu     in   fp32 [M, 2I]  (typically the y of the gate/up projection)
+ *   qp     out  int8 [M, I] plane order
+ *   S, T   out  fp32 / int32 [M, I/128]
+ * M >= 0 (M == 0 enqueues nothing), 1 <= I <= PQ2_MAX_K, I % 128 == 0.
+ * NaN or Inf in gu: the result is undefined.
+ */
+pq2_status pq2_quantize_swiglu(const float* gu, int64_t M, int64_t I,
+                               int8_t* qp, float* S, int32_t* T, void* stream);
 
 /*
  * pq2_pack_weights -- the "prepared" weight planes: ternary values to codes.
@@ -195,6 +218,19 @@ pq2_status pq2_matmul(const void* x_f16, const uint8_t* codes, const void* ws_f1
 pq2_status pq2_matmul_ex(const void* x_f16, const uint8_t* codes, const void* ws_f16, float* y,
                          int64_t M, int64_t N, int64_t K, uint32_t flags,
                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pq2_mlp_down_swiglu -- the down projection of a decode MLP from its gate/up
+ * output: pq2_quantize_swiglu, then pq2_gemv (M == 1), pq2_gemm_small
+ * (M <= 16) or pq2_gemm_prefill, as pq2_matmul routes.
+ *   gu [M, 2I] fp32 in; codes [N, I/4], ws_f16 [N, I/128] in; y [M, N] fp32 out.
+ *   workspace: pq2_workspace_bytes(PQ2_OP_SWIGLU_DOWN, M, N, I) bytes (the
+ *   quantised h plus the matmul's own scratch); never 0.
+ * Errors as pq2_matmul.
+ */
+pq2_status pq2_mlp_down_swiglu(const float* gu, const uint8_t* codes, const void* ws_f16, float* y,
+                               int64_t M, int64_t N, int64_t I,
+                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * pq2_workspace_bytes -- scratch bytes `op` needs for this shape (0 if none,

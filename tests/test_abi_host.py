@@ -109,6 +109,18 @@ def test_matmul_ex_rejects_unknown_flags(lib):
     assert st == b.PQ2_ERR_WORKSPACE
 
 
+def test_swiglu_entry_points_check_arguments(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    assert 0 < b.pq2_workspace_bytes(b.PQ2_OP_SWIGLU_DOWN, 1, 5120, 17408) < b.SIZE_MAX
+    assert b.pq2_workspace_bytes(b.PQ2_OP_SWIGLU_DOWN, 1, 5120, 100) == b.SIZE_MAX
+    st = lib.pq2_quantize_swiglu(_p(FAKE), 1, 100, _p(FAKE), _p(FAKE), _p(FAKE), None)
+    assert st == b.PQ2_ERR_UNSUPPORTED_SHAPE
+    st = lib.pq2_quantize_swiglu(_p(ODD), 1, 128, _p(FAKE), _p(FAKE), _p(FAKE), None)
+    assert st == b.PQ2_ERR_MISALIGNED
+    st = lib.pq2_mlp_down_swiglu(_p(FAKE), _p(FAKE), _p(FAKE), _p(FAKE), 1, 64, 128, None, 0, None)
+    assert st == b.PQ2_ERR_WORKSPACE
+
+
 def test_group_dots_rejects_bad_op(lib):
     from gemm_pq2_ternary_gb300 import binding as b
     st = lib.pq2_group_dots(7, _p(FAKE), _p(FAKE), _p(FAKE), 1, 8, 128, _p(FAKE), None, 0, None)
