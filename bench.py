@@ -16,6 +16,8 @@ Workloads (--workload):
            intermediate h, down 17408 -> 5120
   prefill  M=--m (128 or 4096), 5120 -> 17408
   lmhead   M=1, K=5120 -> N=248320 (an lm_head-scale decode GEMV)
+  mlp_swiglu  M=--m: gate/up 5120 -> 34816, then the down projection straight
+           from its output (pq2_mlp_down_swiglu: SwiGLU + quantise, 17408 -> 5120)
 
 --impl reference runs the CPU oracle (the method's plain definition) on the
 host cores on a bounded sample of the same workload, as the baseline arm.
@@ -62,6 +64,24 @@ def gemm_bytes(M, N, K):
     return N * K // 4 + 2 * N * G + M * K + 8 * M * G + 4 * M * N
 
 
+def swiglu_down_bytes(M, N, I):
+    """Algorithmic bytes of pq2_mlp_down_swiglu: codes, weight scales, the fp32
+    gate/up input [M, 2I] and the fp32 output (the quantised h stays inside)."""
+    return N * I // 4 + 2 * N * (I // 128) + 8 * M * I + 4 * M * N
+
+
+# Workloads whose projection `dst` reads the output of projection `src` of
+# the same layer through pq2_mlp_down_swiglu (SwiGLU + quantise + matmul).
+SWIGLU_CHAINS = {"mlp_swiglu": (0, 1)}
+
+
+def chain_of(name):
+    for prefix, pair in SWIGLU_CHAINS.items():
+        if name.startswith(prefix + "_m"):
+            return pair
+    return None
+
+
 def quant_bytes(M, K):
     return 2 * M * K + M * K + 8 * M * (K // 128)
 
@@ -80,6 +100,10 @@ def workload_spec(args):
     if w == "mlp":
         return f"mlp_pair_m{args.m}", [(args.m, 5120, 34816, "uniform", "normal"),
                                        (args.m, 17408, 5120, "uniform", "normal")], "GB/s"
+    if w == "mlp_swiglu":
+        # the down projection reads the gate/up output (SWIGLU_CHAINS)
+        return f"mlp_swiglu_m{args.m}", [(args.m, 5120, 34816, "uniform", "normal"),
+                                         (args.m, 17408, 5120, "uniform", "normal")], "GB/s"
     if w == "lmhead":
         return "lmhead_gemv_m1_k5120_n248320", [(1, 5120, 248320, "uniform", "normal")], "GB/s"
     if w == "prefill":
@@ -129,12 +153,31 @@ def recorded_traffic(workload, family):
     return None
 
 
-def per_layer_units(layer, kind):
+def per_layer_units(layer, kind, name=""):
     """Algorithmic bytes (GB/s workloads) or int8-equivalent ops (TOPS) of one
-    layer, and the dominant kernel's share."""
+    layer."""
     if kind == "TOPS":
         return sum(2.0 * M * N * K for (M, K, N, _, _) in layer)
-    return float(sum(gemm_bytes(M, N, K) for (M, K, N, _, _) in layer))
+    chain = chain_of(name)
+    total = 0.0
+    for j, (M, K, N, _, _) in enumerate(layer):
+        total += swiglu_down_bytes(M, N, K) if chain and j == chain[1] else gemm_bytes(M, N, K)
+    return total
+
+
+def layer_launches(layer, name=""):
+    """Kernel launches of one layer: the fused quantise + GEMV for M = 1;
+    quantise, token preparation and matmul otherwise; SwiGLU-quantise and
+    the matmul (plus its preparation for M > 1) for a chained down
+    projection."""
+    chain = chain_of(name)
+    n = 0
+    for j, (M, K, N, _, _) in enumerate(layer):
+        if chain and j == chain[1]:
+            n += 2 if M == 1 else 3
+        else:
+            n += 1 if M == 1 else 3
+    return n
 
 
 # ---------------------------------------------------------------------------
@@ -197,7 +240,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-def build_layers(args, layer, R, device):
+def build_layers(args, layer, R, device, name=""):
     """R layers of distinct weight sets.  Each projection type j keeps its
     activations of all R layers in one tensor X[j] [R, M, K] and its outputs
     in Y[j] [R, M, N] (contiguous, so the end-to-end arm copies them in one
@@ -225,6 +268,13 @@ def build_layers(args, layer, R, device):
             mmws = pq2.alloc_workspace(pq2.PQ2_OP_MATMUL, M, N, K, device)
             projs.append(dict(M=M, K=K, N=N, codes=codes, ws=ws_p, x=X[j][r], qp=qp, S=S, T=T,
                               y=Y[j][r], op=op, wsp=wsp, mmws=mmws))
+        chain = chain_of(name)
+        if chain:
+            src, dst = projs[chain[0]], projs[chain[1]]
+            assert src["N"] == 2 * dst["K"] and src["M"] == dst["M"]
+            dst["gu"] = src["y"]
+            dst["swws"] = pq2.alloc_workspace(pq2.PQ2_OP_SWIGLU_DOWN, dst["M"], dst["N"],
+                                              dst["K"], device)
         layers.append(projs)
     torch.cuda.synchronize()
     return layers, X, Y
@@ -252,6 +302,9 @@ def step_fn(pq2, layers, matmul_only=False, flags=0):
     def fn():
         for projs in layers:
             for p in projs:
+                if "gu" in p:  # down projection from the gate/up output
+                    pq2.pq2_mlp_down_swiglu(p["gu"], p["codes"], p["ws"], p["y"], p["swws"])
+                    continue
                 if p["M"] == 1:
                     pq2.pq2_matmul_ex(p["x"], p["codes"], p["ws"], p["y"], flags, p["mmws"])
                     continue
@@ -298,7 +351,7 @@ def gpu_arm(args, rank, world, dist):
     name, layer, kind = workload_spec(args)
     layer_weight_bytes = sum(N * K // 4 + 2 * N * (K // 128) for (M, K, N, _, _) in layer)
     R = args.projections or max(1, math.ceil(4 * l2 / layer_weight_bytes))
-    layers, X, Y = build_layers(args, layer, R, device)
+    layers, X, Y = build_layers(args, layer, R, device, name)
 
     stream = torch.cuda.Stream(device)
     flags = weight_flags(pq2, args)
@@ -337,7 +390,7 @@ def gpu_arm(args, rank, world, dist):
     ms_mm = timed_replays(torch, g_mm, reps * args.steps, stream)
     mm_per_launch_ms = ms_mm / (reps * args.steps * R * len(layer))
 
-    units_layer = per_layer_units(layer, kind)
+    units_layer = per_layer_units(layer, kind, name)
     units_step = units_layer * R * reps
     scale = 1e-9 if kind == "GB/s" else 1e-12
     value = units_step * world / (ms_step * 1e-3) * scale
@@ -360,9 +413,9 @@ def gpu_arm(args, rank, world, dist):
     e2e = None
     if not args.no_e2e:
         e2e = e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_layer * R, world,
-                      dist, device)
+                      dist, device, name)
 
-    launches = args.steps * reps * R * sum(1 if M == 1 else 2 for (M, _, _, _, _) in layer)
+    launches = args.steps * reps * R * layer_launches(layer, name)
     out = {
         "metric": f"ternary matmul {kind} ({name})",
         "value": round(value, 2), "unit": kind, "n_gpus": world, "steps": args.steps,
@@ -391,12 +444,19 @@ def gpu_arm(args, rank, world, dist):
     return out, (name, layer, kind)
 
 
-def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dist, device):
+def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dist, device,
+            name=""):
     """The same metric through pq2_matmul_ex (the public call, eager) with host
     buffers: every pass copies all activations in from pinned host memory
     and all outputs back, inside the timed region (CUDA events on the
-    stream)."""
+    stream).  In a SwiGLU chain the down projection's input is the gate/up
+    output on the device, and only the down projection's output is read
+    back."""
     flags = weight_flags(pq2, args)
+    chain = chain_of(name)
+    if chain:
+        X = [x for j, x in enumerate(X) if j != chain[1]]
+        Y = [y for j, y in enumerate(Y) if j != chain[0]]
     Xh = [x.cpu().pin_memory() for x in X]
     Yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in Y]
     h2d = sum(x.numel() * x.element_size() for x in Xh)
@@ -407,7 +467,10 @@ def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dis
         for x, xh in zip(X, Xh):
             x.copy_(xh, non_blocking=True)
         for p in projs:
-            pq2.pq2_matmul_ex(p["x"], p["codes"], p["ws"], p["y"], flags, p["mmws"], stream)
+            if "gu" in p:
+                pq2.pq2_mlp_down_swiglu(p["gu"], p["codes"], p["ws"], p["y"], p["swws"], stream)
+            else:
+                pq2.pq2_matmul_ex(p["x"], p["codes"], p["ws"], p["y"], flags, p["mmws"], stream)
         for y, yh in zip(Y, Yh):
             yh.copy_(y, non_blocking=True)
 
@@ -510,7 +573,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pq2", choices=["pq2", "reference"])
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "pr1", "small", "mlp", "prefill", "lmhead"])
+                    choices=["decode", "pr1", "small", "mlp", "mlp_swiglu", "prefill", "lmhead"])
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--shape", default="5120,17408")
     ap.add_argument("--projections", type=int, default=0, help="weight sets per step (0: auto)")
