@@ -208,3 +208,49 @@ def swiglu(gu: np.ndarray) -> np.ndarray:
     h = np.empty((M, I), dtype=np.float32)
     _check(_lib().pq2o_swiglu(_ptr(gu), M, I, _ptr(h)), "swiglu")
     return np.clip(h, -FP16_MAX, FP16_MAX).astype(np.float16)
+
+
+# ---------------------------------------------------------------------------
+# The pages' second, unquantised workload: a small bf16 projection
+# (in_proj_ba, N = 96, K = 5120) computed as a split-K GEMM whose fp32 partial
+# sums are reduced in the fixed order 0, 1, 2, ... and rounded once to bf16
+# ("Making a ternary reasoning model fast in vLLM", page "From CUDA to Triton
+# and Gluon", section "Speed up a small unquantised projection").  The result
+# has a plain definition: y = bf16(x @ w^T); the oracle is that definition in
+# float64 (numpy's matmul as the primitive) and the kernels' fp32 summation
+# order is covered by bf16_gemm_tolerance.
+# ---------------------------------------------------------------------------
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 values stored as uint16 bit patterns -> float64 (exact)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16(v: np.ndarray) -> np.ndarray:
+    """float64 -> bf16 bit patterns, rounded once to nearest, ties to even
+    (bf16 keeps 8 significant bits).  Domain: zero and finite values whose
+    magnitude lies in the normal bf16 range [2^-126, 2^128); the rounded
+    value is exact in float32, whose upper 16 bits are the bf16 pattern."""
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)                       # v = m * 2^e, 0.5 <= |m| < 1
+    r = np.ldexp(np.round(m * 256.0) / 256.0, e)   # np.round: half to even
+    return (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def gemm_bf16(x_bits: np.ndarray, w_bits: np.ndarray):
+    """x [M, K], w [N, K] as bf16 bit patterns -> (ref float64 [M, N],
+    A = sum |x w| float64 [M, N]).  ref is the exact product sum (float64 is
+    exact here: every bf16 x bf16 product has at most 16 significant bits and
+    K <= 2^20 terms keep the sum well inside the 53-bit mantissa for the
+    magnitudes the tests use)."""
+    x = bf16_to_f64(x_bits)
+    w = bf16_to_f64(w_bits)
+    return x @ w.T, np.abs(x) @ np.abs(w).T
+
+
+def bf16_gemm_tolerance(ref, A, K):
+    """|y - ref| bound for y = bf16(fp32 sum of the K products in any order):
+    the fp32 summation error gamma_K * A plus one bf16 rounding of the result
+    (half a bf16 ulp, 2^-9 relative, of a value within gamma_K * A of ref)."""
+    gam = K * 2.0 ** -24 / (1 - K * 2.0 ** -24)
+    return 2.0 ** -8 * (np.abs(ref) + gam * A) + gam * A + 1e-30
