@@ -18,6 +18,8 @@ Workloads (--workload):
   lmhead   M=1, K=5120 -> N=248320 (an lm_head-scale decode GEMV)
   mlp_swiglu  M=--m: gate/up 5120 -> 34816, then the down projection straight
            from its output (pq2_mlp_down_swiglu: SwiGLU + quantise, 17408 -> 5120)
+  in_proj_ba  M=--m (1..16): the unquantised bf16 projection 5120 -> 96
+           (pq2_gemm_bf16_splitk)
 
 --impl reference runs the CPU oracle (the method's plain definition) on the
 host cores on a bounded sample of the same workload, as the baseline arm.
@@ -64,6 +66,21 @@ def gemm_bytes(M, N, K):
     return N * K // 4 + 2 * N * G + M * K + 8 * M * G + 4 * M * N
 
 
+def bf16_bytes(M, N, K):
+    """Algorithmic bytes of one bf16 projection: w, x and the bf16 y, once
+    each."""
+    return 2 * (N * K + M * K + M * N)
+
+
+def is_bf16(proj):
+    return proj[3] == "bf16"
+
+
+def weight_bytes(proj):
+    M, K, N = proj[:3]
+    return 2 * N * K if is_bf16(proj) else N * K // 4 + 2 * N * (K // 128)
+
+
 def swiglu_down_bytes(M, N, I):
     """Algorithmic bytes of pq2_mlp_down_swiglu: codes, weight scales, the fp32
     gate/up input [M, 2I] and the fp32 output (the quantised h stays inside)."""
@@ -106,6 +123,9 @@ def workload_spec(args):
                                          (args.m, 17408, 5120, "uniform", "normal")], "GB/s"
     if w == "lmhead":
         return "lmhead_gemv_m1_k5120_n248320", [(1, 5120, 248320, "uniform", "normal")], "GB/s"
+    if w == "in_proj_ba":
+        return f"in_proj_ba_bf16_m{args.m}_k5120_n96", [(args.m, 5120, 96, "bf16", "normal")], \
+            "GB/s"
     if w == "prefill":
         return f"prefill_m{args.m}_k5120_n17408", [(args.m, 5120, 17408, "uniform", "normal")], \
             "TOPS"
@@ -119,10 +139,13 @@ KERNEL_SOURCES = {
     "gemv": ["pq2_gemv.cu", "pq2_common.cuh"],
     "small": ["pq2_small.cu", "pq2_common.cuh"],
     "prefill": ["pq2_prefill.cu", "pq2_common.cuh"],
+    "bf16": ["pq2_bf16.cu", "pq2_common.cuh"],
 }
 
 
 def kernel_family(layer):
+    if is_bf16(layer[0]):
+        return "bf16"
     M = layer[0][0]
     return "gemv" if M == 1 else ("small" if M <= 16 else "prefill")
 
@@ -160,8 +183,13 @@ def per_layer_units(layer, kind, name=""):
         return sum(2.0 * M * N * K for (M, K, N, _, _) in layer)
     chain = chain_of(name)
     total = 0.0
-    for j, (M, K, N, _, _) in enumerate(layer):
-        total += swiglu_down_bytes(M, N, K) if chain and j == chain[1] else gemm_bytes(M, N, K)
+    for j, (M, K, N, cdist, _) in enumerate(layer):
+        if cdist == "bf16":
+            total += bf16_bytes(M, N, K)
+        elif chain and j == chain[1]:
+            total += swiglu_down_bytes(M, N, K)
+        else:
+            total += gemm_bytes(M, N, K)
     return total
 
 
@@ -169,11 +197,13 @@ def layer_launches(layer, name=""):
     """Kernel launches of one layer: the fused quantise + GEMV for M = 1;
     quantise, token preparation and matmul otherwise; SwiGLU-quantise and
     the matmul (plus its preparation for M > 1) for a chained down
-    projection."""
+    projection; one split-K launch for a bf16 projection."""
     chain = chain_of(name)
     n = 0
-    for j, (M, K, N, _, _) in enumerate(layer):
-        if chain and j == chain[1]:
+    for j, (M, K, N, cdist, _) in enumerate(layer):
+        if cdist == "bf16":
+            n += 1
+        elif chain and j == chain[1]:
             n += 2 if M == 1 else 3
         else:
             n += 1 if M == 1 else 3
@@ -249,14 +279,21 @@ def build_layers(args, layer, R, device, name=""):
     from gemm_pq2_ternary_gb300 import binding as pq2
     from gemm_pq2_ternary_gb300 import inputs
 
-    X = [torch.empty((R, M, K), dtype=torch.float16, device=device) for (M, K, N, _, _) in layer]
-    Y = [torch.empty((R, M, N), dtype=torch.float32, device=device) for (M, K, N, _, _) in layer]
+    X = [torch.empty((R, M, K), dtype=torch.bfloat16 if c == "bf16" else torch.float16,
+                     device=device) for (M, K, N, c, _) in layer]
+    Y = [torch.empty((R, M, N), dtype=torch.bfloat16 if c == "bf16" else torch.float32,
+                     device=device) for (M, K, N, c, _) in layer]
     layers = []
     for r in range(R):
         gen = torch.Generator(device=device)
         gen.manual_seed(1000 + r)
         projs = []
         for j, (M, K, N, cdist, xdist) in enumerate(layer):
+            if cdist == "bf16":
+                w = inputs.draw_bf16_torch((N, K), 0.02, gen, device)
+                X[j][r].copy_(inputs.draw_bf16_torch((M, K), 1.0, gen, device))
+                projs.append(dict(M=M, K=K, N=N, bf16=True, w=w, x=X[j][r], y=Y[j][r]))
+                continue
             tern = inputs.draw_ternary_torch(N, K, cdist, gen, device)
             ws = inputs.draw_ws_torch(N, K, gen, device)
             codes, ws_p = pq2.pack(tern, ws)
@@ -302,6 +339,9 @@ def step_fn(pq2, layers, matmul_only=False, flags=0):
     def fn():
         for projs in layers:
             for p in projs:
+                if "bf16" in p:
+                    pq2.pq2_gemm_bf16_splitk(p["x"], p["w"], p["y"], flags)
+                    continue
                 if "gu" in p:  # down projection from the gate/up output
                     pq2.pq2_mlp_down_swiglu(p["gu"], p["codes"], p["ws"], p["y"], p["swws"])
                     continue
@@ -339,6 +379,12 @@ def timed_replays(torch, graph, n, stream):
     return t0.elapsed_time(t1)
 
 
+def metric_name(kind, name, layer):
+    if is_bf16(layer[0]):
+        return f"bf16 split-K projection {kind} ({name})"
+    return f"ternary matmul {kind} ({name})"
+
+
 def gpu_arm(args, rank, world, dist):
     import torch
     from gemm_pq2_ternary_gb300 import binding as pq2
@@ -349,7 +395,8 @@ def gpu_arm(args, rank, world, dist):
     props = torch.cuda.get_device_properties(device)
     l2 = props.L2_cache_size
     name, layer, kind = workload_spec(args)
-    layer_weight_bytes = sum(N * K // 4 + 2 * N * (K // 128) for (M, K, N, _, _) in layer)
+    layer_weight_bytes = sum(weight_bytes(pr) for pr in layer)
+    bf16 = is_bf16(layer[0])
     R = args.projections or max(1, math.ceil(4 * l2 / layer_weight_bytes))
     layers, X, Y = build_layers(args, layer, R, device, name)
 
@@ -416,23 +463,31 @@ def gpu_arm(args, rank, world, dist):
                       dist, device, name)
 
     launches = args.steps * reps * R * layer_launches(layer, name)
+    if bf16:
+        arith = "bf16 x bf16 products and fp32 sums on the CUDA cores, one rounding to bf16"
+        graph = ("one CUDA graph per pass (per projection one pq2_gemm_bf16_splitk launch), "
+                 "programmatic dependent launch")
+    else:
+        arith = "int8 activations x 2-bit ternary codes, int32 group dots, fp32 sums"
+        graph = ("one CUDA graph per pass (per projection: fused quantise+GEMV "
+                 "for M=1, quantise then matmul otherwise), programmatic dependent launch")
     out = {
-        "metric": f"ternary matmul {kind} ({name})",
+        "metric": metric_name(kind, name, layer),
         "value": round(value, 2), "unit": kind, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "i8",
-        "data": "synthetic (seeded; ternary codes, fp16 scales and activations drawn on device)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "i8",
+        "data": ("synthetic (seeded; bf16 weights and activations drawn on device)" if bf16 else
+                 "synthetic (seeded; ternary codes, fp16 scales and activations drawn on device)"),
         "config": {"workload": name, "projections_per_pass": R * len(layer),
                    "passes_per_step": reps,
                    "shapes": [{"M": M, "K": K, "N": N} for (M, K, N, _, _) in layer],
                    "l2": f"inputs larger than L2: {R * layer_weight_bytes / 1e6:.0f} MB of distinct "
                          f"weights per pass vs {l2 / 1e6:.0f} MB L2",
-                   "graph": "one CUDA graph per pass (per projection: fused quantise+GEMV "
-                            "for M=1, quantise then matmul otherwise), programmatic dependent "
-                            "launch",
-                   "arith": "int8 activations x 2-bit ternary codes, int32 group dots, fp32 sums",
-                   "weights": ("static: M = 1 calls pass PQ2_WEIGHTS_STATIC (weights uploaded once; "
-                               "each call may read them before the preceding call ends)"
+                   "graph": graph,
+                   "arith": arith,
+                   "weights": ("static: M = 1 and bf16 calls pass PQ2_WEIGHTS_STATIC (weights "
+                               "uploaded once; each call may read them before the preceding call "
+                               "ends)"
                                if args.weights == "static" else "default ordering"),
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
@@ -467,7 +522,9 @@ def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dis
         for x, xh in zip(X, Xh):
             x.copy_(xh, non_blocking=True)
         for p in projs:
-            if "gu" in p:
+            if "bf16" in p:
+                pq2.pq2_gemm_bf16_splitk(p["x"], p["w"], p["y"], flags, stream)
+            elif "gu" in p:
                 pq2.pq2_mlp_down_swiglu(p["gu"], p["codes"], p["ws"], p["y"], p["swws"], stream)
             else:
                 pq2.pq2_matmul_ex(p["x"], p["codes"], p["ws"], p["y"], flags, p["mmws"], stream)
@@ -495,7 +552,8 @@ def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dis
     return {"value": round(units_pass * world / dt * scale, 2), "unit": kind,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(dt * 1e3, 4),
-            "step": "one pass over all projections: copy in, pq2_matmul_ex each, copy out"}
+            "step": "one pass over all projections: copy in, the public call each "
+                    "(pq2_matmul_ex, pq2_mlp_down_swiglu or pq2_gemm_bf16_splitk), copy out"}
 
 
 # ---------------------------------------------------------------------------
@@ -511,6 +569,10 @@ def oracle_sample(layer, kind, seconds):
     probs = []
     for i, (M, K, N, cdist, xdist) in enumerate(layer):
         rows = min(N, 64)
+        if cdist == "bf16":
+            xb, wb = inputs.generate_bf16(M, rows, K, seed=100 + i)
+            probs.append((M, K, rows, "bf16", xb, wb))
+            continue
         p = inputs.Problem("sample", M, K, rows, cdist, xdist, 100 + i)
         tern, ws, x = inputs.generate(p)
         qp, S, T = oracle.quantize_act(x)
@@ -520,8 +582,15 @@ def oracle_sample(layer, kind, seconds):
     def run(rows_frac):
         units = 0.0
         t0 = time.perf_counter()
-        for (M, K, rows, qp, S, codes, ws) in probs:
+        for pr in probs:
+            M, K, rows = pr[:3]
             r = max(1, int(rows * rows_frac))
+            if pr[3] == "bf16":
+                ref, _ = oracle.gemm_bf16(pr[4], pr[5][:r])
+                oracle.f64_to_bf16(ref)
+                units += bf16_bytes(M, r, K)
+                continue
+            qp, S, codes, ws = pr[3:]
             oracle.matmul(qp, S, codes[:r], ws[:r])
             units += (gemm_bytes(M, r, K) if kind == "GB/s" else 2.0 * M * r * K)
         return units, time.perf_counter() - t0
@@ -536,7 +605,12 @@ def oracle_sample(layer, kind, seconds):
     scale = 1e-9 if kind == "GB/s" else 1e-12
     desc = (f"{reps} x first {[p[2] for p in probs]} output rows of the "
             f"{[(p[0], p[1]) for p in probs]} (M,K) projections; all M tokens, all K")
-    return tot / dt * scale, desc, oracle.threads(), dt
+    threads = oracle.threads()
+    if any(p[3] == "bf16" for p in probs):
+        # numpy's float64 matmul: its BLAS may use every host core
+        threads = os.cpu_count() or 1
+        desc += "; float64 matmul through numpy's BLAS (up to all host cores)"
+    return tot / dt * scale, desc, threads, dt
 
 
 def reference_arm(args, rank, world):
@@ -553,9 +627,10 @@ def reference_arm(args, rank, world):
     ms = float(np.mean([dt for _, dt in vals])) * 1e3
     return {
         "impl": "reference",
-        "metric": f"ternary matmul {kind} ({name})", "value": round(value, 6), "unit": kind,
+        "metric": metric_name(kind, name, layer), "value": round(value, 6), "unit": kind,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i8",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64" if is_bf16(layer[0]) else "i8",
         "data": "synthetic (seeded host draws)",
         "config": {"workload": name, "parallelism": "host cores, one process"},
         "cpu_baseline": {"value": round(value, 6), "unit": kind, "cores": threads, "kind": "oracle",
@@ -573,7 +648,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pq2", choices=["pq2", "reference"])
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "pr1", "small", "mlp", "mlp_swiglu", "prefill", "lmhead"])
+                    choices=["decode", "pr1", "small", "mlp", "mlp_swiglu", "prefill", "lmhead",
+                             "in_proj_ba"])
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--shape", default="5120,17408")
     ap.add_argument("--projections", type=int, default=0, help="weight sets per step (0: auto)")

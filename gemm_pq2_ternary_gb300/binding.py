@@ -47,6 +47,7 @@ SIGNATURES = {
     "pq2_matmul": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _I),
     "pq2_matmul_ex": ([_P, _P, _P, _P, _I64, _I64, _I64, _U32, _P, _SZ, _P], _I),
     "pq2_quantize_swiglu": ([_P, _I64, _I64, _P, _P, _P, _P], _I),
+    "pq2_gemm_bf16_splitk": ([_P, _P, _P, _I64, _I64, _I64, _U32, _P], _I),
     "pq2_mlp_down_swiglu": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _I),
     "pq2_workspace_bytes": ([_I, _I64, _I64, _I64], _SZ),
     "pq2_group_dots": ([_I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _SZ, _P], _I),
@@ -200,6 +201,15 @@ def pq2_matmul_ex(x, codes, ws, y, flags, workspace, stream=None):
     wp, wb = _ws(workspace)
     _check(_lib.pq2_matmul_ex(_ptr(x), _ptr(codes), _ptr(ws), _ptr(y), M, N, K, flags, wp, wb,
                               _stream(stream)), "pq2_matmul_ex")
+
+
+def pq2_gemm_bf16_splitk(x, w, y, flags=0, stream=None):
+    """x [M, K], w [N, K], y [M, N]: torch.bfloat16 (or int16/uint16 bit
+    patterns) on the device."""
+    M, K = x.shape
+    N = w.shape[0]
+    _check(_lib.pq2_gemm_bf16_splitk(_ptr(x), _ptr(w), _ptr(y), M, N, K, flags,
+                                     _stream(stream)), "pq2_gemm_bf16_splitk")
 
 
 def pq2_quantize_swiglu(gu, qp, S, T, stream=None):

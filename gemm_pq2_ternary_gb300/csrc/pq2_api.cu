@@ -377,6 +377,24 @@ pq2_status pq2_mlp_down_swiglu(const float* gu, const uint8_t* codes, const void
                             stream);
 }
 
+pq2_status pq2_gemm_bf16_splitk(const uint16_t* x, const uint16_t* w, uint16_t* y, int64_t M,
+                                int64_t N, int64_t K, uint32_t flags, void* stream) {
+    if (M < 0 || N < 0 || K < 0) return PQ2_ERR_INVALID_ARG;
+    if (flags & ~static_cast<uint32_t>(PQ2_WEIGHTS_STATIC)) return PQ2_ERR_INVALID_ARG;
+    if (K % 8 != 0 || K > PQ2_MAX_K || M > PQ2_MAX_M_BF16 || N > PQ2_MAX_N_BF16)
+        return PQ2_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return PQ2_OK;
+    if (!y || (K > 0 && (!x || !w))) return PQ2_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || (reinterpret_cast<uintptr_t>(y) & 1u))
+        return PQ2_ERR_MISALIGNED;
+    Ctx c;
+    pq2_status s = get_ctx(&c);
+    if (s != PQ2_OK) return s;
+    return cuda_status(pq2h::launch_bf16_splitk(x, w, y, M, N, K,
+                                                (flags & PQ2_WEIGHTS_STATIC) != 0,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 pq2_status pq2_group_dots(int op, const int8_t* qp, const int32_t* T, const uint8_t* codes,
                           int64_t M, int64_t N, int64_t K, int32_t* dots, void* workspace,
                           size_t workspace_bytes, void* stream) {

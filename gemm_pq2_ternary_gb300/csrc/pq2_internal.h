@@ -30,6 +30,11 @@ cudaError_t launch_quantize_swiglu(const float* gu, int8_t* qp, float* S, int32_
                                    int64_t I, cudaStream_t st, const pq2::DevCtl& ctl,
                                    const DeviceInfo& dev);
 
+// y = bf16(x . w^T), bf16 operands as 16-bit patterns, split-K over a
+// cluster of CTAs with a fixed-order reduction (pq2_bf16.cu).
+cudaError_t launch_bf16_splitk(const uint16_t* x, const uint16_t* w, uint16_t* y, int64_t M,
+                               int64_t N, int64_t K, bool weights_static, cudaStream_t stream);
+
 cudaError_t launch_pack(const int8_t* tern, uint8_t* codes, int64_t N, int64_t K,
                         cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev);
 

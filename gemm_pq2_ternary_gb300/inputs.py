@@ -136,3 +136,42 @@ def draw_x_torch(M: int, K: int, dist: str, gen, device):
         mask = torch.rand((M, K), generator=gen, device=device) < 0.01
         x = torch.where(mask, x * 20.0, x)
     return x.to(torch.float16)
+
+
+# ---------------------------------------------------------------------------
+# The unquantised bf16 projection (in_proj_ba: 96 output rows, K = 5120, a
+# few decode tokens).  Values are float32 draws with the lower 16 bits of
+# each dropped, so every value is a bf16 pattern; the arrays hold those
+# patterns as uint16.
+#   x "normal"    N(0, 1)             (hidden states after the norm)
+#   x "integer"   integers in [-4, 4] (exact-arithmetic cases)
+#   w "normal"    N(0, 0.02^2)        (a projection's initial scale)
+#   w "integer"   integers in [-4, 4]
+# Draw order: w, then x, from one PCG64 stream seeded explicitly.
+# ---------------------------------------------------------------------------
+def _bf16_bits(v: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(v, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _draw_bf16(rng: np.random.Generator, shape, dist: str, sigma: float) -> np.ndarray:
+    if dist == "normal":
+        return _bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(sigma))
+    if dist == "integer":
+        return _bf16_bits(rng.integers(-4, 5, size=shape).astype(np.float32))
+    raise ValueError(dist)
+
+
+def generate_bf16(M: int, N: int, K: int, seed: int, x: str = "normal", w: str = "normal"):
+    """-> (x_bits [M, K], w_bits [N, K]) uint16."""
+    rng = np.random.default_rng(seed)
+    wb = _draw_bf16(rng, (N, K), w, 0.02)
+    xb = _draw_bf16(rng, (M, K), x, 1.0)
+    return xb, wb
+
+
+def draw_bf16_torch(shape, sigma: float, gen, device):
+    """bf16 tensor on `device`: N(0, sigma^2) float32 draws (torch's seeded
+    generator) with the lower 16 bits of each dropped."""
+    import torch
+    v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32) * sigma
+    return (v.view(torch.int32) >> 16).to(torch.int16).view(torch.bfloat16)

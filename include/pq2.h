@@ -233,6 +233,29 @@ pq2_status pq2_mlp_down_swiglu(const float* gu, const uint8_t* codes, const void
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pq2_gemm_bf16_splitk -- the small unquantised projection of a decode step
+ * ([P1] "Speed up a small unquantised projection": in_proj_ba, N = 96,
+ * K = 5120, a few tokens at a time): y = bf16(x . w^T), computed as a
+ * split-K GEMM whose fp32 partial sums are added in a fixed order, so the
+ * same inputs give the same bits on every call.
+ *   x [M, K] bf16 in, w [N, K] bf16 in, y [M, N] bf16 out; bf16 values are
+ *   passed as their 16-bit patterns, rows contiguous.  Products and sums in
+ *   fp32, one rounding of each output to bf16 (nearest, ties to even).
+ *   M >= 0 and N >= 0 (either 0 enqueues nothing), 0 <= K <= PQ2_MAX_K
+ *   (K == 0 writes zeros; x and w may then be null), K % 8 == 0, M <= PQ2_MAX_M_BF16,
+ *   N <= PQ2_MAX_N_BF16: PQ2_ERR_UNSUPPORTED_SHAPE otherwise.  x and w
+ *   16-byte aligned, y 2-byte aligned: PQ2_ERR_MISALIGNED otherwise.
+ *   flags: 0 or PQ2_WEIGHTS_STATIC (w may be read before the preceding
+ *   kernel on the stream has finished); other bits: PQ2_ERR_INVALID_ARG.
+ *   One launch, no workspace.  Built for M <= 16; a larger M runs as
+ *   independent 16-token tiles that each read w again.
+ */
+#define PQ2_MAX_M_BF16 1048560
+#define PQ2_MAX_N_BF16 1073741824
+pq2_status pq2_gemm_bf16_splitk(const uint16_t* x, const uint16_t* w, uint16_t* y, int64_t M,
+                                int64_t N, int64_t K, uint32_t flags, void* stream);
+
+/*
  * pq2_workspace_bytes -- scratch bytes `op` needs for this shape (0 if none,
  * SIZE_MAX if the shape is not supported).
  */

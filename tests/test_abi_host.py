@@ -139,3 +139,19 @@ def test_quantize_and_pack_reject_bad_arguments(lib):
     assert lib.pq2_quantize_act(P, 2, 128, _p(ODD), P, P, None) == b.PQ2_ERR_MISALIGNED
     assert lib.pq2_pack_weights(P, P, 4, 96, P, P, None) == b.PQ2_ERR_UNSUPPORTED_SHAPE
     assert lib.pq2_pack_weights(P, P, 4, 128, P, None, None) == b.PQ2_ERR_INVALID_ARG
+
+
+def test_bf16_splitk_checks_arguments(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    f = lib.pq2_gemm_bf16_splitk
+    assert f(_p(FAKE), _p(FAKE), _p(FAKE), 2, 96, 5124, 0, None) == b.PQ2_ERR_UNSUPPORTED_SHAPE
+    assert f(_p(FAKE), _p(FAKE), _p(FAKE), 2, 96, 5120, 2, None) == b.PQ2_ERR_INVALID_ARG
+    assert f(_p(FAKE), _p(FAKE), _p(FAKE), -1, 96, 5120, 0, None) == b.PQ2_ERR_INVALID_ARG
+    assert f(None, _p(FAKE), _p(FAKE), 2, 96, 5120, 0, None) == b.PQ2_ERR_INVALID_ARG
+    assert f(_p(ODD), _p(FAKE), _p(FAKE), 2, 96, 5120, 0, None) == b.PQ2_ERR_MISALIGNED
+    assert f(_p(FAKE), _p(ODD), _p(FAKE), 2, 96, 5120, 0, None) == b.PQ2_ERR_MISALIGNED
+    assert f(_p(FAKE), _p(FAKE), _p(FAKE + 1), 2, 96, 5120, 0, None) == b.PQ2_ERR_MISALIGNED
+    assert f(_p(FAKE), _p(FAKE), _p(FAKE), 1048561, 96, 5120, 0, None) == b.PQ2_ERR_UNSUPPORTED_SHAPE
+    # empty problems enqueue nothing, whatever the pointers
+    assert f(None, None, None, 0, 96, 5120, 0, None) == b.PQ2_OK
+    assert f(None, None, None, 4, 0, 5120, 0, None) == b.PQ2_OK
