@@ -457,6 +457,10 @@ def gpu_arm(args, rank, world, dist):
                 "traffic": recorded_traffic(name, kernel_family(layer)),
                 "peak_source": f"{peak_src}: MEASURED_PEAKS.json bf16_tflops (burst)"}
 
+    library = None
+    if bf16:
+        library = library_baseline(torch, layers, stream, reps, args.steps, R * len(layer))
+
     e2e = None
     if not args.no_e2e:
         e2e = e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_layer * R, world,
@@ -481,8 +485,12 @@ def gpu_arm(args, rank, world, dist):
         "config": {"workload": name, "projections_per_pass": R * len(layer),
                    "passes_per_step": reps,
                    "shapes": [{"M": M, "K": K, "N": N} for (M, K, N, _, _) in layer],
-                   "l2": f"inputs larger than L2: {R * layer_weight_bytes / 1e6:.0f} MB of distinct "
-                         f"weights per pass vs {l2 / 1e6:.0f} MB L2",
+                   "l2": (f"inputs larger than L2: {R * layer_weight_bytes / 1e6:.0f} MB of distinct "
+                          f"weights per pass vs {l2 / 1e6:.0f} MB L2"
+                          if R * layer_weight_bytes > l2 else
+                          f"inputs SMALLER than L2 ({R * layer_weight_bytes / 1e6:.1f} MB of weights "
+                          f"vs {l2 / 1e6:.0f} MB; --projections set: a profiling case, not a "
+                          f"measurement)"),
                    "graph": graph,
                    "arith": arith,
                    "weights": ("static: M = 1 and bf16 calls pass PQ2_WEIGHTS_STATIC (weights "
@@ -492,11 +500,26 @@ def gpu_arm(args, rank, world, dist):
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "matmul_us_per_launch": round(mm_per_launch_ms * 1e3, 3),
+        **({"library_baseline": library} if library else {}),
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk,
     }
     return out, (name, layer, kind)
+
+
+def library_baseline(torch, layers, stream, reps, steps, calls_per_pass):
+    """Context for the bf16 projection: the same calls through torch.matmul
+    (cuBLAS) on the same weight sets, captured and replayed the same way."""
+    def fn():
+        for projs in layers:
+            for p in projs:
+                torch.matmul(p["x"], p["w"].t(), out=p["y"])
+    g = capture(torch, fn, stream)
+    timed_replays(torch, g, reps, stream)
+    ms = timed_replays(torch, g, reps * steps, stream)
+    return {"impl": "torch.matmul (cuBLAS), same graph of calls",
+            "us_per_call": round(ms * 1e3 / (reps * steps * calls_per_pass), 3)}
 
 
 def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dist, device,

@@ -62,6 +62,11 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
     return r;
 }
 
+// L2 prefetch of [src, src + bytes): both 16-byte multiples, bytes <= 64 KiB.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
@@ -135,8 +140,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bf16_splitk_kernel(Bf16Params 
     constexpr int kOutPerRank = kOut / kSplits;
     static_assert(kOut % 32 == 0 && kOut <= kMaxOut, "the warp reduce-scatter wants 32 | kOut");
     static_assert(kOut % kSplits == 0, "each cluster rank finishes an equal share");
-    // partials received from every (source rank, warp) for this rank's outputs
-    __shared__ __align__(16) float red[kSplits][kMaxWarps][kOutPerRank];
+    __shared__ __align__(16) float wsum[kMaxWarps][kOut];        // this CTA's warps
+    __shared__ __align__(16) float red[kSplits][kOutPerRank];    // from every rank
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
@@ -153,6 +158,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bf16_splitk_kernel(Bf16Params 
 
     int kv = kv0 + tid;
     ColVec<kVK> wv[kNT];
+    // x may still be in flight from the preceding kernel: an L2 prefetch is
+    // only a hint (L2 is where that kernel's writes land), the loads come
+    // after the wait.  Splits start and end on 16-byte boundaries.
+    if (tid < kMT && m0 + tid < p.M && kv1 > kv0)
+        prefetch_l2(p.x + static_cast<size_t>(m0 + tid) * p.K +
+                             static_cast<size_t>(kv0) * kVK,
+                         static_cast<uint32_t>(kv1 - kv0) * kVK * 2);
     if (!p.weights_static) pdl_wait();
     if (kv < kv1) load_w<kNT, kVK>(p, n0, kv, wv);
     if (p.weights_static) pdl_wait();
@@ -202,23 +214,25 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bf16_splitk_kernel(Bf16Params 
             acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
     }
-    cluster_wait();  // every rank of the cluster has started
 #pragma unroll
-    for (int j = 0; j < kPerLane; ++j) {
-        const int o = kPerLane * lane + j;
-        const uint32_t owner = static_cast<uint32_t>(o / kOutPerRank);
-        st_cluster_f32(map_to_rank(smem_u32(&red[rank][warp][o % kOutPerRank]), owner), acc[j]);
+    for (int j = 0; j < kPerLane; ++j) wsum[warp][kPerLane * lane + j] = acc[j];
+    __syncthreads();
+    // one partial per output and CTA (its warps in increasing K), stored
+    // into the owning rank's shared memory
+    cluster_wait();  // every rank of the cluster has started
+    if (tid < kOut) {
+        float part = 0.0f;
+        for (int w = 0; w < nwarps; ++w) part += wsum[w][tid];
+        const uint32_t owner = static_cast<uint32_t>(tid / kOutPerRank);
+        st_cluster_f32(map_to_rank(smem_u32(&red[rank][tid % kOutPerRank]), owner), part);
     }
     cluster_sync_release_acquire();  // all partials of this rank's outputs have landed
 
     if (tid < kOutPerRank) {
-        // the sum in increasing K: source rank, then warp
+        // the sum in increasing K: source rank by source rank
         float sum = 0.0f;
 #pragma unroll
-        for (int r = 0; r < kSplits; ++r)
-#pragma unroll
-            for (int w = 0; w < kMaxWarps; ++w)
-                if (w < nwarps) sum += red[r][w][tid];
+        for (int r = 0; r < kSplits; ++r) sum += red[r][tid];
         const int o = static_cast<int>(rank) * kOutPerRank + tid;
         const int m = m0 + o / kNT, n = n0 + o % kNT;
         if (m < p.M && n < p.N) p.y[static_cast<size_t>(m) * p.N + n] = f32_to_bf16_rn(sum);
@@ -255,7 +269,9 @@ cudaError_t launch_bf16_splitk(const uint16_t* x, const uint16_t* w, uint16_t* y
         mt = 8, nt = 4;
     }
     const int kv_total = static_cast<int>(K / vk);
+    // splits of whole 16-byte pieces (K % 8 == 0, so kv_total is even for vk = 4)
     p.kv_per_split = (kv_total + kSplits - 1) / kSplits;
+    if (vk == 4) p.kv_per_split = (p.kv_per_split + 1) & ~1;
     p.weights_static = weights_static ? 1 : 0;
     const int threads = std::min(kMaxThreads, std::max(32, (p.kv_per_split + 31) / 32 * 32));
 
