@@ -396,7 +396,7 @@ def gpu_arm(args, rank, world, dist):
     l2 = props.L2_cache_size
     name, layer, kind = workload_spec(args)
     layer_weight_bytes = sum(weight_bytes(pr) for pr in layer)
-    bf16 = is_bf16(layer[0])
+    bf16_proj = is_bf16(layer[0])
     R = args.projections or max(1, math.ceil(4 * l2 / layer_weight_bytes))
     layers, X, Y = build_layers(args, layer, R, device, name)
 
@@ -458,7 +458,7 @@ def gpu_arm(args, rank, world, dist):
                 "peak_source": f"{peak_src}: MEASURED_PEAKS.json bf16_tflops (burst)"}
 
     library = None
-    if bf16:
+    if bf16_proj:
         library = library_baseline(torch, layers, stream, reps, args.steps, R * len(layer))
 
     e2e = None
@@ -467,7 +467,7 @@ def gpu_arm(args, rank, world, dist):
                       dist, device, name)
 
     launches = args.steps * reps * R * layer_launches(layer, name)
-    if bf16:
+    if bf16_proj:
         arith = "bf16 x bf16 products and fp32 sums on the CUDA cores, one rounding to bf16"
         graph = ("one CUDA graph per pass (per projection one pq2_gemm_bf16_splitk launch), "
                  "programmatic dependent launch")
@@ -479,8 +479,8 @@ def gpu_arm(args, rank, world, dist):
         "metric": metric_name(kind, name, layer),
         "value": round(value, 2), "unit": kind, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "i8",
-        "data": ("synthetic (seeded; bf16 weights and activations drawn on device)" if bf16 else
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16_proj else "i8",
+        "data": ("synthetic (seeded; bf16 weights and activations drawn on device)" if bf16_proj else
                  "synthetic (seeded; ternary codes, fp16 scales and activations drawn on device)"),
         "config": {"workload": name, "projections_per_pass": R * len(layer),
                    "passes_per_step": reps,

@@ -176,6 +176,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Two-wide fp32 arithmetic (one instruction, two IEEE round-to-nearest
+// operations: the same bits as two scalar ones).
+__device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -369,9 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
             const int m = mt * kTileM + quad * 32 + lane;  // token row of this thread
             const bool mvalid = m < p.M;
-            float acc[64];
+            // accumulators as pairs of adjacent columns (two-wide fp32 ops)
+            unsigned long long acc2[32];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < 32; ++j) acc2[j] = 0ull;
             float2 stv = (mvalid && !failed) ? p.st[m] : make_float2(0.0f, 0.0f);  // group 0
             for (int g = 0; g < G; ++g, ++it) {
                 const int s = it % kStages;
@@ -388,29 +411,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     tc_fence_after();
                     // the 64 weight scales of this thread's columns: 16-byte
                     // broadcast loads (every lane reads the same address)
-                    const float4* ws4 = reinterpret_cast<const float4*>(ws_sm[s] + col0);
+                    const ulonglong2* ws2 = reinterpret_cast<const ulonglong2*>(ws_sm[s] + col0);
+                    const unsigned long long k512 = f2pack(512.0f, 512.0f);
+                    const unsigned long long negt = f2pack(-stv.y, -stv.y);
+                    const unsigned long long sv2 = f2pack(stv.x, stv.x);
 #pragma unroll
                     for (int c = 0; c < 64; c += 32) {
                         float d[32];
                         tmem_ld32(tmem + lane_off + db * 128 + col0 + c, d);
                         tmem_wait_ld();
+                        if (DOTS) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float dot = fmaf(d[j], 512.0f, -stv.y);  // exact integer
-                            if (DOTS) {
+                            for (int j = 0; j < 32; ++j) {
+                                const float dot = fmaf(d[j], 512.0f, -stv.y);  // exact integer
                                 const int n = nt * kTileN + col0 + c + j;
                                 if (mvalid && n < p.N)
                                     p.dots[(static_cast<size_t>(m) * p.N + n) * G + g] =
                                         static_cast<int>(dot);
-                            } else {
-                                // the first group's term seeds the sum (0 + x would
-                                // turn a -0 term into +0)
-                                const float term = dot * stv.x;
-                                const float4 w4 = ws4[(c + j) >> 2];
-                                const float wj = (j & 3) == 0 ? w4.x
-                                               : (j & 3) == 1 ? w4.y
-                                               : (j & 3) == 2 ? w4.z : w4.w;
-                                acc[c + j] = g > 0 ? fmaf(term, wj, acc[c + j]) : term * wj;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 2) {
+                                // exact integer dots of columns j, j + 1, then the
+                                // scales; the first group's term seeds the sum (0 + x
+                                // would turn a -0 term into +0)
+                                const unsigned long long dot2 =
+                                    fma2(f2pack(d[j], d[j + 1]), k512, negt);
+                                const unsigned long long term2 = mul2(dot2, sv2);
+                                const ulonglong2 w4 = ws2[(c + j) >> 2];
+                                const unsigned long long w2 = ((j >> 1) & 1) ? w4.y : w4.x;
+                                const int a = (c + j) >> 1;
+                                acc2[a] = g > 0 ? fma2(term2, w2, acc2[a]) : mul2(term2, w2);
                             }
                         }
                     }
@@ -423,6 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 }
                 stv = st_next;
             }
+            float acc[64];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) f2unpack(acc2[j], acc[2 * j], acc[2 * j + 1]);
             // tile done: acc -> y
             if (!DOTS && !failed && mvalid) {
                 const int nb = nt * kTileN + col0;
