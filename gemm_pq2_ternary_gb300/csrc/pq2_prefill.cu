@@ -41,7 +41,12 @@
 //               registers (64 columns per thread); finally acc -> y.
 // Four D buffers (all 512 columns of tensor memory) give the MMAs three
 // groups of slack on the epilogue.
+//
+// prefill_wide_kernel (below) runs the same arithmetic on 128 x 256 tiles
+// and is the default once its tiles fill every SM.
 // Every mbarrier wait is bounded (device error word on expiry).
+#include <cstdlib>
+
 #include "pq2_internal.h"
 
 namespace {
@@ -484,7 +489,361 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                      "r"(kTmemCols));
 }
 
+// ---------------------------------------------------------------------------
+// wide variant: 128 tokens x 256 weight rows per tile
+// ---------------------------------------------------------------------------
+// The same arithmetic as prefill_kernel (bit-identical y) with twice the MMA
+// work per group: every barrier round trip of the per-group protocol (stage
+// landed, weights expanded, D full, D drained) and every MMA instruction
+// now covers 256 weight rows, and each tensor-core operand read of the token
+// tile serves twice the products.  Tensor memory holds two D buffers of 256
+// columns; three stages of 72 KB fill shared memory.
+//   warp 0        TMA producer
+//   warp 1        TMEM allocation, the MMA issuer (one thread; an N = 256
+//                 MMA keeps the pipe busy for longer than it holds the warp)
+//   warps 2-3     idle
+//   warps 4-7     expansion: weight rows r and r + 128 per thread
+//   warps 8-15    epilogue: a TMEM lane quadrant and 128 columns each, the
+//                 fp32 accumulator (128 columns) in registers
+// Registers: warpgroups 0-1 give theirs back (setmaxnreg.dec to kRegsLow),
+// warpgroups 2-3 take them (setmaxnreg.inc to kRegsHigh).  The launch
+// checks that the kernel's register allocation covers the split.
+constexpr int kWTileN = 256;
+constexpr int kWStages = 3;
+constexpr int kWThreads = 16 * 32;
+constexpr int kWExp0 = 4;             // first expansion warp
+constexpr int kWEpi0 = 8;             // first epilogue warp
+constexpr int kRegsLow = 56;
+constexpr int kRegsHigh = 200;
+constexpr int kWRegsNeeded = 2 * 128 * kRegsLow + 2 * 128 * kRegsHigh;  // 65536
+constexpr uint32_t kWBTileBytes = kWTileN * 128;
+constexpr uint32_t kWCTileBytes = kWTileN * 32;
+constexpr uint32_t kWStageBytes = 2 * kATileBytes + kWBTileBytes + kWCTileBytes;  // 73728
+static_assert(kWStageBytes % 1024 == 0, "stages on 1024-byte boundaries");
+static_assert(kWRegsNeeded <= 65536, "register split");
+
+constexpr uint32_t kWIdesc = (1u << 4) | (0u << 7) | (0u << 10) |
+                             (static_cast<uint32_t>(kWTileN >> 3) << 17) |
+                             (static_cast<uint32_t>(kTileM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f8_wide(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(kWIdesc), "r"(acc));
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid_constant__ PrefillParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t full[kWStages];    // TMA bytes of a stage landed
+    __shared__ uint64_t bready[kWStages];  // expanded weight tile written (8 warps)
+    __shared__ uint64_t empty[kWStages];   // MMAs of the stage done (commit)
+    __shared__ uint64_t wsfree[kWStages];  // epilogue done with a slot of ws_sm (8 warps)
+    __shared__ uint64_t dfull[kDBufs / 2]; // D buffer holds a finished group (commit)
+    __shared__ uint64_t dempty[kDBufs / 2];// epilogue done with a D buffer (8 warps)
+    __shared__ __align__(16) float ws_sm[kWStages][kWTileN];
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    constexpr int kWDBufs = kDBufs / 2;  // 2 buffers of 256 columns
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const uint32_t base = pq2::smem_u32(smem);
+    uint8_t* stage0 = smem + ((1024 - (base & 1023)) & 1023);
+
+    if (tid == 0) {
+        for (int i = 0; i < kWStages; ++i) {
+            pq2::mbar_init(&full[i], 1);
+            pq2::mbar_init(&bready[i], 4);
+            pq2::mbar_init(&empty[i], 1);
+            pq2::mbar_init(&wsfree[i], 8);
+        }
+        for (int i = 0; i < kWDBufs; ++i) {
+            pq2::mbar_init(&dfull[i], 1);
+            pq2::mbar_init(&dempty[i], 8);
+        }
+        abort_flag = 0;
+        pq2::fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         pq2::smem_u32(&tmem_base)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pq2::pdl_wait();
+    pq2::pdl_launch_dependents();
+
+    const uint32_t tmem = tmem_base;
+    const int G = p.G;
+    const int n_tiles_total = p.m_tiles * p.n_tiles;
+    volatile int* abort_v = &abort_flag;
+
+    // Each role's code follows its own setmaxnreg, so that the compiler
+    // allocates its registers to the new limit.
+    if (warp < kWEpi0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            int it = 0;  // global group counter (stage = it % kWStages)
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
+                const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+                for (int g = 0; g < G; ++g, ++it) {
+                    const int s = it % kWStages;
+                    if (it >= kWStages &&
+                        !pq2::mbar_wait_bounded(&empty[s], ((it / kWStages) - 1) & 1, p.ctl, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    if (it == p.ctl.debug_skip_stage) continue;
+                    uint8_t* st = stage0 + static_cast<size_t>(s) * kWStageBytes;
+                    pq2::mbar_arrive_expect_tx(&full[s], kWStageBytes - kWBTileBytes);
+                    pq2::tma_load_2d(st, &p.tm_ahi, g * 128, mt * kTileM, &full[s]);
+                    pq2::tma_load_2d(st + kATileBytes, &p.tm_alo, g * 128, mt * kTileM, &full[s]);
+                    pq2::tma_load_2d(st + 2 * kATileBytes + kWBTileBytes, &p.tm_codes, g * 32,
+                                     nt * kWTileN, &full[s]);
+                }
+            }
+            // drain: every armed stage must have landed before exit
+            const int issued = it;
+            for (int s = 0; s < kWStages; ++s) {
+                if (issued <= s) continue;
+                int last = s + ((issued - 1 - s) / kWStages) * kWStages;
+                if (last == p.ctl.debug_skip_stage) last -= kWStages;
+                if (last >= 0) pq2::mbar_wait_bounded(&full[s], (last / kWStages) & 1, p.ctl);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            int it = 0;
+            int last = -1;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
+                for (int g = 0; g < G; ++g, ++it) {
+                    const int s = it % kWStages;
+                    const int db = it % kWDBufs;
+                    if (!pq2::mbar_spin_bounded(&bready[s], (it / kWStages) & 1, p.ctl, abort_v) ||
+                        (it >= kWDBufs &&
+                         !pq2::mbar_spin_bounded(&dempty[db], ((it / kWDBufs) - 1) & 1, p.ctl,
+                                                 abort_v))) {
+                        ok = false;
+                        *abort_v = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = pq2::smem_u32(stage0 + static_cast<size_t>(s) * kWStageBytes);
+                    const uint32_t d_tmem = tmem + db * kWTileN;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t bdesc = sw128_desc(st + 2 * kATileBytes + 32 * k);
+                        mma_f8_wide(d_tmem, sw128_desc(st + 32 * k), bdesc, k > 0);
+                        mma_f8_wide(d_tmem, sw128_desc(st + kATileBytes + 32 * k), bdesc, 1);
+                    }
+                    mma_commit(&empty[s]);
+                    mma_commit(&dfull[db]);
+                    last = it;
+                }
+            }
+            // no MMA may still be running when tensor memory is released
+            if (last >= 0)
+                pq2::mbar_wait_bounded(&dfull[last % kWDBufs], (last / kWDBufs) & 1, p.ctl);
+        }
+    } else if (warp >= kWExp0 && warp < kWEpi0) {
+        // ------------------------------ expansion ------------------------------
+        const int r0 = (warp - kWExp0) * 32 + lane;  // weight rows r0 and r0 + 128 of the tile
+        const int half = (lane >> 2) & 1;            // conflict-free order of the 2 loads
+        int it = 0;
+        bool failed = false;
+        for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x) {
+            const int nt = tile / p.m_tiles;
+            for (int g = 0; g < G; ++g, ++it) {
+                const int s = it % kWStages;
+                const int n0 = nt * kWTileN + r0;
+                const float wsv0 =
+                    n0 < p.N ? __half2float(p.ws[static_cast<size_t>(n0) * G + g]) : 0.0f;
+                const float wsv1 = n0 + 128 < p.N
+                                       ? __half2float(p.ws[static_cast<size_t>(n0 + 128) * G + g])
+                                       : 0.0f;
+                if (!failed &&
+                    (!pq2::mbar_wait_bounded(&full[s], (it / kWStages) & 1, p.ctl, abort_v) ||
+                     (it >= kWStages &&
+                      !pq2::mbar_wait_bounded(&wsfree[s], ((it / kWStages) - 1) & 1, p.ctl,
+                                              abort_v)))) {
+                    failed = true;
+                    *abort_v = 1;
+                }
+                if (!failed) {
+                    uint8_t* st = stage0 + static_cast<size_t>(s) * kWStageBytes;
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
+                        const int r = r0 + 128 * h;
+                        const uint8_t* crow = st + 2 * kATileBytes + kWBTileBytes + r * 32;
+                        const uint4 ca = *reinterpret_cast<const uint4*>(crow + 16 * half);
+                        const uint4 cb = *reinterpret_cast<const uint4*>(crow + 16 * (half ^ 1));
+                        const uint32_t w[8] = {half ? cb.x : ca.x, half ? cb.y : ca.y,
+                                               half ? cb.z : ca.z, half ? cb.w : ca.w,
+                                               half ? ca.x : cb.x, half ? ca.y : cb.y,
+                                               half ? ca.z : cb.z, half ? ca.w : cb.w};
+                        uint8_t* brow = st + 2 * kATileBytes + r * 128;
+#pragma unroll
+                        for (int pl = 0; pl < 4; ++pl) {
+#pragma unroll
+                            for (int hc = 0; hc < 2; ++hc) {  // 16-byte chunk 2*pl + hc
+                                uint4 v;
+                                v.x = (w[4 * hc + 0] >> (2 * pl)) & 0x03030303u;
+                                v.y = (w[4 * hc + 1] >> (2 * pl)) & 0x03030303u;
+                                v.z = (w[4 * hc + 2] >> (2 * pl)) & 0x03030303u;
+                                v.w = (w[4 * hc + 3] >> (2 * pl)) & 0x03030303u;
+                                const int chunk = (2 * pl + hc) ^ (r & 7);
+                                *reinterpret_cast<uint4*>(brow + 16 * chunk) = v;
+                            }
+                        }
+                        ws_sm[s][r] = h ? wsv1 : wsv0;
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                __syncwarp();
+                if (lane == 0) pq2::mbar_arrive(&bready[s]);
+            }
+        }
+    }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+        // ------------------------------ epilogue ------------------------------
+        const int ew = warp - kWEpi0;      // 0..7
+        const int quad = warp & 3;         // TMEM lane quadrant of this warp
+        const int col0 = (ew >> 2) * 128;  // two warps per quadrant: columns [0,128), [128,256)
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        int it = 0;
+        bool failed = false;
+        for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x) {
+            const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+            const int m = mt * kTileM + quad * 32 + lane;  // token row of this thread
+            const bool mvalid = m < p.M;
+            unsigned long long acc2[64];  // columns 2j, 2j + 1
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc2[j] = 0ull;
+            float2 stv = (mvalid && !failed) ? p.st[m] : make_float2(0.0f, 0.0f);  // group 0
+            for (int g = 0; g < G; ++g, ++it) {
+                const int s = it % kWStages;
+                const int db = it % kWDBufs;
+                float2 st_next = make_float2(0.0f, 0.0f);
+                if (mvalid && g + 1 < G) st_next = p.st[static_cast<size_t>(g + 1) * p.M + m];
+                if (!failed &&
+                    !pq2::mbar_wait_bounded(&dfull[db], (it / kWDBufs) & 1, p.ctl, abort_v)) {
+                    failed = true;
+                    *abort_v = 1;
+                }
+                if (!failed) {
+                    tc_fence_after();
+                    const ulonglong2* ws2 = reinterpret_cast<const ulonglong2*>(ws_sm[s] + col0);
+                    const unsigned long long k512 = f2pack(512.0f, 512.0f);
+                    const unsigned long long negt = f2pack(-stv.y, -stv.y);
+                    const unsigned long long sv2 = f2pack(stv.x, stv.x);
+#pragma unroll
+                    for (int c = 0; c < 128; c += 16) {
+                        float d[16];
+                        tmem_ld16(tmem + lane_off + db * kWTileN + col0 + c, d);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; j += 2) {
+                            // exact integer dots of two columns, then the scales;
+                            // the first group's term seeds the sum
+                            const unsigned long long dot2 = fma2(f2pack(d[j], d[j + 1]), k512, negt);
+                            const unsigned long long term2 = mul2(dot2, sv2);
+                            const ulonglong2 w4 = ws2[(c + j) >> 2];
+                            const unsigned long long w2 = ((j >> 1) & 1) ? w4.y : w4.x;
+                            const int a = (c + j) >> 1;
+                            acc2[a] = g > 0 ? fma2(term2, w2, acc2[a]) : mul2(term2, w2);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    pq2::mbar_arrive(&dempty[db]);
+                    pq2::mbar_arrive(&wsfree[s]);
+                }
+                stv = st_next;
+            }
+            // tile done: acc -> y
+            if (!failed && mvalid) {
+                const int nb = nt * kWTileN + col0;
+                float* yrow = p.y + static_cast<size_t>(m) * p.N + nb;
+                if (nb + 128 <= p.N && (p.N & 3) == 0) {
+#pragma unroll
+                    for (int j = 0; j < 64; j += 2) {
+                        float a0, a1, a2, a3;
+                        f2unpack(acc2[j], a0, a1);
+                        f2unpack(acc2[j + 1], a2, a3);
+                        *reinterpret_cast<float4*>(yrow + 2 * j) = make_float4(a0, a1, a2, a3);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        float a0, a1;
+                        f2unpack(acc2[j], a0, a1);
+                        if (nb + 2 * j < p.N) yrow[2 * j] = a0;
+                        if (nb + 2 * j + 1 < p.N) yrow[2 * j + 1] = a1;
+                    }
+                }
+            }
+        }
+    }
+
+    // teardown: every role is done with tensor memory
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols));
+}
+
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+// PQ2_PREFILL_WIDE (environment, read once): 1 = the 128 x 256 kernel
+// whenever it applies, 2 = never, unset = by tile count.
+int prefill_wide_mode() {
+    static const int mode = [] {
+        const char* v = std::getenv("PQ2_PREFILL_WIDE");
+        const int x = (v && *v) ? std::atoi(v) : 0;
+        return (x == 1 || x == 2) ? x : 0;
+    }();
+    return mode;
+}
+
+// setmaxnreg.inc draws on the registers the block was launched with: the
+// wide kernel runs only if its compiled allocation covers the split (else
+// the raising warps would wait forever).
+bool wide_kernel_fits() {
+    static const bool ok = [] {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, prefill_wide_kernel) != cudaSuccess) return false;
+        return fa.numRegs * kWThreads >= kWRegsNeeded;
+    }();
+    return ok;
+}
 
 }  // namespace
 
@@ -532,6 +891,27 @@ cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, c
     p.m_tiles = static_cast<int>((M + kTileM - 1) / kTileM);
     p.n_tiles = static_cast<int>((N + kTileN - 1) / kTileN);
     p.ctl = ctl;
+    // The wide tiles (128 x 256) once they fill every SM at least once
+    // (measured at N = 17408: M = 512, 1.8 waves, 784 against 660 TOPS for
+    // the 128 x 128 kernel; below one wave the wide tiles leave SMs idle);
+    // the debug integer-dot output always takes the 128 x 128 kernel.
+    const int wide_tiles = p.m_tiles * static_cast<int>((N + kWTileN - 1) / kWTileN);
+    const int wide_mode = prefill_wide_mode();
+    if (!dots && wide_mode != 2 && (wide_mode == 1 || wide_tiles >= dev.num_sms) &&
+        wide_kernel_fits()) {
+        p.n_tiles = static_cast<int>((N + kWTileN - 1) / kWTileN);
+        // code rows in boxes of 256 (the wide tile's weight rows)
+        if (!encode_tmap_2d(&p.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes,
+                            static_cast<uint64_t>(K / 4), static_cast<uint64_t>(N),
+                            static_cast<uint64_t>(K / 4), 32u, kWTileN, false))
+            return cudaErrorInvalidValue;
+        const int grid = wide_tiles < dev.num_sms ? wide_tiles : dev.num_sms;
+        const size_t smem = 1024 + static_cast<size_t>(kWStages) * kWStageBytes;
+        static SmemLimit lim_wide;
+        cudaError_t e = ensure_smem(lim_wide, prefill_wide_kernel, smem);
+        if (e != cudaSuccess) return e;
+        return launch(prefill_wide_kernel, dim3(grid), dim3(kWThreads), smem, st, true, p);
+    }
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = tiles < dev.num_sms ? tiles : dev.num_sms;
     const size_t smem = 1024 + static_cast<size_t>(kStages) * kStageBytes;
