@@ -43,7 +43,8 @@
 // groups of slack on the epilogue.
 //
 // prefill_wide_kernel (below) runs the same arithmetic on 128 x 256 tiles
-// and is the default once its tiles fill every SM.
+// from weights expanded once per call by the preparation kernel; it is the
+// default from 8 token tiles on, once its tiles fill every SM.
 // Every mbarrier wait is bounded (device error word on expiry).
 #include <cstdlib>
 
@@ -98,7 +99,12 @@ __global__ void __launch_bounds__(256) token_planes_kernel(const int8_t* __restr
                                                            uint32_t* __restrict__ ahi,
                                                            uint32_t* __restrict__ alo,
                                                            float2* __restrict__ st, int64_t M,
-                                                           int64_t K) {
+                                                           int64_t K,
+                                                           const uint8_t* __restrict__ codes,
+                                                           const __half* __restrict__ ws,
+                                                           uint8_t* __restrict__ wexp,
+                                                           float* __restrict__ wst, int64_t N,
+                                                           int64_t Npad) {
     pq2::pdl_wait();
     pq2::pdl_launch_dependents();
     const int64_t words = M * K / 4;
@@ -122,6 +128,31 @@ __global__ void __launch_bounds__(256) token_planes_kernel(const int8_t* __restr
         const int64_t m = i / G, g = i - m * G;
         st[g * M + m] = make_float2(S ? S[i] : 0.0f, static_cast<float>(T[i]));
     }
+    if (!wexp) return;
+    // wide kernel: the weights' e4m3 planes, row n of group g being
+    // [plane 0 bytes 0..31 | plane 1 | plane 2 | plane 3] (plane s of code
+    // byte b = (byte >> 2s) & 3, the e4m3 byte c = c * 2^-9), 16 code bytes
+    // per index
+    const int cpr = static_cast<int>(K / 64);  // 16-byte code chunks per row
+    for (int64_t n = blockIdx.x; n < N; n += gridDim.x) {
+        for (int c = threadIdx.x; c < cpr; c += blockDim.x) {
+            const int g = c >> 1, half = c & 1;
+            const uint4 w = *reinterpret_cast<const uint4*>(codes + n * (K / 4) + g * 32 + half * 16);
+            uint8_t* dst = wexp + n * K + g * 128 + half * 16;
+#pragma unroll
+            for (int pl = 0; pl < 4; ++pl) {
+                const uint4 v = make_uint4(
+                    (w.x >> (2 * pl)) & 0x03030303u, (w.y >> (2 * pl)) & 0x03030303u,
+                    (w.z >> (2 * pl)) & 0x03030303u, (w.w >> (2 * pl)) & 0x03030303u);
+                *reinterpret_cast<uint4*>(dst + 32 * pl) = v;
+            }
+        }
+    }
+    // and the weight scales as fp32 [G][Npad], zero past N
+    for (int64_t g = 0; g < G; ++g)
+        for (int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; n < Npad;
+             n += stride)
+            wst[g * Npad + n] = (ws && n < N) ? __half2float(ws[n * G + g]) : 0.0f;
 }
 
 // ---------------------------------------------------------------------------
@@ -493,38 +524,55 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 // wide variant: 128 tokens x 256 weight rows per tile
 // ---------------------------------------------------------------------------
 // The same arithmetic as prefill_kernel (bit-identical y) with twice the MMA
-// work per group: every barrier round trip of the per-group protocol (stage
-// landed, weights expanded, D full, D drained) and every MMA instruction
-// now covers 256 weight rows, and each tensor-core operand read of the token
-// tile serves twice the products.  Tensor memory holds two D buffers of 256
-// columns; three stages of 72 KB fill shared memory.
+// work per group: every barrier round trip of the per-group protocol and
+// every MMA instruction covers 256 weight rows, and each tensor-core read of
+// the token tile serves twice the products.  The weights' e4m3 planes and
+// the weight scales (fp32, [G][Npad]) are written once per call by the
+// preparation kernel, so the TMA engine brings the B tile in the MMA's
+// layout and no warp writes shared memory per group: shared-memory
+// bandwidth, which the tensor cores' operand reads share with every warp's
+// loads, stores and barrier polls, was the limit with expansion warps.
+// Tensor memory holds two D buffers of 256 columns; three stages of 64 KB
+// (token hi and lo planes, expanded weights) fill shared memory, and a ring
+// of kWsSlots weight-scale rows (1 KB each, bulk copies) feeds the epilogue.
 //   warp 0        TMA producer
 //   warp 1        TMEM allocation, the MMA issuer (one thread; an N = 256
 //                 MMA keeps the pipe busy for longer than it holds the warp)
 //   warps 2-3     idle
-//   warps 4-7     expansion: weight rows r and r + 128 per thread
-//   warps 8-15    epilogue: a TMEM lane quadrant and 128 columns each, the
+//   warps 4-11    epilogue: a TMEM lane quadrant and 128 columns each, the
 //                 fp32 accumulator (128 columns) in registers
-// Registers: warpgroups 0-1 give theirs back (setmaxnreg.dec to kRegsLow),
-// warpgroups 2-3 take them (setmaxnreg.inc to kRegsHigh).  The launch
+// Registers: warpgroup 0 gives its back (setmaxnreg.dec to kRegsLow),
+// warpgroups 1-2 take them (setmaxnreg.inc to kRegsHigh).  The launch
 // checks that the kernel's register allocation covers the split.
 constexpr int kWTileN = 256;
 constexpr int kWStages = 3;
-constexpr int kWThreads = 16 * 32;
-constexpr int kWExp0 = 4;             // first expansion warp
-constexpr int kWEpi0 = 8;             // first epilogue warp
-constexpr int kRegsLow = 56;
-constexpr int kRegsHigh = 200;
-constexpr int kWRegsNeeded = 2 * 128 * kRegsLow + 2 * 128 * kRegsHigh;  // 65536
+constexpr int kWsSlots = 6;
+constexpr int kWThreads = 12 * 32;
+constexpr int kWEpi0 = 4;             // first epilogue warp
+constexpr int kRegsLow = 64;
+constexpr int kRegsHigh = 216;
+constexpr int kWRegsNeeded = 128 * kRegsLow + 2 * 128 * kRegsHigh;  // 63488
 constexpr uint32_t kWBTileBytes = kWTileN * 128;
-constexpr uint32_t kWCTileBytes = kWTileN * 32;
-constexpr uint32_t kWStageBytes = 2 * kATileBytes + kWBTileBytes + kWCTileBytes;  // 73728
+constexpr uint32_t kWStageBytes = 2 * kATileBytes + kWBTileBytes;  // 65536
+constexpr uint32_t kWsRowBytes = kWTileN * 4;
 static_assert(kWStageBytes % 1024 == 0, "stages on 1024-byte boundaries");
 static_assert(kWRegsNeeded <= 65536, "register split");
 
 constexpr uint32_t kWIdesc = (1u << 4) | (0u << 7) | (0u << 10) |
                              (static_cast<uint32_t>(kWTileN >> 3) << 17) |
                              (static_cast<uint32_t>(kTileM >> 4) << 24);
+
+struct PrefillWideParams {
+    CUtensorMap tm_ahi;    // e4m3 [M][K], box {128, 128}, 128B swizzle
+    CUtensorMap tm_alo;
+    CUtensorMap tm_b;      // e4m3 planes of the weights [N][K], box {128, 256}, 128B swizzle
+    const float2* st;      // [G][M] (s, t)
+    const float* wst;      // [G][Npad] weight scales, zero past N
+    float* y;              // [M][N]
+    int M, N, K, G, Npad;
+    int m_tiles, n_tiles;
+    pq2::DevCtl ctl;
+};
 
 __device__ __forceinline__ void mma_f8_wide(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
     asm volatile(
@@ -546,18 +594,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid_constant__ PrefillWideParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint64_t full[kWStages];    // TMA bytes of a stage landed
-    __shared__ uint64_t bready[kWStages];  // expanded weight tile written (8 warps)
     __shared__ uint64_t empty[kWStages];   // MMAs of the stage done (commit)
-    __shared__ uint64_t wsfree[kWStages];  // epilogue done with a slot of ws_sm (8 warps)
-    __shared__ uint64_t dfull[kDBufs / 2]; // D buffer holds a finished group (commit)
-    __shared__ uint64_t dempty[kDBufs / 2];// epilogue done with a D buffer (8 warps)
-    __shared__ __align__(16) float ws_sm[kWStages][kWTileN];
+    __shared__ uint64_t wsfull[kWsSlots];  // a weight-scale row landed
+    __shared__ uint64_t wsfree[kWsSlots];  // epilogue done with a weight-scale row (8 warps)
+    __shared__ uint64_t dfull[2];          // D buffer holds a finished group (commit)
+    __shared__ uint64_t dempty[2];         // epilogue done with a D buffer (8 warps)
+    __shared__ __align__(16) float ws_ring[kWsSlots][kWTileN];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    constexpr int kWDBufs = kDBufs / 2;  // 2 buffers of 256 columns
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -568,11 +615,13 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
     if (tid == 0) {
         for (int i = 0; i < kWStages; ++i) {
             pq2::mbar_init(&full[i], 1);
-            pq2::mbar_init(&bready[i], 4);
             pq2::mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < kWsSlots; ++i) {
+            pq2::mbar_init(&wsfull[i], 1);
             pq2::mbar_init(&wsfree[i], 8);
         }
-        for (int i = 0; i < kWDBufs; ++i) {
+        for (int i = 0; i < 2; ++i) {
             pq2::mbar_init(&dfull[i], 1);
             pq2::mbar_init(&dempty[i], 8);
         }
@@ -599,31 +648,39 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
     // Each role's code follows its own setmaxnreg, so that the compiler
     // allocates its registers to the new limit.
     if (warp < kWEpi0) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
-    if (warp == 0) {
-        // ------------------------------ TMA producer ------------------------------
-        if (lane == 0) {
-            int it = 0;  // global group counter (stage = it % kWStages)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+        if (warp == 0 && lane == 0) {
+            // ------------------------------ TMA producer ------------------------------
+            int it = 0;  // global group counter
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
                 const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
                 for (int g = 0; g < G; ++g, ++it) {
                     const int s = it % kWStages;
-                    if (it >= kWStages &&
-                        !pq2::mbar_wait_bounded(&empty[s], ((it / kWStages) - 1) & 1, p.ctl, abort_v)) {
+                    const int w = it % kWsSlots;
+                    if ((it >= kWStages &&
+                         !pq2::mbar_wait_bounded(&empty[s], ((it / kWStages) - 1) & 1, p.ctl,
+                                                 abort_v)) ||
+                        (it >= kWsSlots &&
+                         !pq2::mbar_wait_bounded(&wsfree[w], ((it / kWsSlots) - 1) & 1, p.ctl,
+                                                 abort_v))) {
                         ok = false;
                         break;
                     }
                     if (it == p.ctl.debug_skip_stage) continue;
                     uint8_t* st = stage0 + static_cast<size_t>(s) * kWStageBytes;
-                    pq2::mbar_arrive_expect_tx(&full[s], kWStageBytes - kWBTileBytes);
+                    pq2::mbar_arrive_expect_tx(&full[s], kWStageBytes);
                     pq2::tma_load_2d(st, &p.tm_ahi, g * 128, mt * kTileM, &full[s]);
                     pq2::tma_load_2d(st + kATileBytes, &p.tm_alo, g * 128, mt * kTileM, &full[s]);
-                    pq2::tma_load_2d(st + 2 * kATileBytes + kWBTileBytes, &p.tm_codes, g * 32,
-                                     nt * kWTileN, &full[s]);
+                    pq2::tma_load_2d(st + 2 * kATileBytes, &p.tm_b, g * 128, nt * kWTileN, &full[s]);
+                    pq2::mbar_arrive_expect_tx(&wsfull[w], kWsRowBytes);
+                    pq2::bulk_g2s(ws_ring[w],
+                                  p.wst + static_cast<size_t>(g) * p.Npad +
+                                      static_cast<size_t>(nt) * kWTileN,
+                                  kWsRowBytes, &wsfull[w]);
                 }
             }
-            // drain: every armed stage must have landed before exit
+            // drain: every armed copy must have landed before exit
             const int issued = it;
             for (int s = 0; s < kWStages; ++s) {
                 if (issued <= s) continue;
@@ -631,21 +688,24 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
                 if (last == p.ctl.debug_skip_stage) last -= kWStages;
                 if (last >= 0) pq2::mbar_wait_bounded(&full[s], (last / kWStages) & 1, p.ctl);
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------ MMA issuer ------------------------------
-        if (lane == 0) {
+            for (int w = 0; w < kWsSlots; ++w) {
+                if (issued <= w) continue;
+                int last = w + ((issued - 1 - w) / kWsSlots) * kWsSlots;
+                if (last == p.ctl.debug_skip_stage) last -= kWsSlots;
+                if (last >= 0) pq2::mbar_wait_bounded(&wsfull[w], (last / kWsSlots) & 1, p.ctl);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------ MMA issuer ------------------------------
             int it = 0;
             int last = -1;
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
                 for (int g = 0; g < G; ++g, ++it) {
                     const int s = it % kWStages;
-                    const int db = it % kWDBufs;
-                    if (!pq2::mbar_spin_bounded(&bready[s], (it / kWStages) & 1, p.ctl, abort_v) ||
-                        (it >= kWDBufs &&
-                         !pq2::mbar_spin_bounded(&dempty[db], ((it / kWDBufs) - 1) & 1, p.ctl,
-                                                 abort_v))) {
+                    const int db = it & 1;
+                    if (!pq2::mbar_spin_bounded(&full[s], (it / kWStages) & 1, p.ctl, abort_v) ||
+                        (it >= 2 &&
+                         !pq2::mbar_spin_bounded(&dempty[db], ((it >> 1) - 1) & 1, p.ctl, abort_v))) {
                         ok = false;
                         *abort_v = 1;
                         break;
@@ -665,68 +725,8 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
                 }
             }
             // no MMA may still be running when tensor memory is released
-            if (last >= 0)
-                pq2::mbar_wait_bounded(&dfull[last % kWDBufs], (last / kWDBufs) & 1, p.ctl);
+            if (last >= 0) pq2::mbar_wait_bounded(&dfull[last & 1], (last >> 1) & 1, p.ctl);
         }
-    } else if (warp >= kWExp0 && warp < kWEpi0) {
-        // ------------------------------ expansion ------------------------------
-        const int r0 = (warp - kWExp0) * 32 + lane;  // weight rows r0 and r0 + 128 of the tile
-        const int half = (lane >> 2) & 1;            // conflict-free order of the 2 loads
-        int it = 0;
-        bool failed = false;
-        for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x) {
-            const int nt = tile / p.m_tiles;
-            for (int g = 0; g < G; ++g, ++it) {
-                const int s = it % kWStages;
-                const int n0 = nt * kWTileN + r0;
-                const float wsv0 =
-                    n0 < p.N ? __half2float(p.ws[static_cast<size_t>(n0) * G + g]) : 0.0f;
-                const float wsv1 = n0 + 128 < p.N
-                                       ? __half2float(p.ws[static_cast<size_t>(n0 + 128) * G + g])
-                                       : 0.0f;
-                if (!failed &&
-                    (!pq2::mbar_wait_bounded(&full[s], (it / kWStages) & 1, p.ctl, abort_v) ||
-                     (it >= kWStages &&
-                      !pq2::mbar_wait_bounded(&wsfree[s], ((it / kWStages) - 1) & 1, p.ctl,
-                                              abort_v)))) {
-                    failed = true;
-                    *abort_v = 1;
-                }
-                if (!failed) {
-                    uint8_t* st = stage0 + static_cast<size_t>(s) * kWStageBytes;
-#pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {
-                        const int r = r0 + 128 * h;
-                        const uint8_t* crow = st + 2 * kATileBytes + kWBTileBytes + r * 32;
-                        const uint4 ca = *reinterpret_cast<const uint4*>(crow + 16 * half);
-                        const uint4 cb = *reinterpret_cast<const uint4*>(crow + 16 * (half ^ 1));
-                        const uint32_t w[8] = {half ? cb.x : ca.x, half ? cb.y : ca.y,
-                                               half ? cb.z : ca.z, half ? cb.w : ca.w,
-                                               half ? ca.x : cb.x, half ? ca.y : cb.y,
-                                               half ? ca.z : cb.z, half ? ca.w : cb.w};
-                        uint8_t* brow = st + 2 * kATileBytes + r * 128;
-#pragma unroll
-                        for (int pl = 0; pl < 4; ++pl) {
-#pragma unroll
-                            for (int hc = 0; hc < 2; ++hc) {  // 16-byte chunk 2*pl + hc
-                                uint4 v;
-                                v.x = (w[4 * hc + 0] >> (2 * pl)) & 0x03030303u;
-                                v.y = (w[4 * hc + 1] >> (2 * pl)) & 0x03030303u;
-                                v.z = (w[4 * hc + 2] >> (2 * pl)) & 0x03030303u;
-                                v.w = (w[4 * hc + 3] >> (2 * pl)) & 0x03030303u;
-                                const int chunk = (2 * pl + hc) ^ (r & 7);
-                                *reinterpret_cast<uint4*>(brow + 16 * chunk) = v;
-                            }
-                        }
-                        ws_sm[s][r] = h ? wsv1 : wsv0;
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                }
-                __syncwarp();
-                if (lane == 0) pq2::mbar_arrive(&bready[s]);
-            }
-        }
-    }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
         // ------------------------------ epilogue ------------------------------
@@ -745,28 +745,33 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
             for (int j = 0; j < 64; ++j) acc2[j] = 0ull;
             float2 stv = (mvalid && !failed) ? p.st[m] : make_float2(0.0f, 0.0f);  // group 0
             for (int g = 0; g < G; ++g, ++it) {
-                const int s = it % kWStages;
-                const int db = it % kWDBufs;
+                const int db = it & 1;
+                const int w = it % kWsSlots;
                 float2 st_next = make_float2(0.0f, 0.0f);
                 if (mvalid && g + 1 < G) st_next = p.st[static_cast<size_t>(g + 1) * p.M + m];
                 if (!failed &&
-                    !pq2::mbar_wait_bounded(&dfull[db], (it / kWDBufs) & 1, p.ctl, abort_v)) {
+                    (!pq2::mbar_wait_bounded(&dfull[db], (it >> 1) & 1, p.ctl, abort_v) ||
+                     !pq2::mbar_wait_bounded(&wsfull[w], (it / kWsSlots) & 1, p.ctl, abort_v))) {
                     failed = true;
                     *abort_v = 1;
                 }
                 if (!failed) {
                     tc_fence_after();
-                    const ulonglong2* ws2 = reinterpret_cast<const ulonglong2*>(ws_sm[s] + col0);
+                    const ulonglong2* ws2 = reinterpret_cast<const ulonglong2*>(ws_ring[w] + col0);
                     const unsigned long long k512 = f2pack(512.0f, 512.0f);
                     const unsigned long long negt = f2pack(-stv.y, -stv.y);
                     const unsigned long long sv2 = f2pack(stv.x, stv.x);
+                    // 64 columns per tensor-memory round trip (two loads, one wait)
 #pragma unroll
-                    for (int c = 0; c < 128; c += 16) {
-                        float d[16];
-                        tmem_ld16(tmem + lane_off + db * kWTileN + col0 + c, d);
+                    for (int c = 0; c < 128; c += 64) {
+                        float d[64];
+                        tmem_ld32(tmem + lane_off + db * kWTileN + col0 + c,
+                                  *reinterpret_cast<float(*)[32]>(&d[0]));
+                        tmem_ld32(tmem + lane_off + db * kWTileN + col0 + c + 32,
+                                  *reinterpret_cast<float(*)[32]>(&d[32]));
                         tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 16; j += 2) {
+                        for (int j = 0; j < 64; j += 2) {
                             // exact integer dots of two columns, then the scales;
                             // the first group's term seeds the sum
                             const unsigned long long dot2 = fma2(f2pack(d[j], d[j + 1]), k512, negt);
@@ -782,7 +787,7 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
                 __syncwarp();
                 if (lane == 0) {
                     pq2::mbar_arrive(&dempty[db]);
-                    pq2::mbar_arrive(&wsfree[s]);
+                    pq2::mbar_arrive(&wsfree[w]);
                 }
                 stv = st_next;
             }
@@ -845,31 +850,113 @@ bool wide_kernel_fits() {
     return ok;
 }
 
+// Workspace: token planes hi, lo [M][K]; (s, t) [G][M]; and, for shapes the
+// wide kernel may take, the weights' e4m3 planes [N][K] and the weight
+// scales [G][Npad] fp32 (Npad = N rounded up to 256).  The wide kernel
+// needs at least kWideMinMTiles token tiles (the expansion pass writes N*K
+// bytes once per call: measured at N = 17408, M = 512 it only ties the
+// 128 x 128 kernel, 662 against 659 TOPS, and M = 1024 gains 778 against
+// 685) and at least kWideMinTiles tiles, a bound below the SM count of the
+// GPUs this library is built for; PQ2_PREFILL_WIDE=1 forces it.  The size
+// depends on the shape only, not on the device.
+constexpr int kWideMinTiles = 128;
+constexpr int kWideMinMTiles = 8;
+struct WsLayout {
+    size_t ahi, alo, st, wexp, wst, total;
+    size_t wexp_bytes;
+    int64_t npad;
+};
+WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
+    WsLayout l = {};
+    const int64_t G = K / 128;
+    const int64_t m_tiles = (M + kTileM - 1) / kTileM;
+    const int64_t wide_tiles = m_tiles * ((N + kWTileN - 1) / kWTileN);
+    const int mode = prefill_wide_mode();
+    const bool room =
+        mode == 1 || (mode != 2 && m_tiles >= kWideMinMTiles && wide_tiles >= kWideMinTiles);
+    l.npad = (N + kWTileN - 1) / kWTileN * kWTileN;
+    size_t off = 0;
+    l.ahi = off;
+    off += align256(static_cast<size_t>(M) * K);
+    l.alo = off;
+    off += align256(static_cast<size_t>(M) * K);
+    l.st = off;
+    off += align256(static_cast<size_t>(M) * G * 8);
+    if (room) {
+        l.wexp = off;
+        l.wexp_bytes = static_cast<size_t>(N) * K;
+        off += align256(l.wexp_bytes);
+        l.wst = off;
+        off += align256(static_cast<size_t>(G) * l.npad * 4);
+    }
+    l.total = off;
+    return l;
+}
+
 }  // namespace
 
 namespace pq2h {
 
 size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    (void)N;
-    return 2 * align256(static_cast<size_t>(M) * K) + align256(static_cast<size_t>(M) * (K / 128) * 8);
+    const WsLayout l = ws_layout(M, N, K);
+    return l.total;
 }
 
 cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
                            const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
                            int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                            const DeviceInfo& dev) {
+    const WsLayout l = ws_layout(M, N, K);
     uint8_t* w = static_cast<uint8_t*>(workspace);
-    uint8_t* ahi = w;
-    uint8_t* alo = w + align256(static_cast<size_t>(M) * K);
-    float2* stv = reinterpret_cast<float2*>(w + 2 * align256(static_cast<size_t>(M) * K));
+    uint8_t* ahi = w + l.ahi;
+    uint8_t* alo = w + l.alo;
+    float2* stv = reinterpret_cast<float2*>(w + l.st);
+    const int G = static_cast<int>(K / 128);
+    const int m_tiles = static_cast<int>((M + kTileM - 1) / kTileM);
+    const int wide_tiles = m_tiles * static_cast<int>((N + kWTileN - 1) / kWTileN);
+    // The wide tiles (128 x 256) where the workspace has room for the
+    // expanded weights (ws_layout) and the tiles fill every SM at least once
+    // (below one wave the wide tiles leave SMs idle); the debug integer-dot
+    // output always takes the 128 x 128 kernel.
+    const bool wide = !dots && l.wexp_bytes > 0 && wide_kernel_fits() &&
+                      (prefill_wide_mode() == 1 || wide_tiles >= dev.num_sms);
+    uint8_t* wexp = wide ? w + l.wexp : nullptr;
+    float* wst = wide ? reinterpret_cast<float*>(w + l.wst) : nullptr;
     {
-        const int64_t words = M * K / 4;
+        const int64_t words = M * K / 4 + (wide ? N * K / 64 : 0);
         const int64_t want = (words + 255) / 256;
         const int grid = static_cast<int>(want < dev.num_sms * 16 ? want : dev.num_sms * 16);
         cudaError_t e = launch(token_planes_kernel, dim3(grid), dim3(256), 0, st, true, qp, S, T,
                                reinterpret_cast<uint32_t*>(ahi), reinterpret_cast<uint32_t*>(alo),
-                               stv, M, K);
+                               stv, M, K, codes, ws, wexp, wst, N, l.npad);
         if (e != cudaSuccess) return e;
+    }
+    if (wide) {
+        PrefillWideParams p = {};
+        if (!encode_tmap_2d(&p.tm_ahi, CU_TENSOR_MAP_DATA_TYPE_UINT8, ahi, static_cast<uint64_t>(K),
+                            static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128u, kTileM, true) ||
+            !encode_tmap_2d(&p.tm_alo, CU_TENSOR_MAP_DATA_TYPE_UINT8, alo, static_cast<uint64_t>(K),
+                            static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128u, kTileM, true) ||
+            !encode_tmap_2d(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, wexp, static_cast<uint64_t>(K),
+                            static_cast<uint64_t>(N), static_cast<uint64_t>(K), 128u, kWTileN, true))
+            return cudaErrorInvalidValue;
+        p.st = stv;
+        p.wst = wst;
+        p.y = y;
+        p.M = static_cast<int>(M);
+        p.N = static_cast<int>(N);
+        p.K = static_cast<int>(K);
+        p.G = G;
+        p.Npad = static_cast<int>(l.npad);
+        p.m_tiles = m_tiles;
+        p.n_tiles = static_cast<int>((N + kWTileN - 1) / kWTileN);
+        p.ctl = ctl;
+        const int grid = wide_tiles < dev.num_sms ? wide_tiles : dev.num_sms;
+        const size_t smem = 1024 + static_cast<size_t>(kWStages) * kWStageBytes;
+        static SmemLimit lim_wide;
+        cudaError_t e = ensure_smem(lim_wide, prefill_wide_kernel, smem);
+        if (e != cudaSuccess) return e;
+        return launch(prefill_wide_kernel, dim3(grid), dim3(kWThreads), smem, st, true, p);
     }
     PrefillParams p = {};
     if (!encode_tmap_2d(&p.tm_ahi, CU_TENSOR_MAP_DATA_TYPE_UINT8, ahi, static_cast<uint64_t>(K),
@@ -887,31 +974,10 @@ cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, c
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
-    p.G = static_cast<int>(K / 128);
-    p.m_tiles = static_cast<int>((M + kTileM - 1) / kTileM);
+    p.G = G;
+    p.m_tiles = m_tiles;
     p.n_tiles = static_cast<int>((N + kTileN - 1) / kTileN);
     p.ctl = ctl;
-    // The wide tiles (128 x 256) once they fill every SM at least once
-    // (measured at N = 17408: M = 512, 1.8 waves, 784 against 660 TOPS for
-    // the 128 x 128 kernel; below one wave the wide tiles leave SMs idle);
-    // the debug integer-dot output always takes the 128 x 128 kernel.
-    const int wide_tiles = p.m_tiles * static_cast<int>((N + kWTileN - 1) / kWTileN);
-    const int wide_mode = prefill_wide_mode();
-    if (!dots && wide_mode != 2 && (wide_mode == 1 || wide_tiles >= dev.num_sms) &&
-        wide_kernel_fits()) {
-        p.n_tiles = static_cast<int>((N + kWTileN - 1) / kWTileN);
-        // code rows in boxes of 256 (the wide tile's weight rows)
-        if (!encode_tmap_2d(&p.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes,
-                            static_cast<uint64_t>(K / 4), static_cast<uint64_t>(N),
-                            static_cast<uint64_t>(K / 4), 32u, kWTileN, false))
-            return cudaErrorInvalidValue;
-        const int grid = wide_tiles < dev.num_sms ? wide_tiles : dev.num_sms;
-        const size_t smem = 1024 + static_cast<size_t>(kWStages) * kWStageBytes;
-        static SmemLimit lim_wide;
-        cudaError_t e = ensure_smem(lim_wide, prefill_wide_kernel, smem);
-        if (e != cudaSuccess) return e;
-        return launch(prefill_wide_kernel, dim3(grid), dim3(kWThreads), smem, st, true, p);
-    }
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = tiles < dev.num_sms ? tiles : dev.num_sms;
     const size_t smem = 1024 + static_cast<size_t>(kStages) * kStageBytes;
