@@ -581,19 +581,6 @@ __device__ __forceinline__ void mma_f8_wide(uint32_t d_tmem, uint64_t a, uint64_
         "l"(a), "l"(b), "r"(kWIdesc), "r"(acc));
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid_constant__ PrefillWideParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint64_t full[kWStages];    // TMA bytes of a stage landed
@@ -755,6 +742,9 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
                     failed = true;
                     *abort_v = 1;
                 }
+                // warp-uniform from here: the tensor-memory loads and the
+                // warp barriers below are executed by all 32 lanes or none
+                failed = __any_sync(0xffffffffu, failed);
                 if (!failed) {
                     tc_fence_after();
                     const ulonglong2* ws2 = reinterpret_cast<const ulonglong2*>(ws_ring[w] + col0);
@@ -770,6 +760,12 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
                         tmem_ld32(tmem + lane_off + db * kWTileN + col0 + c + 32,
                                   *reinterpret_cast<float(*)[32]>(&d[32]));
                         tmem_wait_ld();
+                        if (c == 64) {
+                            // every column is in registers: the D buffer is free
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) pq2::mbar_arrive(&dempty[db]);
+                        }
 #pragma unroll
                         for (int j = 0; j < 64; j += 2) {
                             // exact integer dots of two columns, then the scales;
@@ -782,13 +778,14 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
                             acc2[a] = g > 0 ? fma2(term2, w2, acc2[a]) : mul2(term2, w2);
                         }
                     }
+                } else {
+                    // (the failed path never reached the early release)
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) pq2::mbar_arrive(&dempty[db]);
                 }
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    pq2::mbar_arrive(&dempty[db]);
-                    pq2::mbar_arrive(&wsfree[w]);
-                }
+                if (lane == 0) pq2::mbar_arrive(&wsfree[w]);
                 stv = st_next;
             }
             // tile done: acc -> y
