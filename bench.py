@@ -594,13 +594,13 @@ def oracle_sample(layer, kind, seconds):
         rows = min(N, 64)
         if cdist == "bf16":
             xb, wb = inputs.generate_bf16(M, rows, K, seed=100 + i)
-            probs.append((M, K, rows, "bf16", xb, wb))
+            probs.append((M, K, rows, "bf16", (xb, wb)))
             continue
         p = inputs.Problem("sample", M, K, rows, cdist, xdist, 100 + i)
         tern, ws, x = inputs.generate(p)
         qp, S, T = oracle.quantize_act(x)
         codes = oracle.pack(tern)
-        probs.append((M, K, rows, qp, S, codes, ws))
+        probs.append((M, K, rows, "ternary", (qp, S, codes, ws)))
 
     def run(rows_frac):
         units = 0.0
@@ -609,11 +609,12 @@ def oracle_sample(layer, kind, seconds):
             M, K, rows = pr[:3]
             r = max(1, int(rows * rows_frac))
             if pr[3] == "bf16":
-                ref, _ = oracle.gemm_bf16(pr[4], pr[5][:r])
+                xb, wb = pr[4]
+                ref, _ = oracle.gemm_bf16(xb, wb[:r])
                 oracle.f64_to_bf16(ref)
                 units += bf16_bytes(M, r, K)
                 continue
-            qp, S, codes, ws = pr[3:]
+            qp, S, codes, ws = pr[4]
             oracle.matmul(qp, S, codes[:r], ws[:r])
             units += (gemm_bytes(M, r, K) if kind == "GB/s" else 2.0 * M * r * K)
         return units, time.perf_counter() - t0
