@@ -276,6 +276,11 @@ pq2_status pq2_gemm_small(const int8_t* qp, const float* S, const int32_t* T,
     Ctx c;
     s = get_ctx(&c);
     if (s != PQ2_OK) return s;
+    if (pq2h::gemv_multi_supported(M, N, K, c.dev.num_sms))
+        return cuda_status(pq2h::launch_gemv_multi(qp, S, T, codes,
+                                                   static_cast<const __half*>(ws_f16), y, nullptr,
+                                                   M, N, K, static_cast<cudaStream_t>(stream),
+                                                   c.dev));
     return cuda_status(pq2h::launch_small(qp, S, T, codes, static_cast<const __half*>(ws_f16), y,
                                           nullptr, M, N, K, workspace,
                                           static_cast<cudaStream_t>(stream), c.ctl, c.dev));
@@ -413,9 +418,13 @@ pq2_status pq2_group_dots(int op, const int8_t* qp, const int32_t* T, const uint
         return cuda_status(
             pq2h::launch_gemv(nullptr, qp, nullptr, T, codes, nullptr, nullptr, dots, N, K, st,
                               c.ctl, c.dev));
-    if (op == PQ2_OP_SMALL)
+    if (op == PQ2_OP_SMALL) {
+        if (pq2h::gemv_multi_supported(M, N, K, c.dev.num_sms))
+            return cuda_status(pq2h::launch_gemv_multi(qp, nullptr, T, codes, nullptr, nullptr,
+                                                       dots, M, N, K, st, c.dev));
         return cuda_status(pq2h::launch_small(qp, nullptr, T, codes, nullptr, nullptr, dots, M, N,
                                               K, workspace, st, c.ctl, c.dev));
+    }
     // the prefill path needs S only to prepare its token planes
     return cuda_status(pq2h::launch_prefill(qp, nullptr, T, codes, nullptr, nullptr, dots, M, N,
                                             K, workspace, st, c.ctl, c.dev));

@@ -55,6 +55,15 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const
 // workspace: small_workspace_bytes(M, N, K) bytes.
 size_t small_workspace_bytes(int64_t M, int64_t N, int64_t K);
 size_t small_scratch_bytes(int64_t M, int64_t N, int64_t K, int num_sms);
+// A few tokens (2 <= M <= 4 by default, at most 8) on the DP4A path
+// (pq2_multi.cu), where the shape allows: the code words are shared by the
+// token rows.  No workspace.
+bool gemv_multi_supported(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_gemv_multi(const int8_t* qp, const float* S, const int32_t* T,
+                              const uint8_t* codes, const __half* ws, float* y, int32_t* dots,
+                              int64_t M, int64_t N, int64_t K, cudaStream_t st,
+                              const DeviceInfo& dev);
+
 cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
                          const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
                          int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,

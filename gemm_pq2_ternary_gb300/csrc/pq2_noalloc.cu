@@ -64,6 +64,12 @@ pq2_status pq2_gemm_small_noalloc(const int8_t* qp, const float* S, const int32_
     pq2h::DeviceInfo dev;
     pq2::DevCtl ctl;
     if (!pq2h::device_info(&dev) || !pq2h::make_ctl(&ctl)) return PQ2_ERR_CUDA;
+    if (pq2h::gemv_multi_supported(M, N, K, dev.num_sms))  // needs no scratch
+        return pq2h::launch_gemv_multi(qp, S, T, codes, static_cast<const __half*>(ws_f16), y,
+                                       nullptr, M, N, K, static_cast<cudaStream_t>(stream),
+                                       dev) == cudaSuccess
+                   ? PQ2_OK
+                   : PQ2_ERR_CUDA;
     // scratch this shape needs on this device (split-K partial sums)
     if (pq2h::small_scratch_bytes(M, N, K, dev.num_sms) > kScratchBytes) return PQ2_ERR_WORKSPACE;
     void* scratch = scratch_for_current_device();
