@@ -140,13 +140,28 @@ KERNEL_SOURCES = {
     "small": ["pq2_small.cu", "pq2_common.cuh"],
     "prefill": ["pq2_prefill.cu", "pq2_common.cuh"],
     "bf16": ["pq2_bf16.cu", "pq2_common.cuh"],
+    "multi": ["pq2_multi.cu", "pq2_common.cuh"],
 }
+
+
+def small_takes_dp4a(M, N, K, num_sms=152):
+    """The library's routing of pq2_gemm_small (gemv_multi_supported in
+    csrc/pq2_multi.cu, default PQ2_SMALL_DP4A_MAX_M): 2-4 tokens on the DP4A
+    kernel where a CTA's terms fit its shared memory."""
+    if M < 2 or M > int(os.environ.get("PQ2_SMALL_DP4A_MAX_M", "4") or 4):
+        return False
+    mt = 2 if M <= 2 else (4 if M <= 4 else 8)
+    G = K // 128
+    rows = (N + num_sms - 1) // num_sms
+    return G * mt <= 480 and rows * mt * G * 4 <= 160 * 1024
 
 
 def kernel_family(layer):
     if is_bf16(layer[0]):
         return "bf16"
-    M = layer[0][0]
+    M, K, N = layer[0][:3]
+    if small_takes_dp4a(M, N, K):
+        return "multi"
     return "gemv" if M == 1 else ("small" if M <= 16 else "prefill")
 
 
@@ -195,7 +210,8 @@ def per_layer_units(layer, kind, name=""):
 
 def layer_launches(layer, name=""):
     """Kernel launches of one layer: the fused quantise + GEMV for M = 1;
-    quantise, token preparation and matmul otherwise; SwiGLU-quantise and
+    quantise and the DP4A matmul for 2-4 tokens; quantise, token
+    preparation and matmul otherwise; SwiGLU-quantise and
     the matmul (plus its preparation for M > 1) for a chained down
     projection; one split-K launch for a bf16 projection."""
     chain = chain_of(name)
@@ -204,9 +220,9 @@ def layer_launches(layer, name=""):
         if cdist == "bf16":
             n += 1
         elif chain and j == chain[1]:
-            n += 2 if M == 1 else 3
+            n += 2 if M == 1 or small_takes_dp4a(M, N, K) else 3
         else:
-            n += 1 if M == 1 else 3
+            n += 1 if M == 1 else (2 if small_takes_dp4a(M, N, K) else 3)
     return n
 
 
