@@ -2,7 +2,7 @@
 at token counts the DP4A kernel would otherwise take (child process: the
 library reads PQ2_SMALL_DP4A_MAX_M once per process), and the DP4A kernel's
 per-token rows against the M = 1 GEMV on the same token, bit for bit (both
-sum the same group terms in the same order)."""
+sum the same group terms in the same order), at 2, 3 and 4 tokens."""
 import os
 import subprocess
 import sys
@@ -28,7 +28,7 @@ def test_tensor_core_kernel_at_few_tokens():
         assert f"ok {n}" in r.stdout, r.stdout
 
 
-@pytest.mark.parametrize("M,K,N", [(2, 6144, 5120), (3, 5120, 17408), (8, 1280, 999)])
+@pytest.mark.parametrize("M,K,N", [(2, 6144, 5120), (3, 5120, 17408), (4, 1280, 999)])
 def test_dp4a_rows_equal_the_single_token_gemv(M, K, N):
     from gemm_pq2_ternary_gb300 import binding as pq2
     tern, ws, x = inputs.generate(inputs.Problem("bitid", M, K, N, "p343", "outliers", 80 + M))
