@@ -7,12 +7,13 @@
 // The page's kernel writes one fp32 partial per K split to a buffer and sums
 // the splits in order in a second pass.  Here the K splits of one output tile
 // form a thread-block cluster of kSplits CTAs and the partials never leave
-// the chip: each CTA reduces its lanes' partials inside each warp, then
-// stores each warp's partial of every output straight into the shared memory
-// of the cluster rank that owns that output (distributed shared memory).
-// After one cluster barrier each rank sums the (CTA, warp) partials of its
-// outputs in increasing-K order from its own shared memory and rounds each
-// sum once to bf16.  One launch, no workspace, the same bits on every run.
+// the chip: each CTA reduces its lanes' partials inside each warp, sums its
+// warps (in increasing K) through shared memory, and stores its partial of
+// every output straight into the shared memory of the cluster rank that owns
+// that output (distributed shared memory).  After one cluster barrier each
+// rank sums the kSplits partials of its outputs in increasing-K order from
+// its own shared memory and rounds each sum once to bf16.  One launch, no
+// workspace, the same bits on every run.
 //
 // The work is bound by the bytes of w (983,040 for 96 x 5120) and by latency,
 // not by arithmetic (16 x 96 x 5120 multiply-adds at most), so the products
