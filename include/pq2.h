@@ -163,6 +163,10 @@ pq2_status pq2_gemv(const int8_t* qp, const float* S, const int32_t* T,
  *   Same operands as pq2_gemv with M rows; y [M,N].
  *   workspace: device scratch of pq2_workspace_bytes(PQ2_OP_SMALL, M, N, K)
  *   bytes (may be NULL when that is 0).
+ *   2 to 4 token rows run on DP4A, each code word shared by the rows, where
+ *   a CTA's group terms fit its shared memory (the workspace is then not
+ *   touched; each row's y equals pq2_gemv on that row, bit for bit); larger
+ *   M on the tensor cores.
  */
 pq2_status pq2_gemm_small(const int8_t* qp, const float* S, const int32_t* T,
                           const uint8_t* codes, const void* ws_f16, float* y,
@@ -175,7 +179,10 @@ pq2_status pq2_gemm_small(const int8_t* qp, const float* S, const int32_t* T,
  *   output tiles, per-group integer products and the same per-group
  *   dequantise-accumulate order as the M = 1 path).
  *   Same operands as pq2_gemm_small; y [M,N].
- *   workspace: pq2_workspace_bytes(PQ2_OP_PREFILL, M, N, K) bytes.
+ *   workspace: pq2_workspace_bytes(PQ2_OP_PREFILL, M, N, K) bytes; from 8
+ *   token tiles of 128 (M > 896) it includes the weights expanded to one
+ *   byte per weight (N*K bytes), written once per call for the 128 x 256
+ *   tile kernel.
  */
 pq2_status pq2_gemm_prefill(const int8_t* qp, const float* S, const int32_t* T,
                             const uint8_t* codes, const void* ws_f16, float* y,
