@@ -179,10 +179,11 @@ pq2_status pq2_gemm_small(const int8_t* qp, const float* S, const int32_t* T,
  *   output tiles, per-group integer products and the same per-group
  *   dequantise-accumulate order as the M = 1 path).
  *   Same operands as pq2_gemm_small; y [M,N].
- *   workspace: pq2_workspace_bytes(PQ2_OP_PREFILL, M, N, K) bytes; from 8
- *   token tiles of 128 (M > 896) it includes the weights expanded to one
- *   byte per weight (N*K bytes), written once per call for the 128 x 256
- *   tile kernel.
+ *   workspace: pq2_workspace_bytes(PQ2_OP_PREFILL, M, N, K) bytes; for
+ *   shapes the 128 x 256 tile kernel may take (at least 8 tiles of 128
+ *   tokens, M > 896, and at least 128 tiles of 128 x 256) it includes the
+ *   weights expanded to one byte per weight (N*K bytes), written once per
+ *   call.
  */
 pq2_status pq2_gemm_prefill(const int8_t* qp, const float* S, const int32_t* T,
                             const uint8_t* codes, const void* ws_f16, float* y,
