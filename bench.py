@@ -395,6 +395,24 @@ def timed_replays(torch, graph, n, stream):
     return t0.elapsed_time(t1)
 
 
+def max_over_ranks(x, dist, device):
+    """The largest of every rank's x (the job's time is its slowest rank's);
+    x itself with no process group.  Any backend: NCCL with device tensors
+    on GPUs, gloo with CPU tensors."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank, world, seconds, scale):
+    """Aggregate throughput: every rank processes units_per_rank in the same
+    (max-over-ranks) time (weak scaling)."""
+    return units_per_rank * world / seconds * scale
+
+
 def metric_name(kind, name, layer):
     if is_bf16(layer[0]):
         return f"bf16 split-K projection {kind} ({name})"
@@ -442,11 +460,7 @@ def gpu_arm(args, rank, world, dist):
     ms_total = timed_replays(torch, g_step, reps * args.steps, stream)
     barrier()
     clk = clocks.stop()
-    ms_step = ms_total / args.steps
-    if dist is not None:
-        t = torch.tensor([ms_step], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_total / args.steps, dist, device)
 
     # dominant kernel (the matmul) alone, same weight sets, for the roofline
     timed_replays(torch, g_mm, reps, stream)
@@ -456,7 +470,7 @@ def gpu_arm(args, rank, world, dist):
     units_layer = per_layer_units(layer, kind, name)
     units_step = units_layer * R * reps
     scale = 1e-9 if kind == "GB/s" else 1e-12
-    value = units_step * world / (ms_step * 1e-3) * scale
+    value = whole_job_value(units_step, world, ms_step * 1e-3, scale)
 
     hbm, bf16, bf16_sus, peak_src = load_peaks()
     per_launch = units_layer / len(layer)
@@ -582,13 +596,9 @@ def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dis
             one_pass()
         t1.record(stream)
     t1.synchronize()
-    dt = t0.elapsed_time(t1) * 1e-3 / passes
-    if dist is not None:
-        t = torch.tensor([dt], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt = float(t.item())
+    dt = max_over_ranks(t0.elapsed_time(t1) * 1e-3 / passes, dist, device)
     scale = 1e-9 if kind == "GB/s" else 1e-12
-    return {"value": round(units_pass * world / dt * scale, 2), "unit": kind,
+    return {"value": round(whole_job_value(units_pass, world, dt, scale), 2), "unit": kind,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(dt * 1e3, 4),
             "step": "one pass over all projections: copy in, the public call each "
