@@ -40,6 +40,10 @@ import numpy as np  # noqa: E402
 
 HBM_FALLBACK_GBS = 6800.0
 BF16_FALLBACK_TFLOPS = 1900.0
+# nominal GB300 figures (context beside the measured peaks): HBM3e ~8 TB/s,
+# dense bf16 2.25 PFLOP/s
+HBM_NOMINAL_GBS = 8000.0
+BF16_NOMINAL_TFLOPS = 2250.0
 
 
 def load_peaks():
@@ -381,6 +385,22 @@ def capture(torch, fn, stream):
     return g
 
 
+def timed_steps(torch, graph, reps, steps, stream):
+    """`steps` steps of `reps` replays each, back to back on `stream`, with an
+    event after each step (events do not synchronise).  Returns (total ms,
+    per-step ms list)."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(steps):
+            for _ in range(reps):
+                graph.replay()
+            ev[i + 1].record(stream)
+    ev[-1].synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return ev[0].elapsed_time(ev[-1]), per
+
+
 def timed_replays(torch, graph, n, stream):
     """Replays `graph` n times on `stream`; returns elapsed ms (CUDA events
     recorded on that stream)."""
@@ -457,7 +477,7 @@ def gpu_arm(args, rank, world, dist):
     barrier()
     clocks.start()
     time.sleep(0.25)  # let the sampler attach
-    ms_total = timed_replays(torch, g_step, reps * args.steps, stream)
+    ms_total, per_step = timed_steps(torch, g_step, reps, args.steps, stream)
     barrier()
     clk = clocks.stop()
     ms_step = max_over_ranks(ms_total / args.steps, dist, device)
@@ -478,12 +498,14 @@ def gpu_arm(args, rank, world, dist):
         achieved = per_launch / (mm_per_launch_ms * 1e-3) * 1e-9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4),
+                "frac_of_nominal": round(achieved / HBM_NOMINAL_GBS, 4),
                 "traffic": recorded_traffic(name, kernel_family(layer)),
                 "peak_source": f"{peak_src}: MEASURED_PEAKS.json hbm_gbs (copy)"}
     else:
         achieved = per_launch / (mm_per_launch_ms * 1e-3) * 1e-12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
                 "frac": round(achieved / bf16, 4),
+                "frac_of_nominal": round(achieved / BF16_NOMINAL_TFLOPS, 4),
                 "traffic": recorded_traffic(name, kernel_family(layer)),
                 "peak_source": f"{peak_src}: MEASURED_PEAKS.json bf16_tflops (burst)"}
 
@@ -530,6 +552,9 @@ def gpu_arm(args, rank, world, dist):
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "matmul_us_per_launch": round(mm_per_launch_ms * 1e3, 3),
+        "step_ms_spread": {"min": round(min(per_step), 4),
+                           "median": round(float(np.median(per_step)), 4),
+                           "max": round(max(per_step), 4), "rank": rank},
         **({"library_baseline": library} if library else {}),
         "e2e": e2e,
         "gpu_launches": launches,
@@ -663,6 +688,21 @@ def oracle_sample(layer, kind, seconds):
     return tot / dt * scale, desc, threads, dt
 
 
+def oracle_single_core(layer, kind, seconds):
+    """The oracle's C loops on one thread, a shorter sample; None where the
+    sample runs through numpy's BLAS, whose threads the oracle does not set."""
+    if any(is_bf16(pr) for pr in layer):
+        return None
+    import oracle
+    before = oracle.threads()
+    try:
+        oracle.set_threads(1)
+        v, desc, threads, _ = oracle_sample(layer, kind, seconds)
+    finally:
+        oracle.set_threads(before)
+    return {"value": round(v, 6), "unit": kind, "cores": threads, "sample": desc}
+
+
 def reference_arm(args, rank, world):
     name, layer, kind = workload_spec(args)
     if rank != 0:
@@ -738,6 +778,9 @@ def main():
             v, desc, threads, _ = oracle_sample(layer, kind, args.cpu_seconds)
             out["cpu_baseline"] = {"value": round(v, 6), "unit": kind, "cores": threads,
                                    "kind": "oracle", "sample": desc}
+            single = oracle_single_core(layer, kind, args.cpu_seconds / 4)
+            if single is not None:
+                out["cpu_baseline"]["single_core"] = single
         print(json.dumps(out), flush=True)
     if dist is not None:
         dist.barrier()

@@ -27,6 +27,7 @@ def _lib():
         i64, p = ctypes.c_int64, ctypes.c_void_p
         sigs = {
             "pq2o_threads": [],
+            "pq2o_set_threads": [ctypes.c_int],
             "pq2o_quantize": [p, i64, i64, p, p, p],
             "pq2o_plane_order": [p, i64, i64, p],
             "pq2o_natural_order": [p, i64, i64, p],
@@ -59,6 +60,11 @@ def _check(rc, what):
 def threads() -> int:
     """Host threads the oracle's parallel loops use."""
     return int(_lib().pq2o_threads())
+
+
+def set_threads(n: int) -> int:
+    """Sets the oracle's thread count (n >= 1); returns the count in effect."""
+    return int(_lib().pq2o_set_threads(int(n)))
 
 
 def quantize(x_f16: np.ndarray):

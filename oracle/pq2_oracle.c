@@ -76,6 +76,17 @@ int pq2o_threads(void) {
 #endif
 }
 
+/* Sets that number (n >= 1); used to time the oracle on one core.  Returns
+   the number in effect afterwards. */
+int pq2o_set_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+    return pq2o_threads();
+}
+
 /* Position of natural index k (within a row) in plane order. */
 static int64_t plane_pos(int64_t k) {
     int64_t g = k / 128;        /* group                        */

@@ -40,3 +40,26 @@ def test_oracle_sample_runs(workload, m):
     name, layer, kind = bench.workload_spec(_args(workload, m))
     value, desc, threads, dt = bench.oracle_sample(layer, kind, 0.05)
     assert value > 0 and threads >= 1 and dt > 0 and "output rows" in desc
+
+
+def test_oracle_single_core_sample_and_thread_independence():
+    import numpy as np
+
+    import oracle
+    from gemm_pq2_ternary_gb300 import inputs
+    name, layer, kind = bench.workload_spec(_args("decode", 1))
+    single = bench.oracle_single_core(layer, kind, 0.05)
+    assert single["cores"] == 1 and single["value"] > 0
+    assert bench.oracle_single_core(*bench.workload_spec(_args("in_proj_ba", 4))[1:], 0.05) is None
+    # the oracle's parallel loops split output rows only: the same bits on one thread
+    tern, ws, x = inputs.generate(inputs.Problem("thr", 3, 512, 40, "p343", "outliers", 9))
+    qp, S, _ = oracle.quantize_act(x)
+    codes = oracle.pack(tern)
+    before = oracle.threads()
+    try:
+        oracle.set_threads(1)
+        y1, _ = oracle.matmul(qp, S, codes, ws)
+    finally:
+        oracle.set_threads(before)
+    yn, _ = oracle.matmul(qp, S, codes, ws)
+    assert np.array_equal(y1, yn)
