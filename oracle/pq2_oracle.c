@@ -305,8 +305,8 @@ int pq2o_matmul_entries(const int8_t* qp, const float* S, const uint8_t* codes,
 
 /*
  * SwiGLU of the MLP's gate/up output, the activation between the two
- * projections of a decode MLP.  The pages do not define it; SURVEY's next row
- * names it as assumed.  This oracle takes the plain reading:
+ * projections of a decode MLP.  The pages do not define it, so it is an
+ * assumed activation.  This oracle takes the plain reading:
  *   gate = gu[m, 0..I), up = gu[m, I..2I);  h = silu(gate) * up,
  *   silu(g) = g / (1 + exp(-g)),
  * every step one IEEE fp32 operation in this order (the caller rounds h to
