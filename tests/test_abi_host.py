@@ -155,3 +155,20 @@ def test_bf16_splitk_checks_arguments(lib):
     # empty problems enqueue nothing, whatever the pointers
     assert f(None, None, None, 0, 96, 5120, 0, None) == b.PQ2_OK
     assert f(None, None, None, 4, 0, 5120, 0, None) == b.PQ2_OK
+
+
+def test_prefill_workspace_holds_expanded_weights_for_wide_shapes(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    K, N = 5120, 17408
+    G = K // 128
+
+    def planes(M):  # token planes hi and lo, (s, t) per group
+        return 2 * M * K + M * G * 8
+
+    small = b.pq2_workspace_bytes(b.PQ2_OP_PREFILL, 128, N, K)      # one token tile
+    assert planes(128) <= small < planes(128) + N * K
+    big = b.pq2_workspace_bytes(b.PQ2_OP_PREFILL, 4096, N, K)       # 32 token tiles
+    npad = (N + 255) // 256 * 256
+    assert big >= planes(4096) + N * K + G * npad * 4
+    # the matmul's workspace for large M includes the prefill's
+    assert b.pq2_workspace_bytes(b.PQ2_OP_MATMUL, 4096, N, K) >= big
