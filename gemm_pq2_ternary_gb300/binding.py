@@ -204,10 +204,15 @@ def pq2_matmul_ex(x, codes, ws, y, flags, workspace, stream=None):
 
 
 def pq2_gemm_bf16_splitk(x, w, y, flags=0, stream=None):
-    """x [M, K], w [N, K], y [M, N]: torch.bfloat16 (or int16/uint16 bit
-    patterns) on the device."""
+    """x [M, K], w [N, K], y [M, N]: torch.bfloat16 (or int16 bit patterns)
+    on the device."""
+    for t, name in ((x, "x"), (w, "w"), (y, "y")):
+        if t.dtype not in (torch.bfloat16, torch.int16):
+            raise ValueError(f"{name}: expected torch.bfloat16 (or int16 bit patterns), got {t.dtype}")
     M, K = x.shape
-    N = w.shape[0]
+    N, Kw = w.shape
+    if Kw != K or tuple(y.shape) != (M, N):
+        raise ValueError(f"shapes: x {tuple(x.shape)}, w {tuple(w.shape)}, y {tuple(y.shape)}")
     _check(_lib.pq2_gemm_bf16_splitk(_ptr(x), _ptr(w), _ptr(y), M, N, K, flags,
                                      _stream(stream)), "pq2_gemm_bf16_splitk")
 

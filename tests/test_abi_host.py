@@ -172,3 +172,17 @@ def test_prefill_workspace_holds_expanded_weights_for_wide_shapes(lib):
     assert big >= planes(4096) + N * K + G * npad * 4
     # the matmul's workspace for large M includes the prefill's
     assert b.pq2_workspace_bytes(b.PQ2_OP_MATMUL, 4096, N, K) >= big
+
+
+def test_bf16_binding_checks_dtype_and_shapes(lib):
+    import torch
+    from gemm_pq2_ternary_gb300 import binding as b
+    x = torch.zeros((2, 64), dtype=torch.float32)
+    w = torch.zeros((8, 64), dtype=torch.bfloat16)
+    y = torch.zeros((2, 8), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="x: expected"):
+        b.pq2_gemm_bf16_splitk(x, w, y)
+    with pytest.raises(ValueError, match="shapes"):
+        b.pq2_gemm_bf16_splitk(x.bfloat16(), w, torch.zeros((2, 9), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="CUDA"):   # host tensors never reach the library
+        b.pq2_gemm_bf16_splitk(x.bfloat16(), w, y)
