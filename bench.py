@@ -1,7 +1,10 @@
 """Benchmark of the PQ2_0 ternary matmul hot path on GB300.
 
-One JSON line (rank 0).  A step is one pass of the hot path over one batch of
-synthetic input: for each of R distinct projections (distinct weight sets, so
+One JSON line (rank 0).  The default run measures the decode GEMV (the
+headline) and then every configuration of SUITE with shorter timing, each
+with its own roofline, clocks, end-to-end figure, oracle sample and accuracy,
+in the line's `configs` list.  A step is one pass of the hot path over one
+batch of synthetic input: for each of R distinct projections (distinct weight sets, so
 the step's weights exceed 4x L2 and come from HBM), quantise its fp16
 activations (pq2_quantize_act) and run its matmul (pq2_gemv for M = 1,
 pq2_gemm_small for M <= 16, pq2_gemm_prefill above).  The R projections are
@@ -15,6 +18,7 @@ Workloads (--workload):
   mlp      M=--m (1 or 16): gate/up 5120 -> 34816, quantise the synthetic
            intermediate h, down 17408 -> 5120
   prefill  M=--m (128 or 4096), 5120 -> 17408
+  mid      M=--m (17..64), 5120 -> 17408 through pq2_gemm_prefill, in GB/s
   lmhead   M=1, K=5120 -> N=248320 (an lm_head-scale decode GEMV)
   mlp_swiglu  M=--m: gate/up 5120 -> 34816, then the down projection straight
            from its output (pq2_mlp_down_swiglu: SwiGLU + quantise, 17408 -> 5120)
@@ -118,6 +122,10 @@ def workload_spec(args):
     if w == "small":
         K, N = (int(v) for v in args.shape.split(","))
         return f"small_m{args.m}_k{K}_n{N}", [(args.m, K, N, "p343", "outliers")], "GB/s"
+    if w == "mid":
+        if not 16 < args.m <= 64:
+            raise SystemExit("--workload mid takes 17 <= --m <= 64")
+        return f"mid_m{args.m}_k5120_n17408", [(args.m, 5120, 17408, "p343", "outliers")], "GB/s"
     if w == "mlp":
         return f"mlp_pair_m{args.m}", [(args.m, 5120, 34816, "uniform", "normal"),
                                        (args.m, 17408, 5120, "uniform", "normal")], "GB/s"
@@ -150,9 +158,9 @@ KERNEL_SOURCES = {
 
 def small_takes_dp4a(M, N, K, num_sms=152):
     """The library's routing of pq2_gemm_small (gemv_multi_supported in
-    csrc/pq2_multi.cu, default PQ2_SMALL_DP4A_MAX_M): 2-4 tokens on the DP4A
-    kernel where a CTA's terms fit its shared memory."""
-    if M < 2 or M > int(os.environ.get("PQ2_SMALL_DP4A_MAX_M", "4") or 4):
+    csrc/pq2_multi.cu): 2-4 tokens on the DP4A kernel where a CTA's terms fit
+    its shared memory."""
+    if M < 2 or M > 4:
         return False
     mt = 2 if M <= 2 else (4 if M <= 4 else 8)
     G = K // 128
@@ -290,11 +298,18 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+ACC_ROWS = 64       # output rows of the first projection compared with the oracle
+ACC_TOKENS = 256    # at most this many token rows of it
+
+
 def build_layers(args, layer, R, device, name=""):
     """R layers of distinct weight sets.  Each projection type j keeps its
     activations of all R layers in one tensor X[j] [R, M, K] and its outputs
     in Y[j] [R, M, N] (contiguous, so the end-to-end arm copies them in one
-    transfer each)."""
+    transfer each).  Also returns a host copy of the inputs of layer 0's
+    first projection, restricted to its first ACC_ROWS output rows and
+    ACC_TOKENS token rows (drawn by torch's generator on the device, like
+    every weight here), for the accuracy check against the oracle."""
     import torch
     from gemm_pq2_ternary_gb300 import binding as pq2
     from gemm_pq2_ternary_gb300 import inputs
@@ -304,21 +319,31 @@ def build_layers(args, layer, R, device, name=""):
     Y = [torch.empty((R, M, N), dtype=torch.bfloat16 if c == "bf16" else torch.float32,
                      device=device) for (M, K, N, c, _) in layer]
     layers = []
+    sample = None
     for r in range(R):
         gen = torch.Generator(device=device)
         gen.manual_seed(1000 + r)
         projs = []
         for j, (M, K, N, cdist, xdist) in enumerate(layer):
+            rows, toks = min(N, ACC_ROWS), min(M, ACC_TOKENS)
             if cdist == "bf16":
                 w = inputs.draw_bf16_torch((N, K), 0.02, gen, device)
                 X[j][r].copy_(inputs.draw_bf16_torch((M, K), 1.0, gen, device))
                 projs.append(dict(M=M, K=K, N=N, bf16=True, w=w, x=X[j][r], y=Y[j][r]))
+                if r == 0 and j == 0:
+                    sample = dict(bf16=True, rows=rows, toks=toks,
+                                  w=w[:rows].view(torch.int16).cpu().numpy().view("uint16"),
+                                  x=X[j][r][:toks].view(torch.int16).cpu().numpy().view("uint16"))
                 continue
             tern = inputs.draw_ternary_torch(N, K, cdist, gen, device)
             ws = inputs.draw_ws_torch(N, K, gen, device)
             codes, ws_p = pq2.pack(tern, ws)
-            del tern
             X[j][r].copy_(inputs.draw_x_torch(M, K, xdist, gen, device))
+            if r == 0 and j == 0:
+                sample = dict(bf16=False, rows=rows, toks=toks, K=K,
+                              tern=tern[:rows].cpu().numpy(), ws=ws[:rows].cpu().numpy(),
+                              x=X[j][r][:toks].cpu().numpy())
+            del tern
             qp, S, T = pq2.alloc_act(M, K, device)
             op = pq2.PQ2_OP_GEMV if M == 1 else (pq2.PQ2_OP_SMALL if M <= 16 else pq2.PQ2_OP_PREFILL)
             wsp = pq2.alloc_workspace(op, M, N, K, device)
@@ -334,7 +359,7 @@ def build_layers(args, layer, R, device, name=""):
                                               dst["K"], device)
         layers.append(projs)
     torch.cuda.synchronize()
-    return layers, X, Y
+    return layers, X, Y, sample
 
 
 def weight_flags(pq2, args):
@@ -439,20 +464,39 @@ def metric_name(kind, name, layer):
     return f"ternary matmul {kind} ({name})"
 
 
-def gpu_arm(args, rank, world, dist):
+def latency_floor(torch, pq2, layer, R, flags, stream, reps):
+    """Per-launch time of a chain of empty kernels shaped like the fused
+    M = 1 calls of the step (pq2_debug_gemv_floor), captured and replayed
+    like the step: what a dependent chain of calls pays before any byte
+    moves."""
+    M, K, N = layer[0][:3]
+
+    def fn():
+        for _ in range(R):
+            for (_, k, n, _, _) in layer:
+                pq2.pq2_debug_gemv_floor(n, k, flags)
+    g = capture(torch, fn, stream)
+    timed_replays(torch, g, reps, stream)
+    ms = timed_replays(torch, g, reps, stream)
+    return ms * 1e3 / (reps * R * len(layer))
+
+
+def measure(args, wl, rank, world, dist, steps, warmup, target_ms, e2e_passes, floor):
+    """Build R layers of the workload, capture the step graph, time `steps`
+    steps of `reps` replays (after `warmup` untimed ones), then the dominant
+    kernel alone, the latency floor (M = 1, if `floor`) and the end-to-end
+    arm.  Returns (bench-line dict, accuracy sample, Y)."""
     import torch
     from gemm_pq2_ternary_gb300 import binding as pq2
 
+    name, layer, kind = wl
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    props = torch.cuda.get_device_properties(device)
-    l2 = props.L2_cache_size
-    name, layer, kind = workload_spec(args)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
     layer_weight_bytes = sum(weight_bytes(pr) for pr in layer)
     bf16_proj = is_bf16(layer[0])
     R = args.projections or max(1, math.ceil(4 * l2 / layer_weight_bytes))
-    layers, X, Y = build_layers(args, layer, R, device, name)
+    layers, X, Y, sample = build_layers(args, layer, R, device, name)
 
     stream = torch.cuda.Stream(device)
     flags = weight_flags(pq2, args)
@@ -460,11 +504,11 @@ def gpu_arm(args, rank, world, dist):
     g_mm = capture(torch, step_fn(pq2, layers, matmul_only=True, flags=flags), stream)
     assert pq2.pq2_last_device_error(stream) == pq2.PQ2_OK
 
-    # A step replays the R-layer graph `reps` times, so the timed region
-    # lasts long enough for the clock sampler (>= ~1.5 s over all steps).
+    # A step replays the R-layer graph `reps` times, so that the timed region
+    # lasts about target_ms over all steps (long enough for the clock sampler).
     timed_replays(torch, g_step, 3, stream)
     t_rep = timed_replays(torch, g_step, 3, stream) / 3
-    reps = args.reps or max(1, math.ceil(1500.0 / (args.steps * t_rep)))
+    reps = args.reps or max(1, math.ceil(target_ms / (steps * t_rep)))
 
     def barrier():
         if dist is not None:
@@ -472,20 +516,20 @@ def gpu_arm(args, rank, world, dist):
         torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         timed_replays(torch, g_step, reps, stream)
     barrier()
     clocks.start()
     time.sleep(0.25)  # let the sampler attach
-    ms_total, per_step = timed_steps(torch, g_step, reps, args.steps, stream)
+    ms_total, per_step = timed_steps(torch, g_step, reps, steps, stream)
     barrier()
     clk = clocks.stop()
-    ms_step = max_over_ranks(ms_total / args.steps, dist, device)
+    ms_step = max_over_ranks(ms_total / steps, dist, device)
 
     # dominant kernel (the matmul) alone, same weight sets, for the roofline
     timed_replays(torch, g_mm, reps, stream)
-    ms_mm = timed_replays(torch, g_mm, reps * args.steps, stream)
-    mm_per_launch_ms = ms_mm / (reps * args.steps * R * len(layer))
+    ms_mm = timed_replays(torch, g_mm, reps * steps, stream)
+    mm_per_launch_ms = ms_mm / (reps * steps * R * len(layer))
 
     units_layer = per_layer_units(layer, kind, name)
     units_step = units_layer * R * reps
@@ -509,16 +553,20 @@ def gpu_arm(args, rank, world, dist):
                 "traffic": recorded_traffic(name, kernel_family(layer)),
                 "peak_source": f"{peak_src}: MEASURED_PEAKS.json bf16_tflops (burst)"}
 
+    floor_us = None
+    if floor and all(M == 1 and not is_bf16(pr) for pr in layer for M in [pr[0]]):
+        floor_us = latency_floor(torch, pq2, layer, R, flags, stream, reps)
+
     library = None
     if bf16_proj:
-        library = library_baseline(torch, layers, stream, reps, args.steps, R * len(layer))
+        library = library_baseline(torch, layers, stream, reps, steps, R * len(layer))
 
     e2e = None
-    if not args.no_e2e:
-        e2e = e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_layer * R, world,
-                      dist, device, name)
+    if e2e_passes and not args.no_e2e:
+        e2e = e2e_arm(torch, pq2, layers, X, Y, flags, stream, kind, units_layer * R, world,
+                      dist, device, name, e2e_passes)
 
-    launches = args.steps * reps * R * layer_launches(layer, name)
+    launches = steps * reps * R * layer_launches(layer, name)
     if bf16_proj:
         arith = "bf16 x bf16 products and fp32 sums on the CUDA cores, one rounding to bf16"
         graph = ("one CUDA graph per pass (per projection one pq2_gemm_bf16_splitk launch), "
@@ -529,8 +577,8 @@ def gpu_arm(args, rank, world, dist):
                  "for M=1, quantise then matmul otherwise), programmatic dependent launch")
     out = {
         "metric": metric_name(kind, name, layer),
-        "value": round(value, 2), "unit": kind, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "value": round(value, 2), "unit": kind, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16_proj else "i8",
         "data": ("synthetic (seeded; bf16 weights and activations drawn on device)" if bf16_proj else
                  "synthetic (seeded; ternary codes, fp16 scales and activations drawn on device)"),
@@ -552,6 +600,11 @@ def gpu_arm(args, rank, world, dist):
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "matmul_us_per_launch": round(mm_per_launch_ms * 1e3, 3),
+        **({"latency_floor_us": round(floor_us, 3),
+            "latency_floor": ("per-launch time of a captured chain of empty kernels with the "
+                              "same grid, block, shared memory and dependent-launch attributes "
+                              "as the step's calls (pq2_debug_gemv_floor), same run")}
+           if floor_us is not None else {}),
         "step_ms_spread": {"min": round(min(per_step), 4),
                            "median": round(float(np.median(per_step)), 4),
                            "max": round(max(per_step), 4), "rank": rank},
@@ -560,7 +613,16 @@ def gpu_arm(args, rank, world, dist):
         "gpu_launches": launches,
         "clocks": clk,
     }
-    return out, (name, layer, kind)
+    if sample is not None:
+        sample["y"] = Y[0][0][:sample["toks"], :sample["rows"]]
+        if sample["bf16"]:
+            sample["y"] = sample["y"].view(torch.int16).cpu().numpy().view("uint16")
+        else:
+            sample["y"] = sample["y"].cpu().numpy()
+    del layers, X, Y, g_step, g_mm
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out, sample
 
 
 def library_baseline(torch, layers, stream, reps, steps, calls_per_pass):
@@ -577,15 +639,14 @@ def library_baseline(torch, layers, stream, reps, steps, calls_per_pass):
             "us_per_call": round(ms * 1e3 / (reps * steps * calls_per_pass), 3)}
 
 
-def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dist, device,
-            name=""):
+def e2e_arm(torch, pq2, layers, X, Y, flags, stream, kind, units_pass, world, dist, device,
+            name, passes):
     """The same metric through pq2_matmul_ex (the public call, eager) with host
     buffers: every pass copies all activations in from pinned host memory
     and all outputs back, inside the timed region (CUDA events on the
     stream).  In a SwiGLU chain the down projection's input is the gate/up
     output on the device, and only the down projection's output is read
     back."""
-    flags = weight_flags(pq2, args)
     chain = chain_of(name)
     if chain:
         X = [x for j, x in enumerate(X) if j != chain[1]]
@@ -609,7 +670,6 @@ def e2e_arm(torch, pq2, layers, X, Y, args, stream, kind, units_pass, world, dis
         for y, yh in zip(Y, Yh):
             yh.copy_(y, non_blocking=True)
 
-    passes = max(3, min(args.steps, 20))
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -688,6 +748,36 @@ def oracle_sample(layer, kind, seconds):
     return tot / dt * scale, desc, threads, dt
 
 
+def accuracy(sample):
+    """The pages' accuracy measures for the GPU's output rows in `sample`
+    (the first output rows and token rows of one projection of the step,
+    inputs copied back from the device) against the oracle on the same
+    inputs: the relative RMS error ([P1] "One token at a time": rel-RMS of
+    the reordered fp32 sum) and the largest elementwise relative error over
+    outputs with |ref| > 1e-3 * A, A = sum_g |dot_g * s * ws| (where ref is
+    near 0 against A, cancellation makes the relative error meaningless);
+    `within_tolerance` applies the parity tests' bound to every sampled
+    output."""
+    import oracle
+    if sample["bf16"]:
+        ref, A = oracle.gemm_bf16(sample["x"], sample["w"])
+        got = oracle.bf16_to_f64(sample["y"])
+        tol = oracle.bf16_gemm_tolerance(ref, A, sample["x"].shape[1])
+    else:
+        qp, S, _ = oracle.quantize_act(sample["x"])
+        ref, A = oracle.matmul(qp, S, oracle.pack(sample["tern"]), sample["ws"])
+        got = sample["y"].astype(np.float64)
+        tol = oracle.fp32_tolerance(ref, A, sample["K"] // 128)
+    err = np.abs(got - ref)
+    big = np.abs(ref) > 1e-3 * A
+    return {"rel_rms": float(np.sqrt(np.sum(err ** 2) / max(np.sum(ref ** 2), 1e-300))),
+            "max_rel_err": float(np.max(err[big] / np.abs(ref[big]))) if big.any() else 0.0,
+            "within_tolerance": bool(np.all(err <= tol)),
+            "outputs": int(ref.size),
+            "sample": f"first {ref.shape[1]} output rows x first {ref.shape[0]} tokens of the "
+                      f"first projection, inputs copied from the device"}
+
+
 def oracle_single_core(layer, kind, seconds):
     """The oracle's C loops on one thread, a shorter sample; None where the
     sample runs through numpy's BLAS, whose threads the oracle does not set."""
@@ -731,15 +821,54 @@ def reference_arm(args, rank, world):
     }
 
 
+# The configurations of the default run (besides the decode headline), each
+# as (workload, M, "K,N"): the PR1 reference shape, the small-batch sweep,
+# the MLP pair, prefill, 17-64 tokens, and the next rows (lm_head-scale
+# GEMV, the bf16 projection, the SwiGLU-chained MLP).
+SUITE = ([("pr1", 1, None)] +
+         [("small", m, sh) for m in (2, 4, 8, 16) for sh in ("6144,5120", "5120,17408")] +
+         [("mlp", 1, None), ("mlp", 16, None), ("prefill", 128, None), ("prefill", 4096, None),
+          ("mid", 32, None), ("mid", 64, None),
+          ("lmhead", 1, None), ("in_proj_ba", 4, None), ("mlp_swiglu", 1, None)])
+
+
+def suite_entry(args, workload, m, shape, rank, world, dist):
+    """One configuration of the default run: short timing, then the oracle on
+    a short sample and the accuracy of the GPU's sampled outputs."""
+    sub = argparse.Namespace(**vars(args))
+    sub.workload, sub.m = workload, m
+    if shape:
+        sub.shape = shape
+    wl = workload_spec(sub)
+    line, sample = measure(sub, wl, rank, world, dist, steps=args.config_steps, warmup=3,
+                           target_ms=args.config_ms, e2e_passes=3, floor=False)
+    keep = ("metric", "value", "unit", "ms_per_step", "roofline", "matmul_us_per_launch",
+            "gpu_launches", "clocks", "library_baseline", "steps", "warmup")
+    entry = {"workload": wl[0], **{k: line[k] for k in keep if k in line},
+             "config": {k: line["config"][k] for k in ("shapes", "projections_per_pass",
+                                                       "passes_per_step", "l2")},
+             "e2e": line["e2e"] and {k: line["e2e"][k] for k in ("value", "unit",
+                                                                  "h2d_bytes_per_step",
+                                                                  "d2h_bytes_per_step")}}
+    if rank == 0 and not args.no_cpu_baseline:
+        v, desc, threads, _ = oracle_sample(wl[1], wl[2], args.config_cpu_seconds)
+        entry["cpu_baseline"] = {"value": round(v, 6), "unit": wl[2], "cores": threads,
+                                 "kind": "oracle", "sample": desc}
+        entry["accuracy"] = accuracy(sample)
+    return entry
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pq2", choices=["pq2", "reference"])
-    ap.add_argument("--workload", default="decode",
-                    choices=["decode", "pr1", "small", "mlp", "mlp_swiglu", "prefill", "lmhead",
-                             "in_proj_ba"])
+    ap.add_argument("--workload", default=None,
+                    choices=["decode", "pr1", "small", "mid", "mlp", "mlp_swiglu", "prefill",
+                             "lmhead", "in_proj_ba"],
+                    help="one workload alone (default: the decode headline plus every "
+                         "configuration in `configs`)")
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--shape", default="5120,17408")
     ap.add_argument("--projections", type=int, default=0, help="weight sets per step (0: auto)")
@@ -750,11 +879,20 @@ def main():
                          "preceding call ends); default: plain pq2_matmul ordering")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="default run: the decode headline only")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    ap.add_argument("--config-steps", type=int, default=5)
+    ap.add_argument("--config-ms", type=float, default=400.0,
+                    help="timed milliseconds per configuration of the default run")
+    ap.add_argument("--config-cpu-seconds", type=float, default=1.0)
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    suite = args.workload is None and not args.no_configs
+    if args.workload is None:
+        args.workload = "decode"
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -766,21 +904,26 @@ def main():
             print(json.dumps(out), flush=True)
         return
 
+    import torch
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     if world > 1:
-        import torch
         import torch.distributed as tdist
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         tdist.init_process_group("nccl")
         dist = tdist
-    out, (name, layer, kind) = gpu_arm(args, rank, world, dist)
+    wl = workload_spec(args)
+    out, sample = measure(args, wl, rank, world, dist, steps=args.steps, warmup=args.warmup,
+                          target_ms=1500.0, e2e_passes=max(3, min(args.steps, 20)), floor=True)
+    if rank == 0 and not args.no_cpu_baseline:
+        v, desc, threads, _ = oracle_sample(wl[1], wl[2], args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(v, 6), "unit": wl[2], "cores": threads,
+                               "kind": "oracle", "sample": desc}
+        single = oracle_single_core(wl[1], wl[2], args.cpu_seconds / 4)
+        if single is not None:
+            out["cpu_baseline"]["single_core"] = single
+        out["accuracy"] = accuracy(sample)
+    if suite:
+        out["configs"] = [suite_entry(args, w, m, sh, rank, world, dist) for (w, m, sh) in SUITE]
     if rank == 0:
-        if not args.no_cpu_baseline:
-            v, desc, threads, _ = oracle_sample(layer, kind, args.cpu_seconds)
-            out["cpu_baseline"] = {"value": round(v, 6), "unit": kind, "cores": threads,
-                                   "kind": "oracle", "sample": desc}
-            single = oracle_single_core(layer, kind, args.cpu_seconds / 4)
-            if single is not None:
-                out["cpu_baseline"]["single_core"] = single
         print(json.dumps(out), flush=True)
     if dist is not None:
         dist.barrier()

@@ -30,10 +30,19 @@ PQ2_OP_SWIGLU_DOWN = 4
 
 PQ2_WEIGHTS_STATIC = 1
 
+# kernel variants for pq2_debug_force_kernel
+PQ2_VARIANT_DEFAULT = 0
+PQ2_VARIANT_GEMV_DIRECT = 1
+PQ2_VARIANT_GEMV_RING = 2
+PQ2_VARIANT_GEMV_STAGED = 3
+PQ2_VARIANT_SMALL_DP4A = 1
+PQ2_VARIANT_SMALL_TC = 2
+PQ2_VARIANT_PREFILL_128 = 1
+PQ2_VARIANT_PREFILL_WIDE = 2
+
 SIZE_MAX = ctypes.c_size_t(-1).value
 
-# Exported names and argument types (every one declared in include/pq2.h,
-# plus the undocumented test hook pq2_debug_skip_stage).
+# Exported names and argument types (every one declared in include/pq2.h).
 _P, _I64, _SZ, _I, _U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint64
 _U32 = ctypes.c_uint32
 SIGNATURES = {
@@ -54,6 +63,8 @@ SIGNATURES = {
     "pq2_last_device_error": ([_P], _I),
     "pq2_debug_set_wait_limit_ns": ([_U64], _I),
     "pq2_debug_skip_stage": ([_I], _I),
+    "pq2_debug_force_kernel": ([_I, _I], _I),
+    "pq2_debug_gemv_floor": ([_I64, _I64, _U32, _P], _I),
     "pq2_gemm_small_noalloc": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _I),
     "pq2_gemm_small_noalloc_max_scratch": ([], _SZ),
 }
@@ -249,6 +260,31 @@ def pq2_debug_set_wait_limit_ns(ns: int):
 
 def pq2_debug_skip_stage(stage: int):
     _check(_lib.pq2_debug_skip_stage(stage), "pq2_debug_skip_stage")
+
+
+def pq2_debug_force_kernel(op: int, variant: int):
+    _check(_lib.pq2_debug_force_kernel(op, variant), "pq2_debug_force_kernel")
+
+
+def pq2_debug_gemv_floor(N: int, K: int, flags: int = 0, stream=None):
+    """One empty launch shaped like a fused M = 1 call (the latency floor)."""
+    _check(_lib.pq2_debug_gemv_floor(N, K, flags, _stream(stream)), "pq2_debug_gemv_floor")
+
+
+class forced_kernel:
+    """Context manager: calls of `op` run kernel `variant` inside the block
+    (pq2_debug_force_kernel), the library's own routing again after it."""
+
+    def __init__(self, op: int, variant: int):
+        self.op, self.variant = op, variant
+
+    def __enter__(self):
+        pq2_debug_force_kernel(self.op, self.variant)
+        return self
+
+    def __exit__(self, *exc):
+        pq2_debug_force_kernel(self.op, PQ2_VARIANT_DEFAULT)
+        return False
 
 
 # ---------------------------------------------------------------------------

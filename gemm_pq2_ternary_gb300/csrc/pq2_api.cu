@@ -1,7 +1,6 @@
 // The C ABI (include/pq2.h): host-side argument checks, per-device set-up,
 // routing to the kernels, and the device error word.
 #include <atomic>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -19,10 +18,19 @@ pq2h::DeviceInfo g_dev[kMaxDevices];
 bool g_dev_ok[kMaxDevices] = {};
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_debug_skip_stage{-1};
+// pq2_debug_force_kernel: forced variant per op (GEMV, SMALL, PREFILL)
+std::atomic<int> g_force[3] = {{0}, {0}, {0}};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-pq2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PQ2_OK : PQ2_ERR_CUDA; }
+pq2_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return PQ2_OK;
+    if (e == pq2h::kUnsupportedVariant) {
+        cudaGetLastError();  // (not sticky; clear it all the same)
+        return PQ2_ERR_UNSUPPORTED_SHAPE;
+    }
+    return PQ2_ERR_CUDA;
+}
 
 // Common shape checks: K a positive multiple of 128 within the supported
 // range, N >= 1.
@@ -50,13 +58,8 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 namespace pq2h {
 
-// Suspend-time hint for mbarrier waits, PQ2_WAIT_HINT_NS (read once; tuning).
-unsigned wait_hint_ns() {
-    static const unsigned v = [] {
-        const char* e = std::getenv("PQ2_WAIT_HINT_NS");
-        return e && *e ? static_cast<unsigned>(std::strtoul(e, nullptr, 10)) : 0u;
-    }();
-    return v;
+int forced_variant(int op) {
+    return (op >= PQ2_OP_GEMV && op <= PQ2_OP_PREFILL) ? g_force[op].load() : PQ2_VARIANT_DEFAULT;
 }
 
 bool device_info(DeviceInfo* out) {
@@ -123,7 +126,6 @@ bool make_ctl(pq2::DevCtl* ctl) {
     ctl->err = d.err;
     ctl->wait_limit_ns = g_wait_limit_ns.load();
     ctl->debug_skip_stage = g_debug_skip_stage.load();
-    ctl->wait_hint_ns = wait_hint_ns();
     return true;
 }
 
@@ -158,6 +160,28 @@ pq2_status pq2_debug_set_wait_limit_ns(uint64_t ns) {
 pq2_status pq2_debug_skip_stage(int stage) {
     g_debug_skip_stage.store(stage < 0 ? -1 : stage);
     return PQ2_OK;
+}
+
+pq2_status pq2_debug_force_kernel(int op, int variant) {
+    int max_variant = -1;
+    if (op == PQ2_OP_GEMV) max_variant = PQ2_VARIANT_GEMV_STAGED;
+    if (op == PQ2_OP_SMALL) max_variant = PQ2_VARIANT_SMALL_TC;
+    if (op == PQ2_OP_PREFILL) max_variant = PQ2_VARIANT_PREFILL_WIDE;
+    if (variant < 0 || variant > max_variant) return PQ2_ERR_INVALID_ARG;
+    g_force[op].store(variant);
+    return PQ2_OK;
+}
+
+pq2_status pq2_debug_gemv_floor(int64_t N, int64_t K, uint32_t flags, void* stream) {
+    if (flags & ~static_cast<uint32_t>(PQ2_WEIGHTS_STATIC)) return PQ2_ERR_INVALID_ARG;
+    pq2_status s = check_nk(N, K);
+    if (s != PQ2_OK) return s;
+    if (!pq2h::gemv_fused_supported(K)) return PQ2_ERR_UNSUPPORTED_SHAPE;
+    Ctx c;
+    s = get_ctx(&c);
+    if (s != PQ2_OK) return s;
+    return cuda_status(pq2h::launch_gemv_floor(N, K, (flags & PQ2_WEIGHTS_STATIC) != 0,
+                                               static_cast<cudaStream_t>(stream), c.ctl, c.dev));
 }
 
 pq2_status pq2_quantize_act(const void* x_f16, int64_t M, int64_t K, int8_t* qp, float* S,

@@ -27,7 +27,6 @@ enum : unsigned {
 struct DevCtl {
     unsigned* err;          // device error word (never null)
     unsigned long long wait_limit_ns;
-    unsigned wait_hint_ns;  // suspend-time hint of mbarrier try_wait (0 = none)
     int debug_skip_stage;   // >= 0: producer withholds that stage (timeout tests)
 };
 
@@ -63,27 +62,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
-// try_wait; with a non-zero suspend-time hint the thread may sleep until the
-// phase completes or the hint (ns) passes.
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, unsigned hint_ns) {
+// try_wait: the thread may be suspended for a system-dependent time until
+// the phase completes.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
-    if (hint_ns) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity)
-            : "memory");
-    }
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
     return ok != 0;
 }
 
@@ -108,10 +97,10 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   const DevCtl& ctl,
                                                   volatile int* abort_flag = nullptr) {
-    if (mbar_try_wait(bar, parity, ctl.wait_hint_ns)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity, ctl.wait_hint_ns)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         // after a few polls, yield the scheduler between polls: a polling
         // warp otherwise takes issue slots from the warps it waits for
         if (i >= 8) __nanosleep(32);

@@ -53,7 +53,6 @@
 //    barrier per chunk).
 //  * Every mbarrier wait is bounded; on expiry the block sets the device
 //    error word, stops, and the producer waits for its copies in flight.
-#include <cstdlib>
 
 #include "pq2_internal.h"
 
@@ -80,10 +79,6 @@ struct GemvParams {
     uint32_t codes_row_bytes;  // K / 4
     uint32_t act_off, red_off, ring_off;  // shared-memory layout
     uint32_t ws_off;                      // staged variant: weight scales
-    int prefetch;              // L2 prefetch of the CTA's weights before the wait
-    int prefetch_x;            // fused paths: L2 prefetch of x before the wait
-    int trigger;               // staged variant: 0 trigger dependents after the wait,
-                               // 1 after the activations are quantised, 2 after the dots
     pq2::DevCtl ctl;
 };
 
@@ -91,14 +86,6 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ void prefetch_range(const uint8_t* src, size_t bytes) {
-    while (bytes > 0) {
-        const uint32_t b = bytes < 65536u ? static_cast<uint32_t>(bytes) : 65536u;
-        bulk_prefetch_l2(src, b);
-        src += b;
-        bytes -= b;
-    }
-}
 
 // One CTA per SM; many consumer warps hide the shared-memory and DP4A
 // latencies of the group dots (the variant with one group per thread keeps to
@@ -172,18 +159,6 @@ __global__ void __launch_bounds__((GPT == 1 ? kMaxConsumersSmall : kMaxConsumers
         pq2::mbar_init(abar, 1);
         *abort_flag = 0;
         pq2::fence_mbar_init();
-    }
-    if (tid == p.TC && p.prefetch) {
-        // Start pulling this CTA's weights into L2 before waiting for the
-        // preceding kernel.  They are not its output in normal use; and even
-        // if they were, a prefetch into L2 (the coherence point) cannot make
-        // the copies issued after the wait return stale data.
-        const size_t rows = static_cast<size_t>(n_end - n_begin);
-        prefetch_range(p.codes + static_cast<size_t>(n_begin) * p.codes_row_bytes,
-                       rows * p.codes_row_bytes);
-        if (WS_SMEM)
-            prefetch_range(reinterpret_cast<const uint8_t*>(p.ws + static_cast<size_t>(n_begin) * p.G),
-                           rows * p.G * 2);
     }
     __syncthreads();
     // Activations, scales and (possibly) weights may come from the preceding
@@ -433,7 +408,7 @@ __global__ void __launch_bounds__(kDirectConsumers + 32, 1) gemv_direct_kernel(c
     // kernel: wait for it before reading any of them.  (An L2 prefetch of x
     // before the wait is only a hint: a write by that kernel still lands in
     // L2.)
-    if (FUSED && tid == p.TC && p.prefetch_x) bulk_prefetch_l2(p.x, 2u * p.K);
+    if (FUSED && tid == p.TC) bulk_prefetch_l2(p.x, 2u * p.K);
     pq2::pdl_wait();
     pq2::pdl_launch_dependents();
     if (rows <= 0) return;
@@ -637,9 +612,9 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
     // An L2 prefetch of it before the wait is only a hint (a write by that
     // kernel still lands in L2), and takes the round trip to HBM off the path
     // when x is final already.
-    if (tid == 32 && p.prefetch_x) bulk_prefetch_l2(p.x, 2u * p.K);
+    if (tid == 32) bulk_prefetch_l2(p.x, 2u * p.K);
     pq2::pdl_wait();
-    if (p.trigger == 0 || rows <= 0) pq2::pdl_launch_dependents();
+    pq2::pdl_launch_dependents();
     if (rows <= 0) return;
 
     const int lane = tid & 31;
@@ -670,7 +645,6 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
             const uint4 h[2] = {ld_cg_v4(src), ld_cg_v4(src + 8)};
             pq2::quantize_group8(h, j, valid, qslot, sslot, tslot);
         }
-        if (pass == 0 && p.trigger == 1) pq2::pdl_launch_dependents();
         __syncwarp();
         uint32_t q[32];
 #pragma unroll
@@ -722,7 +696,6 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
         }
         __syncwarp();  // the slot is rewritten by the next pass
     }
-    if (p.trigger == 2) pq2::pdl_launch_dependents();
     if (__syncthreads_or(failed)) {
         if (tid == 0) pq2::mbar_wait_bounded(wbar, 0, p.ctl);  // no copy in flight at exit
         return;
@@ -787,41 +760,13 @@ cudaError_t launch_gpt(const GemvParams& p, int grid, size_t smem, bool ws_smem,
     return launch_variant<GPT, false, false, false>(p, grid, smem, st);
 }
 
-// Tuning knobs (environment, read once): PQ2_GEMV_CTAS_PER_SM (default 1),
-// PQ2_GEMV_THREADS (consumer threads at most, default and cap 672 for one
-// group per thread), PQ2_GEMV_RING_KB (default 160), PQ2_GEMV_STAGE_KB (default 32:
-// measured on the lm_head shape, 248320 x 5120, 70.5 us per call at 16 KB stages,
-// 56.0 at 32 KB, 56.3 at 64 KB; 8 KB as 16),
-// PQ2_GEMV_PREFETCH (1 = on; 2 = off, default: with one CTA per SM the
-// prefetch only queues ahead of the ring copies), PQ2_GEMV_DIRECT (1 = the
-// direct variant where it applies, default; 2 = always the ring variant),
-// PQ2_GEMV_TRIGGER (staged variant: 1 = let the next kernel launch right
-// after the wait, default; 2 = after the activations are quantised; 3 =
-// after the dots), PQ2_GEMV_PREFETCH_X (fused paths: 1 = L2 prefetch of x
-// before the wait, default; 2 = none).  Compile-time: PQ2_GEMV_LOOKAHEAD
-// (direct variant, rows of loads in flight per thread, default 4).
-int env_int(const char* name, int dflt) {
-    const char* v = std::getenv(name);
-    if (!v || !*v) return dflt;
-    const int x = std::atoi(v);
-    return x > 0 ? x : dflt;
-}
-
-struct Tuning {
-    int ctas_per_sm, threads, ring_kb, stage_kb, prefetch, direct, trigger, prefetch_x;
-};
-
-const Tuning& tuning() {
-    static const Tuning t = {env_int("PQ2_GEMV_CTAS_PER_SM", 1),
-                             env_int("PQ2_GEMV_THREADS", kMaxConsumersSmall),
-                             env_int("PQ2_GEMV_RING_KB", 160),
-                             env_int("PQ2_GEMV_STAGE_KB", 32),
-                             env_int("PQ2_GEMV_PREFETCH", 2) == 1 ? 1 : 0,
-                             env_int("PQ2_GEMV_DIRECT", 1) == 1 ? 1 : 0,
-                             env_int("PQ2_GEMV_TRIGGER", 1) - 1,
-                             env_int("PQ2_GEMV_PREFETCH_X", 1) == 1 ? 1 : 0};
-    return t;
-}
+// Ring-variant sizing, fixed at build time.  The stage size was measured on
+// the lm_head shape (248320 x 5120): 70.5 us per call at 16 KB stages, 56.0
+// at 32 KB, 56.3 at 64 KB; 8 KB as 16.  One CTA per SM with up to 672
+// consumer threads (288 consumers measured 2058 GB/s against 2179 for 480 on
+// the decode shape).
+constexpr int kRingKB = 160;
+constexpr int kStageKB = 32;
 
 uint32_t align128(size_t v) { return static_cast<uint32_t>((v + 127) & ~static_cast<size_t>(127)); }
 
@@ -843,11 +788,26 @@ namespace pq2h {
 
 bool gemv_fused_supported(int64_t K) { return K <= kFusedMaxK; }
 
-cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const int32_t* T,
-                        const uint8_t* codes, const __half* ws, float* y, int32_t* dots, int64_t N,
-                        int64_t K, cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev,
-                        bool weights_static) {
-    const Tuning& tu = tuning();
+}  // namespace pq2h
+
+namespace {
+
+// The launch a call gets: kernel family, parameters, grid, block and
+// dynamic shared memory.
+enum class GemvKind { Staged, Direct, Ring };
+struct GemvPlan {
+    GemvKind kind;
+    GemvParams p;
+    int grid, threads, gpt;
+    size_t smem;
+    bool ws_smem;
+};
+
+cudaError_t plan_gemv(const __half* x, const int8_t* qp, const float* S, const int32_t* T,
+                      const uint8_t* codes, const __half* ws, float* y, int32_t* dots, int64_t N,
+                      int64_t K, const pq2::DevCtl& ctl, const pq2h::DeviceInfo& dev,
+                      bool weights_static, GemvPlan* plan) {
+    using pq2h::kUnsupportedVariant;
     GemvParams p = {};
     p.x = dots ? nullptr : x;
     if (p.x && K > kFusedMaxK) return cudaErrorInvalidValue;
@@ -863,26 +823,25 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const
     p.G = static_cast<int>(K / 128);
     const int gpt = p.G <= kMaxConsumersSmall ? 1 : (p.G <= 2 * kMaxConsumersLarge ? 2 : 4);
     p.GT = (p.G + gpt - 1) / gpt;
-    int max_tc = gpt == 1 ? kMaxConsumersSmall : kMaxConsumersLarge;
-    if (tu.threads >= 32 && tu.threads < max_tc) max_tc = tu.threads;
+    const int max_tc = gpt == 1 ? kMaxConsumersSmall : kMaxConsumersLarge;
     p.RP = max_tc / p.GT > 0 ? max_tc / p.GT : 1;
     p.TC = ((p.RP * p.GT + 31) / 32) * 32;
     p.codes_row_bytes = static_cast<uint32_t>(K / 4);
     const bool ws_smem = (dots == nullptr) && (p.G % 8 == 0);
     const int row_bytes = static_cast<int>(p.codes_row_bytes) + (ws_smem ? 2 * p.G : 0);
-    const int64_t slots = static_cast<int64_t>(dev.num_sms) * tu.ctas_per_sm;
+    const int64_t slots = dev.num_sms;
     const int rows_per_cta = static_cast<int>((N + slots - 1) / slots);
     p.rows_per_cta = rows_per_cta;
     // stage = RP*k rows of about stage_kb, not more than the CTA owns
     const int per_k = p.RP * row_bytes;
-    int k = (tu.stage_kb * 1024 + per_k / 2) / per_k;
+    int k = (kStageKB * 1024 + per_k / 2) / per_k;
     const int max_k = (rows_per_cta + p.RP - 1) / p.RP;
     if (k > max_k) k = max_k;
     if (k < 1) k = 1;
     p.R = p.RP * k;
     p.stage_bytes = static_cast<uint32_t>(((p.R * row_bytes) + 15) & ~15);
     const int cta_stages = (rows_per_cta + p.R - 1) / p.R;
-    int stages = tu.ring_kb * 1024 / static_cast<int>(p.stage_bytes);
+    int stages = kRingKB * 1024 / static_cast<int>(p.stage_bytes);
     if (stages > cta_stages) stages = cta_stages;
     p.stages = stages > 16 ? 16 : (stages < 2 ? 2 : stages);
     // row-sum chunk: ~12 KB of terms (at least one stage, at most the CTA's rows)
@@ -891,17 +850,26 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const
     p.chunk_stages = cs < 1 ? 1 : cs;
     const int grid = static_cast<int>((N + rows_per_cta - 1) / rows_per_cta);
     p.ctl = ctl;
-    p.prefetch = tu.prefetch;
-    p.trigger = tu.trigger;
-    p.prefetch_x = tu.prefetch_x;
-    // (the stage-withholding test hook needs the ring variant's waits)
-    if (weights_static && p.x && ctl.debug_skip_stage < 0) {
+    // Routing: the staged variant for static weights on the fused path, else
+    // the direct variant where its row sums fit, else the ring.  A variant
+    // forced by pq2_debug_force_kernel that cannot take the call gives
+    // kUnsupportedVariant; the stage-withholding test hook needs the ring
+    // variant's waits.
+    const int force = pq2h::forced_variant(PQ2_OP_GEMV);
+    const bool ring_only = ctl.debug_skip_stage >= 0 || force == PQ2_VARIANT_GEMV_RING;
+    if (ring_only && force != PQ2_VARIANT_DEFAULT && force != PQ2_VARIANT_GEMV_RING)
+        return kUnsupportedVariant;
+    if (force == PQ2_VARIANT_GEMV_STAGED ||
+        (force == PQ2_VARIANT_DEFAULT && weights_static && p.x && !ring_only)) {
         GemvParams sp = p;
-        const size_t ssmem = staged_layout(sp);
-        if (ssmem > 0 && ssmem <= static_cast<size_t>(dev.max_smem_optin))
-            return launch_staged(sp, grid, ssmem, st);
+        const size_t ssmem = p.x ? staged_layout(sp) : 0;
+        if (ssmem > 0 && ssmem <= static_cast<size_t>(dev.max_smem_optin)) {
+            *plan = {GemvKind::Staged, sp, grid, kStagedThreads, gpt, ssmem, ws_smem};
+            return cudaSuccess;
+        }
+        if (force == PQ2_VARIANT_GEMV_STAGED) return kUnsupportedVariant;
     }
-    if (gpt == 1 && tu.direct && ctl.debug_skip_stage < 0) {
+    if (gpt == 1 && !ring_only) {
         // direct variant: at most kDirectConsumers threads; shared memory is
         // barrier | activations (fused) | row-sum buffer for all of the CTA's
         // rows (the fused path stages x there first)
@@ -916,21 +884,68 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const
             if (d.x && red < 2 * static_cast<size_t>(d.K)) red = 2 * static_cast<size_t>(d.K);
             const size_t dsmem = d.red_off + red;
             if (dsmem <= kDirectMaxSmem && dsmem <= static_cast<size_t>(dev.max_smem_optin)) {
-                if (dots) return launch_direct<true, false>(d, grid, dsmem, st);
-                if (d.x) return launch_direct<false, true>(d, grid, dsmem, st);
-                return launch_direct<false, false>(d, grid, dsmem, st);
+                *plan = {GemvKind::Direct, d, grid, d.TC + 32, gpt, dsmem, ws_smem};
+                return cudaSuccess;
             }
         }
     }
+    if (force == PQ2_VARIANT_GEMV_DIRECT) return kUnsupportedVariant;
     size_t smem = layout(p);
     while (smem > static_cast<size_t>(dev.max_smem_optin) && p.stages > 2) {
         --p.stages;
         smem = layout(p);
     }
     if (smem > static_cast<size_t>(dev.max_smem_optin)) return cudaErrorInvalidConfiguration;
-    if (gpt == 1) return launch_gpt<1>(p, grid, smem, ws_smem, dots != nullptr, st);
-    if (gpt == 2) return launch_gpt<2>(p, grid, smem, ws_smem, dots != nullptr, st);
-    return launch_gpt<4>(p, grid, smem, ws_smem, dots != nullptr, st);
+    *plan = {GemvKind::Ring, p, grid, p.TC + 32, gpt, smem, ws_smem};
+    return cudaSuccess;
+}
+
+// An empty kernel for the launch-latency floor: the dependency wait and the
+// early launch of the next grid, nothing else.
+__global__ void gemv_floor_kernel() {
+    pq2::pdl_wait();
+    pq2::pdl_launch_dependents();
+}
+
+}  // namespace
+
+namespace pq2h {
+
+cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const int32_t* T,
+                        const uint8_t* codes, const __half* ws, float* y, int32_t* dots, int64_t N,
+                        int64_t K, cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev,
+                        bool weights_static) {
+    GemvPlan pl;
+    const cudaError_t e =
+        plan_gemv(x, qp, S, T, codes, ws, y, dots, N, K, ctl, dev, weights_static, &pl);
+    if (e != cudaSuccess) return e;
+    const bool d = dots != nullptr;
+    switch (pl.kind) {
+        case GemvKind::Staged: return launch_staged(pl.p, pl.grid, pl.smem, st);
+        case GemvKind::Direct:
+            if (d) return launch_direct<true, false>(pl.p, pl.grid, pl.smem, st);
+            if (pl.p.x) return launch_direct<false, true>(pl.p, pl.grid, pl.smem, st);
+            return launch_direct<false, false>(pl.p, pl.grid, pl.smem, st);
+        case GemvKind::Ring:
+            if (pl.gpt == 1) return launch_gpt<1>(pl.p, pl.grid, pl.smem, pl.ws_smem, d, st);
+            if (pl.gpt == 2) return launch_gpt<2>(pl.p, pl.grid, pl.smem, pl.ws_smem, d, st);
+            return launch_gpt<4>(pl.p, pl.grid, pl.smem, pl.ws_smem, d, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemv_floor(int64_t N, int64_t K, bool weights_static, cudaStream_t st,
+                              const pq2::DevCtl& ctl, const DeviceInfo& dev) {
+    // the plan of a fused call (no pointer is dereferenced: nothing runs)
+    const __half* x = reinterpret_cast<const __half*>(static_cast<uintptr_t>(256));
+    GemvPlan pl;
+    const cudaError_t e = plan_gemv(x, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                    nullptr, N, K, ctl, dev, weights_static, &pl);
+    if (e != cudaSuccess) return e;
+    static SmemLimit lim;
+    const cudaError_t a = ensure_smem(lim, gemv_floor_kernel, pl.smem);
+    if (a != cudaSuccess) return a;
+    return launch(gemv_floor_kernel, dim3(pl.grid), dim3(pl.threads), pl.smem, st, true);
 }
 
 }  // namespace pq2h

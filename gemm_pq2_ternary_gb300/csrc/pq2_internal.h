@@ -8,9 +8,16 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "../../include/pq2.h"
 #include "pq2_common.cuh"
 
 namespace pq2h {
+
+// The variant pq2_debug_force_kernel set for `op` (PQ2_VARIANT_DEFAULT when
+// none).  A launcher asked for a variant that cannot take the call returns
+// kUnsupportedVariant, which the C ABI reports as PQ2_ERR_UNSUPPORTED_SHAPE.
+int forced_variant(int op);
+constexpr cudaError_t kUnsupportedVariant = cudaErrorNotSupported;
 
 // 2-D tiled tensor map (zero fill out of range): dims {inner, outer}
 // elements, row pitch in bytes, box {box_inner, box_outer}; swizzle128 =
@@ -49,6 +56,11 @@ cudaError_t launch_gemv(const __half* x, const int8_t* qp, const float* S, const
                         const uint8_t* codes, const __half* ws, float* y, int32_t* dots, int64_t N,
                         int64_t K, cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev,
                         bool weights_static = false);
+
+// An empty kernel (dependency wait, early launch of the next grid) with the
+// grid, block and shared memory a fused M == 1 call of this shape gets.
+cudaError_t launch_gemv_floor(int64_t N, int64_t K, bool weights_static, cudaStream_t st,
+                              const pq2::DevCtl& ctl, const DeviceInfo& dev);
 
 // 2 <= M <= 16: tcgen05 kernel with the weights expanded into tensor memory,
 // split-K partial sums reduced in a fixed order.

@@ -17,7 +17,6 @@
 // are summed in the fixed order of the M = 1 kernels (8 lanes over a stride,
 // then a 3-step butterfly), so each token's y equals pq2_gemv on that token
 // bit for bit.
-#include <cstdlib>
 
 #include "pq2_internal.h"
 
@@ -176,23 +175,20 @@ int tokens_per_pass(int64_t M) { return M <= 2 ? 2 : (M <= 4 ? 4 : 8); }
 
 namespace pq2h {
 
-// PQ2_SMALL_DP4A_MAX_M (environment, read once; tuning): the most tokens
-// this kernel takes, at most 8 (1 turns it off).  Default 4: measured on
-// GB300 against the tensor-core small-batch kernel, GB/s, 6144 -> 5120 and
+// The most tokens this kernel takes by default: 4.  Measured on GB300
+// against the tensor-core small-batch kernel, GB/s, 6144 -> 5120 and
 // 5120 -> 17408: M = 2 1056 / 1900 against 537 / 1049; M = 4 774 / 1256
 // against 519 / 1028; M = 8 523 / 624 against 501 / 1003 (at 8 tokens the
-// DP4A work per code word outweighs the shared loads).
-int multi_max_m() {
-    static const int v = [] {
-        const char* e = std::getenv("PQ2_SMALL_DP4A_MAX_M");
-        const int x = (e && *e) ? std::atoi(e) : 0;
-        return x >= 1 ? (x > 8 ? 8 : x) : 4;
-    }();
-    return v;
-}
+// DP4A work per code word outweighs the shared loads).  Forcing the variant
+// (pq2_debug_force_kernel) extends the range to 8 tokens.
+constexpr int kMultiDefaultMaxM = 4;
+constexpr int kMultiMaxM = 8;
 
 bool gemv_multi_supported(int64_t M, int64_t N, int64_t K, int num_sms) {
-    if (M < 2 || M > multi_max_m()) return false;
+    const int force = forced_variant(PQ2_OP_SMALL);
+    if (force != PQ2_VARIANT_DEFAULT && force != PQ2_VARIANT_SMALL_DP4A) return false;
+    const int max_m = force == PQ2_VARIANT_SMALL_DP4A ? kMultiMaxM : kMultiDefaultMaxM;
+    if (M < 2 || M > max_m) return false;
     const int mt = tokens_per_pass(M);
     const int64_t G = K / 128;
     if (G * mt > kMultiConsumers) return false;

@@ -61,6 +61,11 @@ pq2_status pq2_gemm_small_noalloc(const int8_t* qp, const float* S, const int32_
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (!a16(qp) || !a16(S) || !a16(T) || !a16(codes) || !a16(ws_f16) || !a16(y))
         return PQ2_ERR_MISALIGNED;
+    // Beyond 8 tokens only the tensor-core kernel can take the call, and its
+    // scratch grows with the number of 128-row tiles: a shape that does not
+    // fit even with a single CTA is refused before the device is touched
+    // (e.g. N = 248320 at 16 tokens needs about 16 MB).
+    if (M > 8 && pq2h::small_scratch_bytes(M, N, K, 1) > kScratchBytes) return PQ2_ERR_WORKSPACE;
     pq2h::DeviceInfo dev;
     pq2::DevCtl ctl;
     if (!pq2h::device_info(&dev) || !pq2h::make_ctl(&ctl)) return PQ2_ERR_CUDA;

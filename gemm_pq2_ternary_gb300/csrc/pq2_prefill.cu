@@ -46,8 +46,6 @@
 // from weights expanded once per call by the preparation kernel; it is the
 // default from 8 token tiles on, once its tiles fill every SM.
 // Every mbarrier wait is bounded (device error word on expiry).
-#include <cstdlib>
-
 #include "pq2_internal.h"
 
 namespace {
@@ -443,6 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     failed = true;
                     *abort_v = 1;
                 }
+                // warp-uniform from here: the tensor-memory loads below are
+                // executed by all 32 lanes or none
+                failed = __any_sync(0xffffffffu, failed);
                 if (!failed) {
                     tc_fence_after();
                     // the 64 weight scales of this thread's columns: 16-byte
@@ -569,6 +570,7 @@ struct PrefillWideParams {
     const float2* st;      // [G][M] (s, t)
     const float* wst;      // [G][Npad] weight scales, zero past N
     float* y;              // [M][N]
+    int32_t* dots;         // debug: [M][N][G]
     int M, N, K, G, Npad;
     int m_tiles, n_tiles;
     pq2::DevCtl ctl;
@@ -581,6 +583,7 @@ __device__ __forceinline__ void mma_f8_wide(uint32_t d_tmem, uint64_t a, uint64_
         "l"(a), "l"(b), "r"(kWIdesc), "r"(acc));
 }
 
+template <bool DOTS>
 __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid_constant__ PrefillWideParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint64_t full[kWStages];    // TMA bytes of a stage landed
@@ -766,6 +769,17 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
                             __syncwarp();
                             if (lane == 0) pq2::mbar_arrive(&dempty[db]);
                         }
+                        if (DOTS) {
+#pragma unroll
+                            for (int j = 0; j < 64; ++j) {
+                                const float dot = fmaf(d[j], 512.0f, -stv.y);  // exact integer
+                                const int n = nt * kWTileN + col0 + c + j;
+                                if (mvalid && n < p.N)
+                                    p.dots[(static_cast<size_t>(m) * p.N + n) * G + g] =
+                                        static_cast<int>(dot);
+                            }
+                            continue;
+                        }
 #pragma unroll
                         for (int j = 0; j < 64; j += 2) {
                             // exact integer dots of two columns, then the scales;
@@ -789,7 +803,7 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
                 stv = st_next;
             }
             // tile done: acc -> y
-            if (!failed && mvalid) {
+            if (!DOTS && !failed && mvalid) {
                 const int nb = nt * kWTileN + col0;
                 float* yrow = p.y + static_cast<size_t>(m) * p.N + nb;
                 if (nb + 128 <= p.N && (p.N & 3) == 0) {
@@ -824,24 +838,14 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
 
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
-// PQ2_PREFILL_WIDE (environment, read once): 1 = the 128 x 256 kernel
-// whenever it applies, 2 = never, unset = by tile count.
-int prefill_wide_mode() {
-    static const int mode = [] {
-        const char* v = std::getenv("PQ2_PREFILL_WIDE");
-        const int x = (v && *v) ? std::atoi(v) : 0;
-        return (x == 1 || x == 2) ? x : 0;
-    }();
-    return mode;
-}
-
 // setmaxnreg.inc draws on the registers the block was launched with: the
 // wide kernel runs only if its compiled allocation covers the split (else
 // the raising warps would wait forever).
+template <bool DOTS>
 bool wide_kernel_fits() {
     static const bool ok = [] {
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, prefill_wide_kernel) != cudaSuccess) return false;
+        if (cudaFuncGetAttributes(&fa, prefill_wide_kernel<DOTS>) != cudaSuccess) return false;
         return fa.numRegs * kWThreads >= kWRegsNeeded;
     }();
     return ok;
@@ -854,8 +858,9 @@ bool wide_kernel_fits() {
 // bytes once per call: measured at N = 17408, M = 512 it only ties the
 // 128 x 128 kernel, 662 against 659 TOPS, and M = 1024 gains 778 against
 // 685) and at least kWideMinTiles tiles, a bound below the SM count of the
-// GPUs this library is built for; PQ2_PREFILL_WIDE=1 forces it.  The size
-// depends on the shape only, not on the device.
+// GPUs this library is built for; forcing the variant
+// (pq2_debug_force_kernel) gives it room at any shape.  The size depends on
+// the shape (and the forced variant) only, not on the device.
 constexpr int kWideMinTiles = 128;
 constexpr int kWideMinMTiles = 8;
 struct WsLayout {
@@ -868,9 +873,10 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
     const int64_t G = K / 128;
     const int64_t m_tiles = (M + kTileM - 1) / kTileM;
     const int64_t wide_tiles = m_tiles * ((N + kWTileN - 1) / kWTileN);
-    const int mode = prefill_wide_mode();
-    const bool room =
-        mode == 1 || (mode != 2 && m_tiles >= kWideMinMTiles && wide_tiles >= kWideMinTiles);
+    const int force = pq2h::forced_variant(PQ2_OP_PREFILL);
+    const bool room = force == PQ2_VARIANT_PREFILL_WIDE ||
+                      (force == PQ2_VARIANT_DEFAULT && m_tiles >= kWideMinMTiles &&
+                       wide_tiles >= kWideMinTiles);
     l.npad = (N + kWTileN - 1) / kWTileN * kWTileN;
     size_t off = 0;
     l.ahi = off;
@@ -913,10 +919,14 @@ cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, c
     const int wide_tiles = m_tiles * static_cast<int>((N + kWTileN - 1) / kWTileN);
     // The wide tiles (128 x 256) where the workspace has room for the
     // expanded weights (ws_layout) and the tiles fill every SM at least once
-    // (below one wave the wide tiles leave SMs idle); the debug integer-dot
-    // output always takes the 128 x 128 kernel.
-    const bool wide = !dots && l.wexp_bytes > 0 && wide_kernel_fits() &&
-                      (prefill_wide_mode() == 1 || wide_tiles >= dev.num_sms);
+    // (below one wave the wide tiles leave SMs idle).  The integer-dot debug
+    // output takes the same kernel as y.
+    const int force = forced_variant(PQ2_OP_PREFILL);
+    const bool fits = dots ? wide_kernel_fits<true>() : wide_kernel_fits<false>();
+    const bool wide = l.wexp_bytes > 0 && fits &&
+                      (force == PQ2_VARIANT_PREFILL_WIDE ||
+                       (force == PQ2_VARIANT_DEFAULT && wide_tiles >= dev.num_sms));
+    if (force == PQ2_VARIANT_PREFILL_WIDE && !wide) return kUnsupportedVariant;
     uint8_t* wexp = wide ? w + l.wexp : nullptr;
     float* wst = wide ? reinterpret_cast<float*>(w + l.wst) : nullptr;
     {
@@ -940,6 +950,7 @@ cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, c
         p.st = stv;
         p.wst = wst;
         p.y = y;
+        p.dots = dots;
         p.M = static_cast<int>(M);
         p.N = static_cast<int>(N);
         p.K = static_cast<int>(K);
@@ -950,10 +961,11 @@ cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, c
         p.ctl = ctl;
         const int grid = wide_tiles < dev.num_sms ? wide_tiles : dev.num_sms;
         const size_t smem = 1024 + static_cast<size_t>(kWStages) * kWStageBytes;
-        static SmemLimit lim_wide;
-        cudaError_t e = ensure_smem(lim_wide, prefill_wide_kernel, smem);
+        auto kern = dots ? prefill_wide_kernel<true> : prefill_wide_kernel<false>;
+        static SmemLimit lim_wide[2];
+        cudaError_t e = ensure_smem(lim_wide[dots ? 1 : 0], kern, smem);
         if (e != cudaSuccess) return e;
-        return launch(prefill_wide_kernel, dim3(grid), dim3(kWThreads), smem, st, true, p);
+        return launch(kern, dim3(grid), dim3(kWThreads), smem, st, true, p);
     }
     PrefillParams p = {};
     if (!encode_tmap_2d(&p.tm_ahi, CU_TENSOR_MAP_DATA_TYPE_UINT8, ahi, static_cast<uint64_t>(K),

@@ -689,6 +689,8 @@ cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, con
                          int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                          const DeviceInfo& dev) {
     if (M < 1 || M > kTok) return cudaErrorInvalidValue;
+    // (the DP4A kernel, when forced, takes every shape it can; this is not one)
+    if (forced_variant(PQ2_OP_SMALL) == PQ2_VARIANT_SMALL_DP4A) return kUnsupportedVariant;
     const SmallLayout l = layout_small(M, N, K, dev.num_sms);
     uint8_t* w = static_cast<uint8_t*>(workspace);
     uint32_t* tok = reinterpret_cast<uint32_t*>(w + l.tok);

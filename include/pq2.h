@@ -299,6 +299,12 @@ pq2_status pq2_last_device_error(void* stream);
  *   Same operands as pq2_gemm_small, no workspace.  Returns
  *   PQ2_ERR_WORKSPACE if the shape needs more than
  *   pq2_gemm_small_noalloc_max_scratch() bytes of scratch on this device.
+ *   For the tensor-core kernel (5 or more tokens) the scratch is about
+ *   (min(SMs, 256) + ceil(N/128)) * M * 512 bytes of partial sums plus
+ *   ceil(K/512) * 16 KB of token tiles: on a 152-SM GPU, 16 tokens fit up
+ *   to about N = 40,000 at K = 5120, and an lm_head-scale N = 248,320 gets
+ *   PQ2_ERR_WORKSPACE.  2 to 4 tokens, where the DP4A kernel takes them,
+ *   need no scratch.
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) and should come before any stream capture.
  *   All calls share the array: calls that may run at the same time on the
@@ -311,6 +317,42 @@ pq2_status pq2_gemm_small_noalloc(const int8_t* qp, const float* S, const int32_
 
 /* Size in bytes of the fixed scratch array behind pq2_gemm_small_noalloc. */
 size_t pq2_gemm_small_noalloc_max_scratch(void);
+
+/* Kernel variants for pq2_debug_force_kernel. */
+#define PQ2_VARIANT_DEFAULT 0        /* the library's own routing                  */
+#define PQ2_VARIANT_GEMV_DIRECT 1    /* M = 1: look-ahead loads into registers      */
+#define PQ2_VARIANT_GEMV_RING 2      /* M = 1: bulk-copy ring in shared memory      */
+#define PQ2_VARIANT_GEMV_STAGED 3    /* M = 1 fused: whole slice staged before wait */
+#define PQ2_VARIANT_SMALL_DP4A 1     /* 2..8 tokens: DP4A, code words shared        */
+#define PQ2_VARIANT_SMALL_TC 2       /* tcgen05, weights in tensor memory           */
+#define PQ2_VARIANT_PREFILL_128 1    /* tcgen05 128 x 128 tiles, in-kernel expansion */
+#define PQ2_VARIANT_PREFILL_WIDE 2   /* tcgen05 128 x 256 tiles, pre-expanded weights */
+
+/*
+ * pq2_debug_force_kernel -- test hook: from now on, calls of `op`
+ * (PQ2_OP_GEMV, PQ2_OP_SMALL or PQ2_OP_PREFILL; pq2_matmul, pq2_group_dots
+ * and pq2_mlp_down_swiglu route through them) run kernel `variant` of that op
+ * (PQ2_VARIANT_*), or follow the library's own routing again with
+ * PQ2_VARIANT_DEFAULT.  Every variant computes the same integer group dots
+ * and the same y, bit for bit; the hook exists so that tests can check each
+ * kernel on shapes the routing would give to another.  A call whose shape
+ * the forced variant cannot take returns PQ2_ERR_UNSUPPORTED_SHAPE.
+ * pq2_workspace_bytes accounts for the forced variant, so set it before
+ * sizing a workspace.  Process-wide; not for use while other threads call
+ * the library.  PQ2_ERR_INVALID_ARG for an unknown op or variant.
+ */
+pq2_status pq2_debug_force_kernel(int op, int variant);
+
+/*
+ * pq2_debug_gemv_floor -- measurement hook: enqueues one launch of an empty
+ * kernel (it waits for the preceding kernel on the stream and lets the next
+ * one start launching, nothing else) with the grid, block and shared memory
+ * that pq2_matmul_ex(M = 1, N, K, flags) gets.  A chain of these times the
+ * launch and dependency latency a chain of real calls pays before any byte
+ * moves: the floor of a dependent sequence of M = 1 calls.  No pointer is
+ * passed and nothing is written.  Errors as pq2_matmul_ex (shape, flags).
+ */
+pq2_status pq2_debug_gemv_floor(int64_t N, int64_t K, uint32_t flags, void* stream);
 
 /*
  * pq2_debug_set_wait_limit_ns -- bound on every on-chip barrier wait, in

@@ -186,3 +186,33 @@ def test_bf16_binding_checks_dtype_and_shapes(lib):
         b.pq2_gemm_bf16_splitk(x.bfloat16(), w, torch.zeros((2, 9), dtype=torch.bfloat16))
     with pytest.raises(ValueError, match="CUDA"):   # host tensors never reach the library
         b.pq2_gemm_bf16_splitk(x.bfloat16(), w, y)
+
+
+def test_noalloc_refuses_shapes_beyond_its_scratch(lib):
+    # 16 tokens at lm_head scale (N = 248320, K = 5120): the split-K partial
+    # sums alone need about 16 MB, more than the fixed array holds; the call
+    # is refused on the host, before any CUDA call
+    from gemm_pq2_ternary_gb300 import binding as b
+    P = _p(FAKE)
+    assert b.pq2_gemm_small_noalloc_max_scratch() == 4 << 20
+    st = lib.pq2_gemm_small_noalloc(P, P, P, P, P, P, 16, 248320, 5120, None)
+    assert st == b.PQ2_ERR_WORKSPACE
+    st = lib.pq2_gemm_small_noalloc(P, P, P, P, P, P, 17, 5120, 5120, None)
+    assert st == b.PQ2_ERR_UNSUPPORTED_SHAPE
+
+
+def test_force_kernel_checks_its_arguments(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    f = lib.pq2_debug_force_kernel
+    assert f(b.PQ2_OP_MATMUL, 1) == b.PQ2_ERR_INVALID_ARG      # not a kernel family
+    assert f(b.PQ2_OP_SMALL, 7) == b.PQ2_ERR_INVALID_ARG
+    assert f(b.PQ2_OP_PREFILL, -1) == b.PQ2_ERR_INVALID_ARG
+    K, N = 5120, 17408
+    default = b.pq2_workspace_bytes(b.PQ2_OP_PREFILL, 128, N, K)
+    try:
+        # the 128 x 256 kernel, forced, needs room for the expanded weights
+        assert f(b.PQ2_OP_PREFILL, b.PQ2_VARIANT_PREFILL_WIDE) == b.PQ2_OK
+        assert b.pq2_workspace_bytes(b.PQ2_OP_PREFILL, 128, N, K) >= default + N * K
+    finally:
+        assert f(b.PQ2_OP_PREFILL, b.PQ2_VARIANT_DEFAULT) == b.PQ2_OK
+    assert b.pq2_workspace_bytes(b.PQ2_OP_PREFILL, 128, N, K) == default

@@ -63,3 +63,37 @@ def test_oracle_single_core_sample_and_thread_independence():
         oracle.set_threads(before)
     yn, _ = oracle.matmul(qp, S, codes, ws)
     assert np.array_equal(y1, yn)
+
+
+def test_every_suite_configuration_has_a_workload():
+    names = set()
+    for (w, m, shape) in bench.SUITE:
+        name, layer, kind = bench.workload_spec(_args(w, m, shape or "5120,17408"))
+        assert bench.per_layer_units(layer, kind, name) > 0
+        assert bench.layer_launches(layer, name) >= 1
+        names.add(name)
+    assert len(names) == len(bench.SUITE)
+    # the five configurations the benchmark is quoted on are all there
+    for want in ["pr1_gemv_m1_k1024_n256", "small_m16_k5120_n17408", "small_m2_k6144_n5120",
+                 "mlp_pair_m1", "mlp_pair_m16", "prefill_m128_k5120_n17408",
+                 "prefill_m4096_k5120_n17408"]:
+        assert want in names
+
+
+def test_accuracy_measures():
+    import numpy as np
+
+    import oracle
+    from gemm_pq2_ternary_gb300 import inputs
+    tern, ws, x = inputs.generate(inputs.Problem("acc", 4, 512, 64, "p343", "outliers", 3))
+    qp, S, _ = oracle.quantize_act(x)
+    ref, A = oracle.matmul(qp, S, oracle.pack(tern), ws)
+    sample = dict(bf16=False, K=512, tern=tern, ws=ws, x=x, y=ref.astype(np.float32))
+    got = bench.accuracy(sample)
+    assert got["within_tolerance"] and got["rel_rms"] < 1e-7 and got["outputs"] == 4 * 64
+    # a 1% error on one output shows in both measures and fails the bound
+    bad = ref.astype(np.float32).copy()
+    i = np.unravel_index(np.argmax(np.abs(ref)), ref.shape)
+    bad[i] *= 1.01
+    got = bench.accuracy(dict(sample, y=bad))
+    assert not got["within_tolerance"] and got["max_rel_err"] > 0.009 and got["rel_rms"] > 1e-4

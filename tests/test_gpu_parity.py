@@ -311,3 +311,36 @@ def test_bounded_wait_reports_timeout(pq2):
         pq2.pq2_debug_set_wait_limit_ns(2_000_000_000)
     pq2.pq2_gemv(c.qp_d, c.S_d, c.T_d, c.codes_d, c.ws_d, y)
     _check_full(pq2, c, y)
+
+
+@pytest.mark.parametrize("op,variant,prob", [
+    ("small", "tc", inputs.Problem("timeout_small", 8, 1280, 640, "p343", "outliers", 51)),
+    ("prefill", "128", inputs.Problem("timeout_pf128", 37, 384, 200, "uniform", "normal", 52)),
+    ("prefill", "wide", inputs.Problem("timeout_pfwide", 37, 384, 200, "uniform", "normal", 53)),
+], ids=["small_kernel", "prefill_kernel", "prefill_wide_kernel"])
+def test_tensor_core_pipelines_report_timeout(pq2, op, variant, prob):
+    # As above for the tcgen05 pipelines: the producer of each CTA withholds
+    # its first stage; the MMA issuers and the other roles give up after the
+    # limit, the producer waits for the copies it did issue, every role
+    # reaches the teardown (tensor memory freed), and the host reads
+    # PQ2_ERR_TIMEOUT.  The next normal call is correct.
+    from gemm_pq2_ternary_gb300.binding import alloc_workspace
+    opc = pq2.PQ2_OP_SMALL if op == "small" else pq2.PQ2_OP_PREFILL
+    var = {"tc": pq2.PQ2_VARIANT_SMALL_TC, "128": pq2.PQ2_VARIANT_PREFILL_128,
+           "wide": pq2.PQ2_VARIANT_PREFILL_WIDE}[variant]
+    fn = pq2.pq2_gemm_small if op == "small" else pq2.pq2_gemm_prefill
+    c = Case(pq2, prob)
+    y = torch.empty((prob.M, prob.N), device=DEV)
+    with pq2.forced_kernel(opc, var):
+        wsp = alloc_workspace(opc, prob.M, prob.N, prob.K)
+        try:
+            pq2.pq2_debug_set_wait_limit_ns(20_000_000)
+            pq2.pq2_debug_skip_stage(0)
+            fn(c.qp_d, c.S_d, c.T_d, c.codes_d, c.ws_d, y, wsp)
+            assert pq2.pq2_last_device_error() == pq2.PQ2_ERR_TIMEOUT
+        finally:
+            pq2.pq2_debug_skip_stage(-1)
+            pq2.pq2_debug_set_wait_limit_ns(2_000_000_000)
+        y = torch.full((prob.M, prob.N), float("nan"), device=DEV)
+        fn(c.qp_d, c.S_d, c.T_d, c.codes_d, c.ws_d, y, wsp)
+    _check_full(pq2, c, y)
