@@ -575,6 +575,28 @@ __device__ __forceinline__ uint4 ld_cg_v4(const void* ptr) {
     return v;
 }
 
+// group_codes_dot64 of two code rows against the same activations, the two
+// rows' DP4A chains interleaved (eight independent accumulators).
+__device__ __forceinline__ void group_codes_dot64_x2(const uint32_t (&w0)[8], const uint32_t (&w1)[8],
+                                                     const uint32_t (&q)[32], int bias64, int& r0,
+                                                     int& r1) {
+    int a0 = 0, a1 = 0, a2 = 0, a3 = bias64;
+    int b0 = 0, b1 = 0, b2 = 0, b3 = bias64;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        a0 = pq2::dp4a_us(w0[j] & 0x03030303u, q[0 * 8 + j], a0);
+        b0 = pq2::dp4a_us(w1[j] & 0x03030303u, q[0 * 8 + j], b0);
+        a1 = pq2::dp4a_us(w0[j] & 0x0C0C0C0Cu, q[1 * 8 + j], a1);
+        b1 = pq2::dp4a_us(w1[j] & 0x0C0C0C0Cu, q[1 * 8 + j], b1);
+        a2 = pq2::dp4a_us(w0[j] & 0x30303030u, q[2 * 8 + j], a2);
+        b2 = pq2::dp4a_us(w1[j] & 0x30303030u, q[2 * 8 + j], b2);
+        a3 = pq2::dp4a_us(w0[j] & 0xC0C0C0C0u, q[3 * 8 + j], a3);
+        b3 = pq2::dp4a_us(w1[j] & 0xC0C0C0C0u, q[3 * 8 + j], b3);
+    }
+    r0 = ((a0 * 4 + a1) * 4 + a2) * 4 + a3;
+    r1 = ((b0 * 4 + b1) * 4 + b2) * 4 + b3;
+}
+
 __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* wbar = reinterpret_cast<uint64_t*>(smem);  // the weight slice has landed
@@ -635,6 +657,7 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
     const uint32_t codes_s = pq2::smem_u32(smem + p.ring_off);
     const uint32_t ws_s = pq2::smem_u32(smem + p.ws_off);
     const uint32_t red_s = pq2::smem_u32(smem + p.red_off);
+    const int rstr = p.G + 1;  // words between rows of terms (conflict-free stores)
     const int passes = (p.G + gstep - 1) / gstep;  // uniform over the CTA
     for (int pass = 0; pass < passes; ++pass) {
         const int g = gslot + pass * gstep;
@@ -666,33 +689,33 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
         const uint32_t cstep = lstep * rs;
         const uint32_t wsa = ws_s + 2u * (li * p.G + gl);
         const uint32_t wstep = 2u * lstep * p.G;
-        // rows li, li + lstep, ...: the next row's codes and scale are requested
-        // before this row's dot
-        uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
-        uint32_t wv = 0;
-        if (nk > 0) {
-            c0 = pq2::lds_v4(cs);
-            c1 = pq2::lds_v4(cs + 16);
-            wv = pq2::lds_u16(wsa);
-        }
-        for (int k = 0; k < nk; ++k) {
-            uint4 n0 = c0, n1 = c1;
-            uint32_t nw = wv;
-            if (k + 1 < nk) {
-                const uint32_t a = cs + (k + 1) * cstep;
-                n0 = pq2::lds_v4(a);
-                n1 = pq2::lds_v4(a + 16);
-                nw = pq2::lds_u16(wsa + (k + 1) * wstep);
+        // rows li, li + lstep, ... two at a time: the two rows' DP4A chains
+        // are independent, which keeps the ALU busy with few warps per
+        // scheduler (the second row of a lane's last pair may be absent)
+        for (int k = 0; k < nk; k += 2) {
+            const bool two = k + 1 < nk;
+            const uint32_t a = cs + k * cstep;
+            const uint4 c0 = pq2::lds_v4(a), c1 = pq2::lds_v4(a + 16);
+            const uint32_t wv0 = pq2::lds_u16(wsa + k * wstep);
+            uint4 d0 = make_uint4(0u, 0u, 0u, 0u), d1 = d0;
+            uint32_t wv1 = 0;
+            if (two) {
+                d0 = pq2::lds_v4(a + cstep);
+                d1 = pq2::lds_v4(a + cstep + 16);
+                wv1 = pq2::lds_u16(wsa + (k + 1) * wstep);
             }
-            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            const int dot64 = pq2::group_codes_dot64(w, q, t64);
+            const uint32_t w0[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            const uint32_t w1[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+            int dot0, dot1;
+            group_codes_dot64_x2(w0, w1, q, t64, dot0, dot1);
             // float(dot64) exactly (|dot64| < 2^22) by the 1.5 * 2^23 bit trick
-            const float dotf = __fsub_rn(__int_as_float(0x4B400000 + dot64), 12582912.0f);
-            const float wsf = __half2float(__ushort_as_half(static_cast<unsigned short>(wv)));
-            pq2::sts_f32(red_s + 4u * ((li + k * lstep) * p.G + g), dotf * s64 * wsf);
-            c0 = n0;
-            c1 = n1;
-            wv = nw;
+            const float f0 = __fsub_rn(__int_as_float(0x4B400000 + dot0), 12582912.0f);
+            const float f1 = __fsub_rn(__int_as_float(0x4B400000 + dot1), 12582912.0f);
+            const float ws0 = __half2float(__ushort_as_half(static_cast<unsigned short>(wv0)));
+            const float ws1 = __half2float(__ushort_as_half(static_cast<unsigned short>(wv1)));
+            const int row = li + k * lstep;
+            pq2::sts_f32(red_s + 4u * (row * rstr + g), f0 * s64 * ws0);
+            if (two) pq2::sts_f32(red_s + 4u * ((row + lstep) * rstr + g), f1 * s64 * ws1);
         }
         __syncwarp();  // the slot is rewritten by the next pass
     }
@@ -708,7 +731,7 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
         const int r = rb + (lane >> 3);
         float sum = 0.0f;
         if (r < rows)
-            for (int c = sub; c < p.G; c += 8) sum += pq2::lds_f32(red_s + 4u * (r * p.G + c));
+            for (int c = sub; c < p.G; c += 8) sum += pq2::lds_f32(red_s + 4u * (r * rstr + c));
         sum += __shfl_xor_sync(0xffffffffu, sum, 4);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
@@ -727,7 +750,7 @@ size_t staged_layout(GemvParams& p) {
     p.act_off = static_cast<uint32_t>((p.ws_off + wsz + 127) & ~static_cast<size_t>(127));
     const size_t act = static_cast<size_t>(kQStride + 8) * kStagedTeams;
     p.red_off = static_cast<uint32_t>((p.act_off + act + 127) & ~static_cast<size_t>(127));
-    const size_t total = p.red_off + rows * p.G * 4;
+    const size_t total = p.red_off + rows * (p.G + 1) * 4;
     if (rows * p.codes_row_bytes < kStagedMinSlice) return 0;
     return total <= kStagedMaxSmem ? total : 0;
 }
