@@ -165,8 +165,8 @@ pq2_status pq2_debug_skip_stage(int stage) {
 pq2_status pq2_debug_force_kernel(int op, int variant) {
     int max_variant = -1;
     if (op == PQ2_OP_GEMV) max_variant = PQ2_VARIANT_GEMV_STAGED;
-    if (op == PQ2_OP_SMALL) max_variant = PQ2_VARIANT_SMALL_TC;
-    if (op == PQ2_OP_PREFILL) max_variant = PQ2_VARIANT_PREFILL_WIDE;
+    if (op == PQ2_OP_SMALL) max_variant = PQ2_VARIANT_SMALL_TILE;
+    if (op == PQ2_OP_PREFILL) max_variant = PQ2_VARIANT_PREFILL_TILE;
     if (variant < 0 || variant > max_variant) return PQ2_ERR_INVALID_ARG;
     g_force[op].store(variant);
     return PQ2_OK;
@@ -270,7 +270,7 @@ size_t pq2_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
     switch (op) {
         case PQ2_OP_GEMV: return M == 1 ? 0 : SIZE_MAX;
         case PQ2_OP_SMALL:
-            return (M >= 2 && M <= 16) ? pq2h::small_workspace_bytes(M, N, K) : SIZE_MAX;
+            return (M >= 2 && M <= 16) ? pq2h::small_tc_workspace_bytes(M, N, K) : SIZE_MAX;
         case PQ2_OP_PREFILL: return pq2h::prefill_workspace_bytes(M, N, K);
         case PQ2_OP_SWIGLU_DOWN:  // K is the intermediate size I
         case PQ2_OP_MATMUL: {
@@ -305,7 +305,7 @@ pq2_status pq2_gemm_small(const int8_t* qp, const float* S, const int32_t* T,
                                                    static_cast<const __half*>(ws_f16), y, nullptr,
                                                    M, N, K, static_cast<cudaStream_t>(stream),
                                                    c.dev));
-    return cuda_status(pq2h::launch_small(qp, S, T, codes, static_cast<const __half*>(ws_f16), y,
+    return cuda_status(pq2h::launch_small_tc(qp, S, T, codes, static_cast<const __half*>(ws_f16), y,
                                           nullptr, M, N, K, workspace,
                                           static_cast<cudaStream_t>(stream), c.ctl, c.dev));
 }
@@ -446,7 +446,7 @@ pq2_status pq2_group_dots(int op, const int8_t* qp, const int32_t* T, const uint
         if (pq2h::gemv_multi_supported(M, N, K, c.dev.num_sms))
             return cuda_status(pq2h::launch_gemv_multi(qp, nullptr, T, codes, nullptr, nullptr,
                                                        dots, M, N, K, st, c.dev));
-        return cuda_status(pq2h::launch_small(qp, nullptr, T, codes, nullptr, nullptr, dots, M, N,
+        return cuda_status(pq2h::launch_small_tc(qp, nullptr, T, codes, nullptr, nullptr, dots, M, N,
                                               K, workspace, st, c.ctl, c.dev));
     }
     // the prefill path needs S only to prepare its token planes

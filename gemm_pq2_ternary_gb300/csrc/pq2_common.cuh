@@ -146,6 +146,37 @@ __device__ __forceinline__ bool mbar_spin_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// Same bound, waiting in try_wait alone: the thread is suspended in hardware
+// until the phase completes (or a system-dependent time passes), so a
+// waiting warp takes no issue slots from the warps that do the work -- with
+// several roles per SM sub-partition, polling warps slow the working ones
+// down severalfold.
+__device__ __forceinline__ bool mbar_suspend_bounded(uint64_t* bar, uint32_t parity,
+                                                     const DevCtl& ctl,
+                                                     volatile int* abort_flag = nullptr) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (globaltimer_ns() - t0 > ctl.wait_limit_ns) {
+            atomicOr(ctl.err, DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Warp-wide suspending wait (lane 0 waits in try_wait, the warp then
+// synchronises).  All 32 lanes must call it; the result is warp-uniform.
+__device__ __forceinline__ bool mbar_suspend_warp(uint64_t* bar, uint32_t parity,
+                                                  const DevCtl& ctl,
+                                                  volatile int* abort_flag = nullptr) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_suspend_bounded(bar, parity, ctl, abort_flag);
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 // Warp-wide busy-polling wait (lane 0 spins with test_wait, the warp then
 // synchronises): for warps on the critical path of a pipeline, where a
 // sleeping poller would wake up late.  All 32 lanes must call it.

@@ -81,6 +81,27 @@ cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, con
                          int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                          const DeviceInfo& dev);
 
+// 1 <= M <= kTileMaxM: the weights-stationary token-tile kernel
+// (pq2_tile.cu): weights expanded into tensor memory, 16, 32 or 64 token
+// rows per tile, split-K partial sums reduced in a fixed order.
+constexpr int kTileMaxM = 64;
+size_t tile_workspace_bytes(int64_t M, int64_t N, int64_t K);
+size_t tile_scratch_bytes(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_tile(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
+                        const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N, int64_t K,
+                        void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
+                        const DeviceInfo& dev);
+
+// The tensor-core kernel pq2_gemm_small runs for 5 to 16 tokens (and for
+// fewer when the DP4A kernel cannot take the shape): the token-tile kernel,
+// or small_kernel when forced.  Scratch for this device / for any device.
+size_t small_tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int num_sms);
+size_t small_tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_small_tc(const int8_t* qp, const float* S, const int32_t* T,
+                            const uint8_t* codes, const __half* ws, float* y, int32_t* dots,
+                            int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st,
+                            const pq2::DevCtl& ctl, const DeviceInfo& dev);
+
 // Any M: tcgen05 tensor-core kernel (token planes prepared in the workspace).
 size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,

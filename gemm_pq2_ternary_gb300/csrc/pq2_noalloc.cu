@@ -65,7 +65,7 @@ pq2_status pq2_gemm_small_noalloc(const int8_t* qp, const float* S, const int32_
     // scratch grows with the number of 128-row tiles: a shape that does not
     // fit even with a single CTA is refused before the device is touched
     // (e.g. N = 248320 at 16 tokens needs about 16 MB).
-    if (M > 8 && pq2h::small_scratch_bytes(M, N, K, 1) > kScratchBytes) return PQ2_ERR_WORKSPACE;
+    if (M > 8 && pq2h::small_tc_scratch_bytes(M, N, K, 1) > kScratchBytes) return PQ2_ERR_WORKSPACE;
     pq2h::DeviceInfo dev;
     pq2::DevCtl ctl;
     if (!pq2h::device_info(&dev) || !pq2h::make_ctl(&ctl)) return PQ2_ERR_CUDA;
@@ -76,10 +76,10 @@ pq2_status pq2_gemm_small_noalloc(const int8_t* qp, const float* S, const int32_
                    ? PQ2_OK
                    : PQ2_ERR_CUDA;
     // scratch this shape needs on this device (split-K partial sums)
-    if (pq2h::small_scratch_bytes(M, N, K, dev.num_sms) > kScratchBytes) return PQ2_ERR_WORKSPACE;
+    if (pq2h::small_tc_scratch_bytes(M, N, K, dev.num_sms) > kScratchBytes) return PQ2_ERR_WORKSPACE;
     void* scratch = scratch_for_current_device();
     if (!scratch) return PQ2_ERR_CUDA;
-    const cudaError_t e = pq2h::launch_small(qp, S, T, codes, static_cast<const __half*>(ws_f16),
+    const cudaError_t e = pq2h::launch_small_tc(qp, S, T, codes, static_cast<const __half*>(ws_f16),
                                              y, nullptr, M, N, K, scratch,
                                              static_cast<cudaStream_t>(stream), ctl, dev);
     return e == cudaSuccess ? PQ2_OK : PQ2_ERR_CUDA;

@@ -861,6 +861,7 @@ bool wide_kernel_fits() {
 // GPUs this library is built for; forcing the variant
 // (pq2_debug_force_kernel) gives it room at any shape.  The size depends on
 // the shape (and the forced variant) only, not on the device.
+constexpr int kTileDefaultMaxM = 32;
 constexpr int kWideMinTiles = 128;
 constexpr int kWideMinMTiles = 8;
 struct WsLayout {
@@ -900,15 +901,29 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
 
 namespace pq2h {
 
+// Up to kTileMaxM tokens the token-tile kernel runs by default; the
+// workspace covers it and the 128-row tile kernels (either may be forced).
 size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     const WsLayout l = ws_layout(M, N, K);
-    return l.total;
+    if (M > kTileMaxM) return l.total;
+    const size_t t = tile_workspace_bytes(M, N, K);
+    return t > l.total ? t : l.total;
 }
 
 cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
                            const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
                            int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                            const DeviceInfo& dev) {
+    // Up to kTileDefaultMaxM tokens the token-tile kernel by default (measured
+    // at 5120 -> 17408, us per call: 17 tokens 33.3 against 39.4 for the
+    // 128 x 128 tile kernel, 32 tokens 34.2 against 34.4; at 64 tokens the
+    // 128 x 128 tiles are ahead, 35.8 against 37.3).
+    const int force = forced_variant(PQ2_OP_PREFILL);
+    if (force == PQ2_VARIANT_PREFILL_TILE ||
+        (force == PQ2_VARIANT_DEFAULT && M <= kTileDefaultMaxM)) {
+        if (M > kTileMaxM) return kUnsupportedVariant;
+        return launch_tile(qp, S, T, codes, ws, y, dots, M, N, K, workspace, st, ctl, dev);
+    }
     const WsLayout l = ws_layout(M, N, K);
     uint8_t* w = static_cast<uint8_t*>(workspace);
     uint8_t* ahi = w + l.ahi;
@@ -921,7 +936,6 @@ cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, c
     // expanded weights (ws_layout) and the tiles fill every SM at least once
     // (below one wave the wide tiles leave SMs idle).  The integer-dot debug
     // output takes the same kernel as y.
-    const int force = forced_variant(PQ2_OP_PREFILL);
     const bool fits = dots ? wide_kernel_fits<true>() : wide_kernel_fits<false>();
     const bool wide = l.wexp_bytes > 0 && fits &&
                       (force == PQ2_VARIANT_PREFILL_WIDE ||

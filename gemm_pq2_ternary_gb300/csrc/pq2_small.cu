@@ -734,4 +734,29 @@ cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, con
     return launch(kern, dim3(l.grid), dim3(kThreads), smem, st, true, p);
 }
 
+// The tensor-core kernel of pq2_gemm_small: small_kernel by default, the
+// token-tile kernel when forced (PQ2_VARIANT_SMALL_TILE).  Measured on GB300
+// at 16 tokens, us per call (5120 -> 17408, 6144 -> 5120): small_kernel 22.7
+// and 15.5 against 23.9 and 18.3; at 8 tokens 22.3 and 15.2 against 23.2 and
+// 17.0.  The workspace covers either.
+size_t small_tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int num_sms) {
+    return forced_variant(PQ2_OP_SMALL) == PQ2_VARIANT_SMALL_TILE
+               ? tile_scratch_bytes(M, N, K, num_sms)
+               : small_scratch_bytes(M, N, K, num_sms);
+}
+
+size_t small_tc_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    const size_t a = small_workspace_bytes(M, N, K), b = tile_workspace_bytes(M, N, K);
+    return a > b ? a : b;
+}
+
+cudaError_t launch_small_tc(const int8_t* qp, const float* S, const int32_t* T,
+                            const uint8_t* codes, const __half* ws, float* y, int32_t* dots,
+                            int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st,
+                            const pq2::DevCtl& ctl, const DeviceInfo& dev) {
+    if (forced_variant(PQ2_OP_SMALL) == PQ2_VARIANT_SMALL_TILE)
+        return launch_tile(qp, S, T, codes, ws, y, dots, M, N, K, workspace, st, ctl, dev);
+    return launch_small(qp, S, T, codes, ws, y, dots, M, N, K, workspace, st, ctl, dev);
+}
+
 }  // namespace pq2h

@@ -324,9 +324,13 @@ size_t pq2_gemm_small_noalloc_max_scratch(void);
 #define PQ2_VARIANT_GEMV_RING 2      /* M = 1: bulk-copy ring in shared memory      */
 #define PQ2_VARIANT_GEMV_STAGED 3    /* M = 1 fused: whole slice staged before wait */
 #define PQ2_VARIANT_SMALL_DP4A 1     /* 2..8 tokens: DP4A, code words shared        */
-#define PQ2_VARIANT_SMALL_TC 2       /* tcgen05, weights in tensor memory           */
+#define PQ2_VARIANT_SMALL_TC 2       /* tcgen05, weights in tensor memory, 16-token
+                                        tile (5..16 tokens by default)              */
+#define PQ2_VARIANT_SMALL_TILE 3     /* tcgen05 token-tile kernel (16 tokens)       */
 #define PQ2_VARIANT_PREFILL_128 1    /* tcgen05 128 x 128 tiles, in-kernel expansion */
 #define PQ2_VARIANT_PREFILL_WIDE 2   /* tcgen05 128 x 256 tiles, pre-expanded weights */
+#define PQ2_VARIANT_PREFILL_TILE 3   /* tcgen05 token-tile kernel, M <= 64 (by
+                                        default up to 32 tokens)                    */
 
 /*
  * pq2_debug_force_kernel -- test hook: from now on, calls of `op`

@@ -282,6 +282,45 @@ def test_prefill_group_dots_bit_exact(pq2, prob):
 
 
 # ----------------------------------------------------------------------------
+# 17 to 64 tokens (pq2_gemm_prefill, token-tile kernel)
+# ----------------------------------------------------------------------------
+MID_PROBLEMS = ([inputs.Problem(f"mid_ragged_m{M}", M, 640, 300, "p343", "outliers", 110 + M)
+                 for M in (17, 31, 33, 50)] +
+                [inputs.Problem(f"mid_m{M}_k{K}_n{N}", M, K, N, "p343", "outliers", 120 + M)
+                 for M in (17, 32, 48, 64) for (K, N) in inputs.SMALL_SHAPES])
+
+
+@pytest.mark.parametrize("prob", MID_PROBLEMS, ids=lambda p: p.name)
+def test_mid_parity(pq2, prob):
+    from gemm_pq2_ternary_gb300.binding import alloc_workspace, PQ2_OP_PREFILL
+    c = Case(pq2, prob)
+    y = torch.full((prob.M, prob.N), float("nan"), device=DEV)
+    pq2.pq2_gemm_prefill(c.qp_d, c.S_d, c.T_d, c.codes_d, c.ws_d, y,
+                         alloc_workspace(PQ2_OP_PREFILL, prob.M, prob.N, prob.K))
+    if prob.M * prob.N * prob.K <= 64 * 1024 * 1024:
+        _check_full(pq2, c, y)
+    else:
+        _check_sampled(pq2, c, y, count=2048)
+
+
+@pytest.mark.parametrize("prob", MID_PROBLEMS[:4] + [MID_PROBLEMS[-1]], ids=lambda p: p.name)
+def test_mid_group_dots_bit_exact(pq2, prob):
+    from gemm_pq2_ternary_gb300.binding import alloc_workspace, PQ2_OP_PREFILL
+    c = Case(pq2, prob)
+    G = prob.K // 128
+    dots = torch.empty((prob.M, prob.N, G), dtype=torch.int32, device=DEV)
+    pq2.pq2_group_dots(pq2.PQ2_OP_PREFILL, c.qp_d, c.T_d, c.codes_d, dots,
+                       alloc_workspace(PQ2_OP_PREFILL, prob.M, prob.N, prob.K))
+    torch.cuda.synchronize()
+    got = dots.cpu().numpy()
+    if prob.M * prob.N * prob.K <= 64 * 1024 * 1024:
+        assert np.array_equal(got, oracle.group_dots(c.oqp, c.ocodes))
+    else:
+        rows = np.r_[0:256, prob.N - 256:prob.N]
+        assert np.array_equal(got[:, rows], oracle.group_dots(c.oqp, c.ocodes[rows]))
+
+
+# ----------------------------------------------------------------------------
 # whole path from fp16 and error reporting
 # ----------------------------------------------------------------------------
 @pytest.mark.parametrize("M", [1, 6, 40])
@@ -315,9 +354,12 @@ def test_bounded_wait_reports_timeout(pq2):
 
 @pytest.mark.parametrize("op,variant,prob", [
     ("small", "tc", inputs.Problem("timeout_small", 8, 1280, 640, "p343", "outliers", 51)),
+    ("small", "tile", inputs.Problem("timeout_tile16", 8, 1280, 640, "p343", "outliers", 54)),
+    ("prefill", "tile", inputs.Problem("timeout_tile64", 40, 1280, 640, "p343", "outliers", 55)),
     ("prefill", "128", inputs.Problem("timeout_pf128", 37, 384, 200, "uniform", "normal", 52)),
     ("prefill", "wide", inputs.Problem("timeout_pfwide", 37, 384, 200, "uniform", "normal", 53)),
-], ids=["small_kernel", "prefill_kernel", "prefill_wide_kernel"])
+], ids=["small_kernel", "tile_kernel_16", "tile_kernel_64", "prefill_kernel",
+        "prefill_wide_kernel"])
 def test_tensor_core_pipelines_report_timeout(pq2, op, variant, prob):
     # As above for the tcgen05 pipelines: the producer of each CTA withholds
     # its first stage; the MMA issuers and the other roles give up after the
@@ -326,8 +368,10 @@ def test_tensor_core_pipelines_report_timeout(pq2, op, variant, prob):
     # PQ2_ERR_TIMEOUT.  The next normal call is correct.
     from gemm_pq2_ternary_gb300.binding import alloc_workspace
     opc = pq2.PQ2_OP_SMALL if op == "small" else pq2.PQ2_OP_PREFILL
-    var = {"tc": pq2.PQ2_VARIANT_SMALL_TC, "128": pq2.PQ2_VARIANT_PREFILL_128,
-           "wide": pq2.PQ2_VARIANT_PREFILL_WIDE}[variant]
+    var = {("small", "tc"): pq2.PQ2_VARIANT_SMALL_TC, ("small", "tile"): pq2.PQ2_VARIANT_SMALL_TILE,
+           ("prefill", "tile"): pq2.PQ2_VARIANT_PREFILL_TILE,
+           ("prefill", "128"): pq2.PQ2_VARIANT_PREFILL_128,
+           ("prefill", "wide"): pq2.PQ2_VARIANT_PREFILL_WIDE}[(op, variant)]
     fn = pq2.pq2_gemm_small if op == "small" else pq2.pq2_gemm_prefill
     c = Case(pq2, prob)
     y = torch.empty((prob.M, prob.N), device=DEV)

@@ -101,6 +101,16 @@ def test_small_tensor_core_kernel_forced(pq2, prob):
     assert np.array_equal(got, oracle.group_dots(c.oqp, c.ocodes))
 
 
+@pytest.mark.parametrize("prob", SMALL_FORCED, ids=lambda p: p.name)
+def test_small_token_tile_kernel_forced(pq2, prob):
+    # forced (the default for 5 to 16 tokens is small_kernel), also at 2 tokens
+    c = Case(pq2, prob)
+    y = _run(pq2, c, pq2.PQ2_OP_SMALL, pq2.PQ2_VARIANT_SMALL_TILE)
+    _check_oracle(c, y)
+    got = _dots(pq2, c, pq2.PQ2_OP_SMALL, pq2.PQ2_VARIANT_SMALL_TILE)
+    assert np.array_equal(got, oracle.group_dots(c.oqp, c.ocodes))
+
+
 @pytest.mark.parametrize("prob", [SMALL_FORCED[1], SMALL_FORCED[2]], ids=lambda p: p.name)
 def test_small_dp4a_kernel_forced(pq2, prob):
     # 5 and 8 tokens: the routing gives them to the tensor cores
@@ -159,6 +169,21 @@ def test_prefill_kernels_forced_agree_bit_for_bit(pq2, prob):
     want = oracle.group_dots(c.oqp, c.ocodes)
     assert np.array_equal(_dots(pq2, c, pq2.PQ2_OP_PREFILL, pq2.PQ2_VARIANT_PREFILL_WIDE), want)
     assert np.array_equal(_dots(pq2, c, pq2.PQ2_OP_PREFILL, pq2.PQ2_VARIANT_PREFILL_128), want)
+
+
+@pytest.mark.parametrize("prob", PREFILL_FORCED[:2] + [
+    inputs.Problem("tile_m64", 64, 1024, 520, "uniform", "normal", 65),
+    inputs.Problem("tile_m5", 5, 384, 300, "p343", "outliers", 66)], ids=lambda p: p.name)
+def test_prefill_token_tile_kernel_forced(pq2, prob):
+    # the token-tile kernel through pq2_gemm_prefill (its default up to 32
+    # tokens), and the 128 x 128 tile kernel forced on the same shapes
+    c = Case(pq2, prob)
+    y_tile = _run(pq2, c, pq2.PQ2_OP_PREFILL, pq2.PQ2_VARIANT_PREFILL_TILE)
+    _check_oracle(c, y_tile)
+    want = oracle.group_dots(c.oqp, c.ocodes)
+    assert np.array_equal(_dots(pq2, c, pq2.PQ2_OP_PREFILL, pq2.PQ2_VARIANT_PREFILL_TILE), want)
+    y_128 = _run(pq2, c, pq2.PQ2_OP_PREFILL, pq2.PQ2_VARIANT_PREFILL_128)
+    _check_oracle(c, y_128)
 
 
 def test_prefill_full_size_kernels_agree_bit_for_bit(pq2):
@@ -221,6 +246,15 @@ def test_small_deterministic(pq2, K, N):
     y0 = _run(pq2, c, pq2.PQ2_OP_SMALL)
     for _ in range(4):
         assert torch.equal(_run(pq2, c, pq2.PQ2_OP_SMALL), y0)
+
+
+@pytest.mark.parametrize("M", [32, 64])
+def test_mid_deterministic(pq2, M):
+    # 32 tokens: the token-tile kernel; 64: the 128 x 128 tile kernel
+    c = Case(pq2, inputs.Problem(f"det_mid_m{M}", M, 5120, 17408, "p343", "outliers", 95 + M))
+    y0 = _run(pq2, c, pq2.PQ2_OP_PREFILL)
+    for _ in range(4):
+        assert torch.equal(_run(pq2, c, pq2.PQ2_OP_PREFILL), y0)
 
 
 @pytest.mark.parametrize("M", [128, 300])
