@@ -150,6 +150,7 @@ def workload_spec(args):
 KERNEL_SOURCES = {
     "gemv": ["pq2_gemv.cu", "pq2_common.cuh"],
     "small": ["pq2_small.cu", "pq2_common.cuh"],
+    "tile": ["pq2_tile.cu", "pq2_common.cuh"],
     "prefill": ["pq2_prefill.cu", "pq2_common.cuh"],
     "bf16": ["pq2_bf16.cu", "pq2_common.cuh"],
     "multi": ["pq2_multi.cu", "pq2_common.cuh"],
@@ -174,7 +175,11 @@ def kernel_family(layer):
     M, K, N = layer[0][:3]
     if small_takes_dp4a(M, N, K):
         return "multi"
-    return "gemv" if M == 1 else ("small" if M <= 16 else "prefill")
+    if M == 1:
+        return "gemv"
+    # the library's routing: small_kernel to 16 tokens, the token-tile kernel
+    # to 32 (pq2_gemm_prefill), the 128-row tile kernels above
+    return "small" if M <= 16 else ("tile" if M <= 32 else "prefill")
 
 
 def sources_hash(family):

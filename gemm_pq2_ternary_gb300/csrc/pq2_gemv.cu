@@ -79,6 +79,7 @@ struct GemvParams {
     uint32_t codes_row_bytes;  // K / 4
     uint32_t act_off, red_off, ring_off;  // shared-memory layout
     uint32_t ws_off;                      // staged variant: weight scales
+    uint32_t x_off;                       // staged variant: fp16 activations
     pq2::DevCtl ctl;
 };
 
@@ -553,6 +554,7 @@ cudaError_t launch_direct(const GemvParams& p, int grid, size_t smem, cudaStream
 // an SM, so under programmatic dependent launch the next call's CTA stages
 // its slice while this one computes: the weight stream of call i+1 overlaps
 // the quantisation, dots and row sums of call i.
+// After the wait, x reaches shared memory in one bulk copy per CTA.
 // Work split: 48 teams of 8 lanes.  A team quantises one group into its own
 // shared slot (no barrier across warps), then lane j of the team computes the
 // group's terms for rows j, j+8, ... (or, when groups are fewer than teams,
@@ -566,14 +568,6 @@ constexpr int kStagedTeams = kStagedThreads / 8;
 constexpr uint32_t kStagedPad = 16;             // extra bytes between staged code rows
 constexpr size_t kStagedMaxSmem = 100 * 1024;   // two CTAs per SM
 constexpr size_t kStagedMinSlice = 16 * 1024;   // smaller per-CTA slices: the direct variant
-
-__device__ __forceinline__ uint4 ld_cg_v4(const void* ptr) {
-    uint4 v;
-    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr));
-    return v;
-}
 
 // group_codes_dot64 of two code rows against the same activations, the two
 // rows' DP4A chains interleaved (eight independent accumulators).
@@ -600,6 +594,7 @@ __device__ __forceinline__ void group_codes_dot64_x2(const uint32_t (&w0)[8], co
 __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* wbar = reinterpret_cast<uint64_t*>(smem);  // the weight slice has landed
+    uint64_t* xbar = wbar + 1;                           // all of x has landed
     const int n_begin = blockIdx.x * p.rows_per_cta;
     const int rows = min(p.N, n_begin + p.rows_per_cta) - n_begin;
     const int tid = threadIdx.x;
@@ -607,6 +602,7 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
     const uint32_t rs = rowb + kStagedPad;
     if (tid == 0) {
         pq2::mbar_init(wbar, 1);
+        pq2::mbar_init(xbar, 1);
         pq2::fence_mbar_init();
     }
     __syncthreads();
@@ -638,6 +634,10 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
     pq2::pdl_wait();
     pq2::pdl_launch_dependents();
     if (rows <= 0) return;
+    if (tid == 0) {
+        pq2::mbar_arrive_expect_tx(xbar, 2u * p.K);
+        pq2::bulk_g2s(smem + p.x_off, p.x, 2u * p.K, xbar);
+    }
 
     const int lane = tid & 31;
     const int warp = tid >> 5;
@@ -657,15 +657,17 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
     const uint32_t codes_s = pq2::smem_u32(smem + p.ring_off);
     const uint32_t ws_s = pq2::smem_u32(smem + p.ws_off);
     const uint32_t red_s = pq2::smem_u32(smem + p.red_off);
+    const uint32_t x_s = pq2::smem_u32(smem + p.x_off);
     const int rstr = p.G + 1;  // words between rows of terms (conflict-free stores)
     const int passes = (p.G + gstep - 1) / gstep;  // uniform over the CTA
     for (int pass = 0; pass < passes; ++pass) {
         const int g = gslot + pass * gstep;
         const bool valid = tactive && g < p.G;
         const int gl = valid ? g : 0;
+        if (pass == 0 && !pq2::mbar_wait_warp(xbar, 0, p.ctl)) failed = true;
         {
-            const __half* src = p.x + static_cast<size_t>(gl) * 128 + 16 * j;
-            const uint4 h[2] = {ld_cg_v4(src), ld_cg_v4(src + 8)};
+            const uint32_t src = x_s + gl * 256u + 32u * j;
+            const uint4 h[2] = {pq2::lds_v4(src), pq2::lds_v4(src + 16)};
             pq2::quantize_group8(h, j, valid, qslot, sslot, tslot);
         }
         __syncwarp();
@@ -683,7 +685,7 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
         // the weights were requested before the dependency wait; by now they
         // have usually landed (every warp waits on its own; a warp whose wait
         // runs out computes nothing and the CTA writes no y)
-        if (pass == 0) failed = !pq2::mbar_wait_warp(wbar, 0, p.ctl);
+        if (pass == 0 && !failed) failed = !pq2::mbar_wait_warp(wbar, 0, p.ctl);
         const int nk = !failed && valid && li < rows ? (rows - li + lstep - 1) / lstep : 0;
         const uint32_t cs = codes_s + li * rs + gl * 32;
         const uint32_t cstep = lstep * rs;
@@ -720,7 +722,10 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
         __syncwarp();  // the slot is rewritten by the next pass
     }
     if (__syncthreads_or(failed)) {
-        if (tid == 0) pq2::mbar_wait_bounded(wbar, 0, p.ctl);  // no copy in flight at exit
+        if (tid == 0) {  // no copy in flight at exit
+            pq2::mbar_wait_bounded(wbar, 0, p.ctl);
+            pq2::mbar_wait_bounded(xbar, 0, p.ctl);
+        }
         return;
     }
     // row sums: 8 lanes per row, each over a fixed stride of the row's terms,
@@ -750,7 +755,8 @@ size_t staged_layout(GemvParams& p) {
     p.act_off = static_cast<uint32_t>((p.ws_off + wsz + 127) & ~static_cast<size_t>(127));
     const size_t act = static_cast<size_t>(kQStride + 8) * kStagedTeams;
     p.red_off = static_cast<uint32_t>((p.act_off + act + 127) & ~static_cast<size_t>(127));
-    const size_t total = p.red_off + rows * (p.G + 1) * 4;
+    p.x_off = static_cast<uint32_t>((p.red_off + rows * (p.G + 1) * 4 + 127) & ~static_cast<size_t>(127));
+    const size_t total = p.x_off + 2 * static_cast<size_t>(p.K);
     if (rows * p.codes_row_bytes < kStagedMinSlice) return 0;
     return total <= kStagedMaxSmem ? total : 0;
 }

@@ -663,15 +663,16 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1) tile_kernel(const __grid_
             for (int i = 0; i < 8; ++i) f2unpack(acc[i], a[2 * i], a[2 * i + 1]);
             if (C::GP == 2) {
                 // the odd parity hands its sums to the even one: even + odd
-                float* cb = comb + r * MT + 16 * tb;
+                // (comb is [token][row]: consecutive lanes, consecutive words)
+                float* cb = comb + 16 * tb * kRows + r;
                 if (!flusher) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) cb[i] = a[i];
+                    for (int i = 0; i < 16; ++i) cb[i * kRows] = a[i];
                 }
                 pq2::named_bar_sync(1, C::PW * 32);
                 if (flusher) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) a[i] += cb[i];
+                    for (int i = 0; i < 16; ++i) a[i] += cb[i * kRows];
                 }
             }
 #pragma unroll
