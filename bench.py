@@ -486,6 +486,28 @@ def latency_floor(torch, pq2, layer, R, flags, stream, reps):
     return ms * 1e3 / (reps * R * len(layer))
 
 
+def tensor_probe(torch, pq2, device, stream, clk):
+    """The measured issue rate of the tensor-core instruction the prefill
+    kernels use (tcgen05 kind::f8f6f4, e4m3, M = 128, N = 256, K = 32, back
+    to back on every SM: pq2_debug_mma_rate), as int8-equivalent TOPS at the
+    SM clock sampled during the timed region (each int8 product is two e4m3
+    products, hi and lo, so int8-equivalent operations per second equal e4m3
+    multiply-adds per second)."""
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    cycles = torch.zeros(sms, dtype=torch.int64, device=device)
+    iters = 4096
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            pq2.pq2_debug_mma_rate(256, iters, cycles, stream)
+    stream.synchronize()
+    c = cycles.double().mean().item()
+    mac_per_cycle = 128.0 * 256 * 32 * iters / c
+    mhz = (clk or {}).get("sm_mhz") or 2070.0
+    return {"instr": "tcgen05.mma kind::f8f6f4 e4m3 M=128 N=256 K=32, A in tensor memory",
+            "mac_per_cycle_per_sm": round(mac_per_cycle, 1), "sms": sms, "sm_mhz": mhz,
+            "int8eq_tops_at_clock": round(mac_per_cycle * sms * mhz * 1e6 * 1e-12, 1)}
+
+
 def measure(args, wl, rank, world, dist, steps, warmup, target_ms, e2e_passes, floor):
     """Build R layers of the workload, capture the step graph, time `steps`
     steps of `reps` replays (after `warmup` untimed ones), then the dominant
@@ -557,6 +579,10 @@ def measure(args, wl, rank, world, dist, steps, warmup, target_ms, e2e_passes, f
                 "frac_of_nominal": round(achieved / BF16_NOMINAL_TFLOPS, 4),
                 "traffic": recorded_traffic(name, kernel_family(layer)),
                 "peak_source": f"{peak_src}: MEASURED_PEAKS.json bf16_tflops (burst)"}
+
+    if kind == "TOPS":
+        roof["tensor_probe"] = tensor_probe(torch, pq2, device, stream, clk)
+        roof["frac_of_probe"] = round(achieved / roof["tensor_probe"]["int8eq_tops_at_clock"], 4)
 
     floor_us = None
     if floor and all(M == 1 and not is_bf16(pr) for pr in layer for M in [pr[0]]):

@@ -67,6 +67,7 @@ SIGNATURES = {
     "pq2_debug_skip_stage": ([_I], _I),
     "pq2_debug_force_kernel": ([_I, _I], _I),
     "pq2_debug_gemv_floor": ([_I64, _I64, _U32, _P], _I),
+    "pq2_debug_mma_rate": ([_I, _I, _P, _P], _I),
     "pq2_gemm_small_noalloc": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _I),
     "pq2_gemm_small_noalloc_max_scratch": ([], _SZ),
 }
@@ -271,6 +272,15 @@ def pq2_debug_force_kernel(op: int, variant: int):
 def pq2_debug_gemv_floor(N: int, K: int, flags: int = 0, stream=None):
     """One empty launch shaped like a fused M = 1 call (the latency floor)."""
     _check(_lib.pq2_debug_gemv_floor(N, K, flags, _stream(stream)), "pq2_debug_gemv_floor")
+
+
+def pq2_debug_mma_rate(n: int, iters: int, cycles, stream=None):
+    """cycles: int64 CUDA tensor with (at least) one entry per SM."""
+    _dtype(cycles, torch.int64, "cycles")
+    sms = torch.cuda.get_device_properties(cycles.device).multi_processor_count
+    if cycles.numel() < sms:
+        raise ValueError(f"cycles: needs {sms} entries, got {cycles.numel()}")
+    _check(_lib.pq2_debug_mma_rate(n, iters, _ptr(cycles), _stream(stream)), "pq2_debug_mma_rate")
 
 
 class forced_kernel:

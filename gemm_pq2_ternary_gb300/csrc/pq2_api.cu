@@ -184,6 +184,18 @@ pq2_status pq2_debug_gemv_floor(int64_t N, int64_t K, uint32_t flags, void* stre
                                                static_cast<cudaStream_t>(stream), c.ctl, c.dev));
 }
 
+pq2_status pq2_debug_mma_rate(int n, int iters, uint64_t* cycles, void* stream) {
+    if ((n != 32 && n != 64 && n != 128 && n != 256) || iters < 1 || iters > (1 << 24))
+        return PQ2_ERR_INVALID_ARG;
+    if (!cycles) return PQ2_ERR_INVALID_ARG;
+    Ctx c;
+    pq2_status s = get_ctx(&c);
+    if (s != PQ2_OK) return s;
+    return cuda_status(pq2h::launch_mma_rate(n, iters,
+                                             reinterpret_cast<unsigned long long*>(cycles),
+                                             static_cast<cudaStream_t>(stream), c.ctl, c.dev));
+}
+
 pq2_status pq2_quantize_act(const void* x_f16, int64_t M, int64_t K, int8_t* qp, float* S,
                             int32_t* T, void* stream) {
     if (M < 0 || K < 1) return PQ2_ERR_INVALID_ARG;

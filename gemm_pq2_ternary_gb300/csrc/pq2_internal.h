@@ -92,6 +92,11 @@ cudaError_t launch_tile(const int8_t* qp, const float* S, const int32_t* T, cons
                         void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                         const DeviceInfo& dev);
 
+// Back-to-back tcgen05 e4m3 MMAs (M = 128, N = n, K = 32) on every SM:
+// cycles[sm] = clock cycles for `iters` of them (pq2_debug_mma_rate).
+cudaError_t launch_mma_rate(int n, int iters, unsigned long long* cycles, cudaStream_t st,
+                            const pq2::DevCtl& ctl, const DeviceInfo& dev);
+
 // The tensor-core kernel pq2_gemm_small runs for 5 to 16 tokens (and for
 // fewer when the DP4A kernel cannot take the shape): the token-tile kernel,
 // or small_kernel when forced.  Scratch for this device / for any device.

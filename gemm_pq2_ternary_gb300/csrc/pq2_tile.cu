@@ -743,6 +743,81 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1) tile_kernel(const __grid_
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
 }
 
+// ---------------------------------------------------------------------------
+// measurement: the issue rate of back-to-back tcgen05 e4m3 MMAs
+// ---------------------------------------------------------------------------
+// One CTA per SM; one thread issues `iters` MMAs of M = 128, N, K = 32 (A in
+// tensor memory, B in shared memory, all into one accumulator), commits, and
+// waits (bounded) for them; cycles[blockIdx.x] = clock64 cycles from the
+// first issue to the completion.  The operands are constant (e4m3 2^-9).
+template <int N>
+__global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned long long* cycles,
+                                                          pq2::DevCtl ctl) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t done;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    uint8_t* b = smem + ((1024 - (pq2::smem_u32(smem) & 1023)) & 1023);
+    for (int i = tid; i < N * 128 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(b)[i] = 0x01010101u;
+    if (tid == 0) {
+        pq2::mbar_init(&done, 1);
+        pq2::fence_mbar_init();
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         pq2::smem_u32(&tmem_base)),
+                     "r"(512));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    {  // A: columns 256..287 (4 k-steps of 8), each warp its lane quadrant
+        uint32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0x01010101u;
+        const uint32_t a = tmem + (static_cast<uint32_t>(warp * 32) << 16) + 256;
+        tmem_st16(a, v);
+        tmem_st16(a + 16, v);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        constexpr uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
+                                   (static_cast<uint32_t>(kRows >> 4) << 24);
+        const uint64_t b0 = sw128_desc(pq2::smem_u32(b));
+        const long long c0 = clock64();
+        for (int i = 0; i < iters; ++i) {
+            const int k = i & 3;
+            mma_ta<idesc>(tmem, tmem + 256 + 8 * k, b0 + ((32 * k) >> 4), i > 0);
+        }
+        mma_commit(&done);
+        const bool ok = pq2::mbar_wait_bounded(&done, 0, ctl);
+        const long long c1 = clock64();
+        cycles[blockIdx.x] = ok ? static_cast<unsigned long long>(c1 - c0) : 0ull;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+}
+
+template <int N>
+cudaError_t launch_mma_rate(int iters, unsigned long long* cycles, cudaStream_t st,
+                            const pq2::DevCtl& ctl, const pq2h::DeviceInfo& dev) {
+    const size_t smem = 1024 + static_cast<size_t>(N) * 128;
+    static pq2h::SmemLimit lim;
+    const cudaError_t e = pq2h::ensure_smem(lim, mma_rate_kernel<N>, smem);
+    if (e != cudaSuccess) return e;
+    return pq2h::launch(mma_rate_kernel<N>, dim3(dev.num_sms), dim3(128), smem, st, false, iters,
+                        cycles, ctl);
+}
+
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
 struct TileLayout {
@@ -847,6 +922,17 @@ cudaError_t launch_tile(const int8_t* qp, const float* S, const int32_t* T, cons
     if (l.mt == 16) return launch_mt<16>(qp, S, T, codes, ws, y, dots, M, N, K, l, w, st, ctl, dev);
     if (l.mt == 32) return launch_mt<32>(qp, S, T, codes, ws, y, dots, M, N, K, l, w, st, ctl, dev);
     return launch_mt<64>(qp, S, T, codes, ws, y, dots, M, N, K, l, w, st, ctl, dev);
+}
+
+cudaError_t launch_mma_rate(int n, int iters, unsigned long long* cycles, cudaStream_t st,
+                            const pq2::DevCtl& ctl, const DeviceInfo& dev) {
+    switch (n) {
+        case 32: return ::launch_mma_rate<32>(iters, cycles, st, ctl, dev);
+        case 64: return ::launch_mma_rate<64>(iters, cycles, st, ctl, dev);
+        case 128: return ::launch_mma_rate<128>(iters, cycles, st, ctl, dev);
+        case 256: return ::launch_mma_rate<256>(iters, cycles, st, ctl, dev);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace pq2h

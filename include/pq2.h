@@ -359,6 +359,19 @@ pq2_status pq2_debug_force_kernel(int op, int variant);
 pq2_status pq2_debug_gemv_floor(int64_t N, int64_t K, uint32_t flags, void* stream);
 
 /*
+ * pq2_debug_mma_rate -- measurement hook: the rate at which one thread per SM
+ * can issue tcgen05 MMAs of the kind the tensor-core kernels use
+ * (kind::f8f6f4, e4m3 operands, M = 128, N = n, K = 32; A in tensor memory,
+ * B in shared memory), back to back into one accumulator.  Enqueues one
+ * launch of one CTA per SM; on completion cycles[sm] holds the SM clock
+ * cycles from the first issue to the completion of `iters` MMAs (0 if the
+ * bounded wait ran out).  n in {32, 64, 128, 256}, 1 <= iters <= 2^24.
+ *   cycles  device uint64 array of at least (number of SMs) entries.
+ * Multiply-adds per cycle per SM: 128 * n * 32 * iters / cycles.
+ */
+pq2_status pq2_debug_mma_rate(int n, int iters, uint64_t* cycles, void* stream);
+
+/*
  * pq2_debug_set_wait_limit_ns -- bound on every on-chip barrier wait, in
  * nanoseconds (default 2e9).  For tests of the timeout path only.
  */

@@ -216,3 +216,12 @@ def test_force_kernel_checks_its_arguments(lib):
     finally:
         assert f(b.PQ2_OP_PREFILL, b.PQ2_VARIANT_DEFAULT) == b.PQ2_OK
     assert b.pq2_workspace_bytes(b.PQ2_OP_PREFILL, 128, N, K) == default
+
+
+def test_measurement_hooks_check_their_arguments(lib):
+    from gemm_pq2_ternary_gb300 import binding as b
+    assert lib.pq2_debug_mma_rate(48, 16, _p(FAKE), None) == b.PQ2_ERR_INVALID_ARG
+    assert lib.pq2_debug_mma_rate(256, 0, _p(FAKE), None) == b.PQ2_ERR_INVALID_ARG
+    assert lib.pq2_debug_mma_rate(256, 16, None, None) == b.PQ2_ERR_INVALID_ARG
+    assert lib.pq2_debug_gemv_floor(5120, 6144, 2, None) == b.PQ2_ERR_INVALID_ARG
+    assert lib.pq2_debug_gemv_floor(5120, 100, 0, None) == b.PQ2_ERR_UNSUPPORTED_SHAPE

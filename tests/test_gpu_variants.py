@@ -264,3 +264,21 @@ def test_prefill_deterministic(pq2, M):
     y0 = _run(pq2, c, pq2.PQ2_OP_PREFILL)
     for _ in range(4):
         assert torch.equal(_run(pq2, c, pq2.PQ2_OP_PREFILL), y0)
+
+
+def test_mma_rate_probe(pq2):
+    # the measurement hook behind the prefill roofline's tensor probe: N = 256
+    # runs the pipe near its e4m3 peak (about 8190 multiply-adds per cycle per
+    # SM measured), N = 32 is bound by the issue cost (about 46 cycles each)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cycles = torch.zeros(sms, dtype=torch.int64, device=DEV)
+    for n, lo, hi in ((256, 4000.0, 9000.0), (32, 500.0, 9000.0)):
+        pq2.pq2_debug_mma_rate(n, 2048, cycles)
+        torch.cuda.synchronize()
+        assert pq2.pq2_last_device_error() == pq2.PQ2_OK
+        c = cycles.cpu().numpy().astype(np.float64)
+        assert (c > 0).all()
+        rate = 128.0 * n * 32 * 2048 / c.mean()
+        assert lo < rate < hi, (n, rate)
+    with pytest.raises(pq2.PQ2Error):
+        pq2.pq2_debug_mma_rate(48, 16, cycles)
