@@ -271,6 +271,12 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
     unsigned short v;
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
@@ -321,6 +327,36 @@ __device__ __forceinline__ float rcp_approx(float x) {
 
 constexpr uint32_t kRcp127Bits = 0x3C010204u;  // fp32 nearest 1/127
 
+// Two-wide fp32 arithmetic (one instruction, two IEEE round-to-nearest
+// operations): the same bits as two scalar operations.
+__device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi) {
+    unsigned long long v;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+    return v;
+}
+__device__ __forceinline__ void f32x2_unpack(unsigned long long v, uint32_t& lo, uint32_t& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f32x2_mul(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f32x2_fma(unsigned long long a, unsigned long long b,
+                                                        unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f32x2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+#ifndef PQ2_QUANT_X2
+#define PQ2_QUANT_X2 1
+#endif
+
 // Quantise one 128-value group with 8 consecutive lanes of a warp ("Making a
 // ternary reasoning model fast in vLLM", page "From CUDA to Triton and
 // Gluon", section "Prompt processing": q int8, s fp32, t int32 per group;
@@ -334,7 +370,8 @@ constexpr uint32_t kRcp127Bits = 0x3C010204u;  // fp32 nearest 1/127
 // |x / d| below 127.5.  T = sum q.  An all-zero group gives d = 0, q = 0.
 // Nothing is written unless `store`; lane j == 0 writes s and t.
 __device__ __forceinline__ void quantize_group8(const uint4 (&h)[2], int j, bool store,
-                                                int8_t* qg, float* s_out, int32_t* t_out) {
+                                                int8_t* qg, float* s_out, int32_t* t_out,
+                                                float& s_all, int& t_all) {
     const __half2* hv = reinterpret_cast<const __half2*>(h);
     __half2 m = __habs2(hv[0]);
 #pragma unroll
@@ -350,12 +387,34 @@ __device__ __forceinline__ void quantize_group8(const uint4 (&h)[2], int j, bool
     // itself rounds to an integer, half to even, and the low byte of its bit
     // pattern is q as an int8 (|x / d| < 127.5).
     uint32_t qb[16];
+#if PQ2_QUANT_X2
+    // the quotients of div_corrected two at a time: q0 = x*y,
+    // r = q0*(-d) + x (= x - q0*d, one rounding), q = r*y + q0.  An all-zero
+    // group runs with y = 0: every x is +-0 there and every q comes out +0,
+    // as the scalar path's explicit zero does.
+    {
+        const float yz = zero ? 0.0f : y;
+        const unsigned long long y2 = f32x2_pack(yz, yz);
+        const unsigned long long nd2 = f32x2_pack(-d, -d);
+        const unsigned long long mg2 = f32x2_pack(12582912.0f, 12582912.0f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float2 v = __half22float2(hv[k]);
+            const unsigned long long v2 = f32x2_pack(v.x, v.y);
+            const unsigned long long q0 = f32x2_mul(v2, y2);
+            const unsigned long long r = f32x2_fma(q0, nd2, v2);
+            const unsigned long long q = f32x2_fma(r, y2, q0);
+            f32x2_unpack(f32x2_add(q, mg2), qb[2 * k], qb[2 * k + 1]);
+        }
+    }
+#else
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const float v = (i & 1) ? __high2float(hv[i >> 1]) : __low2float(hv[i >> 1]);
         const float qf = zero ? 0.0f : div_corrected(v, d, y);
         qb[i] = __float_as_uint(__fadd_rn(qf, 12582912.0f));
     }
+#endif
     int t = 0;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
@@ -373,6 +432,15 @@ __device__ __forceinline__ void quantize_group8(const uint4 (&h)[2], int j, bool
         *s_out = zero ? 0.0f : d;
         *t_out = t;
     }
+    s_all = zero ? 0.0f : d;  // the same in all eight lanes
+    t_all = t;
+}
+
+__device__ __forceinline__ void quantize_group8(const uint4 (&h)[2], int j, bool store,
+                                                int8_t* qg, float* s_out, int32_t* t_out) {
+    float s_all;
+    int t_all;
+    quantize_group8(h, j, store, qg, s_out, t_out, s_all, t_all);
 }
 
 // Codes-dot of one 128-weight group: 8 code words against the 32 plane-ordered
