@@ -556,52 +556,20 @@ cudaError_t launch_direct(const GemvParams& p, int grid, size_t smem, cudaStream
 // the quantisation, dots and row sums of call i.
 // After the wait, x reaches shared memory in one bulk copy per CTA.
 // Work split: 48 teams of 8 lanes.  A team quantises one group into its own
-// shared slot (no barrier across warps), then lane j of the team computes the
-// group's terms for rows j, j+8, ... (or, when groups are fewer than teams,
-// for rows j, j+8*tpg, ... across the tpg teams given the same group).  Code
-// rows sit 16 bytes further apart than K/4, so the eight rows an 8-lane phase
-// reads fall on eight distinct 16-byte bank groups.  Terms, their order and
-// the row sums are those of the other variants: y is bit-identical.
+// shared slot (no barrier across warps); every lane of the team then holds
+// the group's s and t, and lane j computes the group's terms for rows j,
+// j+8, ... (or, when groups are fewer than teams, for rows j, j+8*tpg, ...
+// across the tpg teams given the same group), two rows per iteration while
+// two are left, then the last one alone.  Code rows sit 16 bytes further
+// apart than K/4, so the eight rows an 8-lane phase reads fall on eight
+// distinct 16-byte bank groups.  Terms, their order and the row sums are
+// those of the other variants: y is bit-identical.
 // ---------------------------------------------------------------------------
 constexpr int kStagedThreads = 384;
 constexpr int kStagedTeams = kStagedThreads / 8;
 constexpr uint32_t kStagedPad = 16;             // extra bytes between staged code rows
 constexpr size_t kStagedMaxSmem = 100 * 1024;   // two CTAs per SM
 constexpr size_t kStagedMinSlice = 16 * 1024;   // smaller per-CTA slices: the direct variant
-#ifndef PQ2_STAGED_XCHUNKS
-#define PQ2_STAGED_XCHUNKS 1
-#endif
-#ifndef PQ2_STAGED_TAIL
-#define PQ2_STAGED_TAIL 2
-#endif
-#ifndef PQ2_STAGED_CARVEOUT
-#define PQ2_STAGED_CARVEOUT 0
-#endif
-#ifndef PQ2_STAGED_STREG
-#define PQ2_STAGED_STREG 1
-#endif
-#ifndef PQ2_STAGED_TRIGGER
-#define PQ2_STAGED_TRIGGER 0
-#endif
-#ifndef PQ2_STAGED_SUM_UNROLL
-#define PQ2_STAGED_SUM_UNROLL 1
-#endif
-#ifndef PQ2_STAGED_QSTRIDE
-#define PQ2_STAGED_QSTRIDE 144
-#endif
-#ifndef PQ2_STAGED_ROWSUM
-#define PQ2_STAGED_ROWSUM 0
-#endif
-// bytes between the teams' activation slots: 144 = 128 + 16 puts eight
-// consecutive slots on eight distinct 16-byte bank groups
-constexpr int kStagedQStride = PQ2_STAGED_QSTRIDE;
-#ifndef PQ2_STAGED_PLAIN
-#define PQ2_STAGED_PLAIN 1
-#endif
-#ifndef PQ2_STAGED_XSPIN
-#define PQ2_STAGED_XSPIN 0
-#endif
-constexpr int kStagedXChunks = PQ2_STAGED_XCHUNKS;  // x copies (<= 15: barriers in 128 bytes)
 
 // group_codes_dot64 of two code rows against the same activations, the two
 // rows' DP4A chains interleaved (eight independent accumulators).
@@ -625,39 +593,27 @@ __device__ __forceinline__ void group_codes_dot64_x2(const uint32_t (&w0)[8], co
     r1 = ((b0 * 4 + b1) * 4 + b2) * 4 + b3;
 }
 
+// float(dot64) exactly (|dot64| < 2^22) by the 1.5 * 2^23 bit trick
+__device__ __forceinline__ float staged_dot_f32(int dot64) {
+    return __fsub_rn(__int_as_float(0x4B400000 + dot64), 12582912.0f);
+}
+
+__device__ __forceinline__ float staged_ws_f32(uint32_t bits) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+}
+
 __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-#if PQ2_STAGED_PLAIN
-    // shared memory through ordinary C++ accesses (the compiler may schedule
-    // them freely between the barriers and mbarrier waits, which order them)
-    const uint32_t sbase = pq2::smem_u32(smem);
-    auto SLDV4 = [&](uint32_t a) { return *reinterpret_cast<const uint4*>(smem + (a - sbase)); };
-    auto SLDU32 = [&](uint32_t a) { return *reinterpret_cast<const uint32_t*>(smem + (a - sbase)); };
-    auto SLDU16 = [&](uint32_t a) {
-        return static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(smem + (a - sbase)));
-    };
-    auto SLDF32 = [&](uint32_t a) { return *reinterpret_cast<const float*>(smem + (a - sbase)); };
-    auto SSTF32 = [&](uint32_t a, float v) { *reinterpret_cast<float*>(smem + (a - sbase)) = v; };
-#else
-    auto SLDV4 = [](uint32_t a) { return pq2::lds_v4(a); };
-    auto SLDU32 = [](uint32_t a) { return pq2::lds_u32(a); };
-    auto SLDU16 = [](uint32_t a) { return pq2::lds_u16(a); };
-    auto SLDF32 = [](uint32_t a) { return pq2::lds_f32(a); };
-    auto SSTF32 = [](uint32_t a, float v) { pq2::sts_f32(a, v); };
-#endif
     uint64_t* wbar = reinterpret_cast<uint64_t*>(smem);  // the weight slice has landed
-    uint64_t* xbar = wbar + 1;  // [kStagedXChunks]: chunk c of x has landed
+    uint64_t* xbar = wbar + 1;                           // all of x has landed
     const int n_begin = blockIdx.x * p.rows_per_cta;
     const int rows = min(p.N, n_begin + p.rows_per_cta) - n_begin;
     const int tid = threadIdx.x;
     const uint32_t rowb = p.codes_row_bytes;
     const uint32_t rs = rowb + kStagedPad;
-#if PQ2_STAGED_TRIGGER < 0
-    pq2::pdl_launch_dependents();
-#endif
     if (tid == 0) {
         pq2::mbar_init(wbar, 1);
-        for (int c = 0; c < kStagedXChunks; ++c) pq2::mbar_init(xbar + c, 1);
+        pq2::mbar_init(xbar, 1);
         pq2::fence_mbar_init();
     }
     __syncthreads();
@@ -687,26 +643,11 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
     // when x is final already.
     if (tid == 32) bulk_prefetch_l2(p.x, 2u * p.K);
     pq2::pdl_wait();
-#if PQ2_STAGED_TRIGGER == 0
     pq2::pdl_launch_dependents();
-#endif
     if (rows <= 0) return;
-    // x in chunks of whole groups, each on its own barrier; the first chunk a
-    // CTA requests rotates with the CTA index, so the CTAs' first requests
-    // spread over the chunks' L2 lines instead of all meeting on the first
-    const int gpc = (p.G + kStagedXChunks - 1) / kStagedXChunks;  // groups per chunk
     if (tid == 0) {
-        for (int i = 0; i < kStagedXChunks; ++i) {
-            const int c = static_cast<int>((blockIdx.x + i) % kStagedXChunks);
-            const int g0 = c * gpc, g1 = min(p.G, g0 + gpc);
-            if (g1 > g0) {
-                const uint32_t bytes = 256u * static_cast<uint32_t>(g1 - g0);
-                pq2::mbar_arrive_expect_tx(xbar + c, bytes);
-                pq2::bulk_g2s(smem + p.x_off + 256u * g0, p.x + 128 * g0, bytes, xbar + c);
-            } else {
-                pq2::mbar_arrive(xbar + c);  // an empty chunk: its phase completes now
-            }
-        }
+        pq2::mbar_arrive_expect_tx(xbar, 2u * p.K);
+        pq2::bulk_g2s(smem + p.x_off, p.x, 2u * p.K, xbar);
     }
 
     const int lane = tid & 31;
@@ -720,10 +661,9 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
     const int li = (team - gslot * tpg) * 8 + j;  // lane index within the group's lanes
     const int lstep = 8 * tpg;
     const bool tactive = gslot < gstep;
-    int8_t* qslot = reinterpret_cast<int8_t*>(smem + p.act_off) + team * kStagedQStride;
-    float* sslot = reinterpret_cast<float*>(smem + p.act_off + kStagedQStride * kStagedTeams) + team;
-    int32_t* tslot =
-        reinterpret_cast<int32_t*>(smem + p.act_off + (kStagedQStride + 4) * kStagedTeams) + team;
+    int8_t* qslot = reinterpret_cast<int8_t*>(smem + p.act_off) + team * kQStride;
+    float* sslot = reinterpret_cast<float*>(smem + p.act_off + kQStride * kStagedTeams) + team;
+    int32_t* tslot = reinterpret_cast<int32_t*>(smem + p.act_off + (kQStride + 4) * kStagedTeams) + team;
     const uint32_t qslot_s = pq2::smem_u32(qslot);
     const uint32_t codes_s = pq2::smem_u32(smem + p.ring_off);
     const uint32_t ws_s = pq2::smem_u32(smem + p.ws_off);
@@ -735,231 +675,97 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
         const int g = gslot + pass * gstep;
         const bool valid = tactive && g < p.G;
         const int gl = valid ? g : 0;
-        float s_reg;
-        int t_reg;
-        {
-            // the chunks of x holding this warp's groups (warp-uniform range)
-            const int cg = valid ? gl / gpc : kStagedXChunks;
-            const int cmin = __reduce_min_sync(0xffffffffu, cg);
-            const int cmax = __reduce_max_sync(0xffffffffu, valid ? cg : -1);
-            for (int c = cmin; c <= cmax && !failed; ++c)
-#if PQ2_STAGED_XSPIN
-                if (!pq2::mbar_spin_warp(xbar + c, 0, p.ctl)) failed = true;
-#else
-                if (!pq2::mbar_wait_warp(xbar + c, 0, p.ctl)) failed = true;
-#endif
-#if PQ2_STAGED_TRIGGER == 1
-            if (pass == 0) pq2::pdl_launch_dependents();
-#endif
-        }
+        if (pass == 0 && !pq2::mbar_wait_warp(xbar, 0, p.ctl)) failed = true;
+        float s_all;
+        int t_all;
         {
             const uint32_t src = x_s + gl * 256u + 32u * j;
-            const uint4 h[2] = {SLDV4(src), SLDV4(src + 16)};
-#if PQ2_STAGED_STREG
-            pq2::quantize_group8(h, j, valid, qslot, sslot, tslot, s_reg, t_reg);
-#else
-            pq2::quantize_group8(h, j, valid, qslot, sslot, tslot);
-#endif
+            const uint4 h[2] = {pq2::lds_v4(src), pq2::lds_v4(src + 16)};
+            pq2::quantize_group8(h, j, valid, qslot, sslot, tslot, s_all, t_all);
         }
         __syncwarp();
-#if PQ2_STAGED_TRIGGER == 2
-        if (pass == 0) pq2::pdl_launch_dependents();
-#endif
         uint32_t q[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-            const uint4 w = SLDV4(qslot_s + 16 * v);
+            const uint4 w = pq2::lds_v4(qslot_s + 16 * v);
             q[4 * v + 0] = w.x;
             q[4 * v + 1] = w.y;
             q[4 * v + 2] = w.z;
             q[4 * v + 3] = w.w;
         }
-#if PQ2_STAGED_STREG
-        // every lane of the team holds the group's s and t after quantising
-        const float s64 = s_reg * 0.015625f;  // exact scaling by 2^-6
-        const int t64 = -64 * t_reg;
-#else
-        const float s64 = SLDF32(pq2::smem_u32(sslot)) * 0.015625f;  // exact scaling by 2^-6
-        const int t64 = -64 * *tslot;
-#endif
+        const float s64 = s_all * 0.015625f;  // exact scaling by 2^-6
+        // -64 t enters each dot last (exact integers), so the dots need not
+        // wait for the team's reduction of t
+        const int t64 = -64 * t_all;
         // the weights were requested before the dependency wait; by now they
         // have usually landed (every warp waits on its own; a warp whose wait
         // runs out computes nothing and the CTA writes no y)
         if (pass == 0 && !failed) failed = !pq2::mbar_wait_warp(wbar, 0, p.ctl);
-#if PQ2_STAGED_TAIL == 1
-        // every lane of the group takes the same number of whole rows (li,
-        // li + lstep, ... for the full rounds); the rows left over go to the
-        // first warps below, one (row, group) per thread
-        const int full = rows / lstep;
-        const int nk = !failed && valid ? full : 0;
-#else
         const int nk = !failed && valid && li < rows ? (rows - li + lstep - 1) / lstep : 0;
-#endif
         const uint32_t cs = codes_s + li * rs + gl * 32;
         const uint32_t cstep = lstep * rs;
         const uint32_t wsa = ws_s + 2u * (li * p.G + gl);
         const uint32_t wstep = 2u * lstep * p.G;
-        // rows li, li + lstep, ... two at a time: the two rows' DP4A chains
-        // are independent, which keeps the ALU busy with few warps per
-        // scheduler (the second row of a lane's last pair may be absent)
-#if PQ2_STAGED_TAIL == 2
-        // pairs while two rows are left, then one row alone (a lane's odd
-        // last row costs one row's work, not a pair's)
+        // rows li, li + lstep, ... two at a time while two are left: the two
+        // rows' DP4A chains are independent, which keeps the ALU busy with few
+        // warps per scheduler; a lane's odd last row then costs one row's work
         int k = 0;
         for (; k + 1 < nk; k += 2) {
-            constexpr bool two = true;
-#else
-        for (int k = 0; k < nk; k += 2) {
-            const bool two = k + 1 < nk;
-#endif
             const uint32_t a = cs + k * cstep;
-            const uint4 c0 = SLDV4(a), c1 = SLDV4(a + 16);
-            const uint32_t wv0 = SLDU16(wsa + k * wstep);
-            uint4 d0 = make_uint4(0u, 0u, 0u, 0u), d1 = d0;
-            uint32_t wv1 = 0;
-            if (two) {
-                d0 = SLDV4(a + cstep);
-                d1 = SLDV4(a + cstep + 16);
-                wv1 = SLDU16(wsa + (k + 1) * wstep);
-            }
+            const uint4 c0 = pq2::lds_v4(a), c1 = pq2::lds_v4(a + 16);
+            const uint4 d0 = pq2::lds_v4(a + cstep), d1 = pq2::lds_v4(a + cstep + 16);
+            const uint32_t wv0 = pq2::lds_u16(wsa + k * wstep);
+            const uint32_t wv1 = pq2::lds_u16(wsa + (k + 1) * wstep);
             const uint32_t w0[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
             const uint32_t w1[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
             int dot0, dot1;
-#if PQ2_STAGED_STREG
             group_codes_dot64_x2(w0, w1, q, 0, dot0, dot1);
-            dot0 += t64;  // the bias added last (exact): the t reduction overlaps the dots
-            dot1 += t64;
-#else
-            group_codes_dot64_x2(w0, w1, q, t64, dot0, dot1);
-#endif
-            // float(dot64) exactly (|dot64| < 2^22) by the 1.5 * 2^23 bit trick
-            const float f0 = __fsub_rn(__int_as_float(0x4B400000 + dot0), 12582912.0f);
-            const float f1 = __fsub_rn(__int_as_float(0x4B400000 + dot1), 12582912.0f);
-            const float ws0 = __half2float(__ushort_as_half(static_cast<unsigned short>(wv0)));
-            const float ws1 = __half2float(__ushort_as_half(static_cast<unsigned short>(wv1)));
             const int row = li + k * lstep;
-            SSTF32(red_s + 4u * (row * rstr + g), f0 * s64 * ws0);
-            if (two) SSTF32(red_s + 4u * ((row + lstep) * rstr + g), f1 * s64 * ws1);
+            pq2::sts_f32(red_s + 4u * (row * rstr + g), staged_dot_f32(dot0 + t64) * s64 * staged_ws_f32(wv0));
+            pq2::sts_f32(red_s + 4u * ((row + lstep) * rstr + g),
+                         staged_dot_f32(dot1 + t64) * s64 * staged_ws_f32(wv1));
         }
-#if PQ2_STAGED_TAIL == 2
         if (k < nk) {
             const uint32_t a = cs + k * cstep;
-            const uint4 c0 = SLDV4(a), c1 = SLDV4(a + 16);
-            const uint32_t wv0 = SLDU16(wsa + k * wstep);
+            const uint4 c0 = pq2::lds_v4(a), c1 = pq2::lds_v4(a + 16);
+            const uint32_t wv0 = pq2::lds_u16(wsa + k * wstep);
             const uint32_t w0[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#if PQ2_STAGED_STREG
             const int dot0 = pq2::group_codes_dot64(w0, q, 0) + t64;
-#else
-            const int dot0 = pq2::group_codes_dot64(w0, q, t64);
-#endif
-            const float f0 = __fsub_rn(__int_as_float(0x4B400000 + dot0), 12582912.0f);
-            const float ws0 = __half2float(__ushort_as_half(static_cast<unsigned short>(wv0)));
-            SSTF32(red_s + 4u * ((li + k * lstep) * rstr + g), f0 * s64 * ws0);
+            pq2::sts_f32(red_s + 4u * ((li + k * lstep) * rstr + g),
+                         staged_dot_f32(dot0) * s64 * staged_ws_f32(wv0));
         }
-#endif
-#if PQ2_STAGED_TAIL == 1
-        // the rows left after the full rounds (fewer than lstep per group):
-        // one (row, group) term per thread, packed into the first warps so
-        // no warp runs a round for a few lanes; each reads the group's
-        // activations from the slot of the group's first team
-        const int tail = rows - full * lstep;  // uniform over the CTA
-        if (tail > 0) {
-            pq2::named_bar_sync(1, kStagedThreads);  // every team's slot is written
-            const int gpass = min(gstep, p.G - pass * gstep);
-            const int ntask = tail * gpass;
-            const uint32_t act_s = pq2::smem_u32(smem + p.act_off);
-            for (int t = tid; t < ntask && !failed; t += kStagedThreads) {
-                const int trow = t / gpass;
-                const int tslot_i = t - trow * gpass;  // group slot in this pass
-                const int gg = tslot_i + pass * gstep;
-                const int row = full * lstep + trow;
-                const int team0 = tslot_i * tpg;
-                const uint32_t qs = act_s + team0 * kStagedQStride;
-                uint32_t qt[32];
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                    const uint4 w = SLDV4(qs + 16 * v);
-                    qt[4 * v + 0] = w.x;
-                    qt[4 * v + 1] = w.y;
-                    qt[4 * v + 2] = w.z;
-                    qt[4 * v + 3] = w.w;
-                }
-                const float st64 =
-                    SLDF32(act_s + kStagedQStride * kStagedTeams + 4 * team0) * 0.015625f;
-                const int tt64 = -64 * static_cast<int>(SLDU32(
-                                           act_s + (kStagedQStride + 4) * kStagedTeams + 4 * team0));
-                const uint32_t a = codes_s + row * rs + gg * 32;
-                const uint4 c0 = SLDV4(a), c1 = SLDV4(a + 16);
-                const uint32_t w0[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                const int dot = pq2::group_codes_dot64(w0, qt, tt64);
-                const float f = __fsub_rn(__int_as_float(0x4B400000 + dot), 12582912.0f);
-                const float wsv = __half2float(__ushort_as_half(
-                    static_cast<unsigned short>(SLDU16(ws_s + 2u * (row * p.G + gg)))));
-                SSTF32(red_s + 4u * (row * rstr + gg), f * st64 * wsv);
-            }
-            if (pass + 1 < passes) pq2::named_bar_sync(1, kStagedThreads);  // slots reused
-        }
-#endif
         __syncwarp();  // the slot is rewritten by the next pass
     }
     if (__syncthreads_or(failed)) {
         if (tid == 0) {  // no copy in flight at exit
             pq2::mbar_wait_bounded(wbar, 0, p.ctl);
-            for (int c = 0; c < kStagedXChunks; ++c) pq2::mbar_wait_bounded(xbar + c, 0, p.ctl);
+            pq2::mbar_wait_bounded(xbar, 0, p.ctl);
         }
         return;
     }
-#if PQ2_STAGED_ROWSUM
-    // row sums, one thread per row, in the order of the other variants: the
-    // partial sum s (s = 0..7) adds the terms s, s + 8, ... from zero, then
-    // the partials combine as ((p0 + p4) + (p2 + p6)) + ((p1 + p5) + (p3 + p7)),
-    // which is what their 8-lane butterfly (xor 4, 2, 1) leaves in lane 0
-    for (int r = tid; r < rows; r += kStagedThreads) {
-        const uint32_t rowa = red_s + 4u * (r * rstr);
-        float ps[8];
-#pragma unroll
-        for (int sub = 0; sub < 8; ++sub) ps[sub] = 0.0f;
-        for (int c0 = 0; c0 < p.G; c0 += 8) {
-            float v[8];
-#pragma unroll
-            for (int sub = 0; sub < 8; ++sub)
-                v[sub] = c0 + sub < p.G ? SLDF32(rowa + 4u * (c0 + sub)) : 0.0f;
-#pragma unroll
-            for (int sub = 0; sub < 8; ++sub)
-                if (c0 + sub < p.G) ps[sub] += v[sub];
-        }
-        p.y[n_begin + r] = ((ps[0] + ps[4]) + (ps[2] + ps[6])) + ((ps[1] + ps[5]) + (ps[3] + ps[7]));
-    }
-#else
-    // row sums: 8 lanes per row, each over a fixed stride of the row's terms,
-    // then a fixed 3-step butterfly (the same order as the other variants)
+    // row sums: 8 lanes per row, each over a fixed stride of the row's terms
+    // (added in that order, the loads in flight together), then a fixed
+    // 3-step butterfly (the same order as the other variants)
     const int sub = lane & 7;
     constexpr int nwarps = kStagedThreads / 32;
     for (int rb = warp * 4; rb < rows; rb += nwarps * 4) {
         const int r = rb + (lane >> 3);
         float sum = 0.0f;
-#if PQ2_STAGED_SUM_UNROLL
-        // terms sub, sub + 8, ... added in that order; eight loads in flight
         if (r < rows)
             for (int c0 = sub; c0 < p.G; c0 += 64) {
                 float v[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    v[u] = c0 + 8 * u < p.G ? SLDF32(red_s + 4u * (r * rstr + c0 + 8 * u)) : 0.0f;
+                    v[u] = c0 + 8 * u < p.G ? pq2::lds_f32(red_s + 4u * (r * rstr + c0 + 8 * u)) : 0.0f;
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                     if (c0 + 8 * u < p.G) sum += v[u];
             }
-#else
-        if (r < rows)
-            for (int c = sub; c < p.G; c += 8) sum += SLDF32(red_s + 4u * (r * rstr + c));
-#endif
         sum += __shfl_xor_sync(0xffffffffu, sum, 4);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         if (sub == 0 && r < rows) p.y[n_begin + r] = sum;
     }
-#endif
 }
 
 // Shared memory of the staged variant: barrier | codes rows (padded) | weight
@@ -971,7 +777,7 @@ size_t staged_layout(GemvParams& p) {
     p.ws_off = static_cast<uint32_t>((p.ring_off + codes + 127) & ~static_cast<size_t>(127));
     const size_t wsz = rows * p.G * 2;
     p.act_off = static_cast<uint32_t>((p.ws_off + wsz + 127) & ~static_cast<size_t>(127));
-    const size_t act = static_cast<size_t>(kStagedQStride + 8) * kStagedTeams;
+    const size_t act = static_cast<size_t>(kQStride + 8) * kStagedTeams;
     p.red_off = static_cast<uint32_t>((p.act_off + act + 127) & ~static_cast<size_t>(127));
     p.x_off = static_cast<uint32_t>((p.red_off + rows * (p.G + 1) * 4 + 127) & ~static_cast<size_t>(127));
     const size_t total = p.x_off + 2 * static_cast<size_t>(p.K);
@@ -983,10 +789,6 @@ cudaError_t launch_staged(const GemvParams& p, int grid, size_t smem, cudaStream
     static pq2h::SmemLimit lim;
     cudaError_t e = pq2h::ensure_smem(lim, gemv_staged_kernel, smem);
     if (e != cudaSuccess) return e;
-#if PQ2_STAGED_CARVEOUT
-    e = cudaFuncSetAttribute(gemv_staged_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-#endif
     return pq2h::launch(gemv_staged_kernel, dim3(grid), dim3(kStagedThreads), smem, st, true, p);
 }
 
