@@ -748,10 +748,25 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
     // 3-step butterfly (the same order as the other variants)
     const int sub = lane & 7;
     constexpr int nwarps = kStagedThreads / 32;
+    // with G a multiple of 8 (at most 64) every lane sums G / 8 terms:
+    // uniform trip counts, ordinary loads the compiler issues together
+    const float* redp = reinterpret_cast<const float*>(smem + p.red_off);
+    const int nper = p.G >> 3;
+    const bool even8 = (p.G & 7) == 0 && nper <= 8;
     for (int rb = warp * 4; rb < rows; rb += nwarps * 4) {
         const int r = rb + (lane >> 3);
         float sum = 0.0f;
-        if (r < rows)
+        if (even8) {
+            if (r < rows) {
+                const float* rp = redp + r * rstr + sub;
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = u < nper ? rp[8 * u] : 0.0f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (u < nper) sum += v[u];
+            }
+        } else if (r < rows) {
             for (int c0 = sub; c0 < p.G; c0 += 64) {
                 float v[8];
 #pragma unroll
@@ -761,6 +776,7 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
                 for (int u = 0; u < 8; ++u)
                     if (c0 + 8 * u < p.G) sum += v[u];
             }
+        }
         sum += __shfl_xor_sync(0xffffffffu, sum, 4);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
