@@ -104,17 +104,15 @@ def _check(status: int, where: str):
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream  # an int: ctypes passes it as the void* argument
 
 
 def _ptr(t):
     if t is None:
         return None
-    if not t.is_cuda:
-        raise ValueError("expected a CUDA tensor")
-    if not t.is_contiguous():
-        raise ValueError("expected a contiguous tensor")
-    return ctypes.c_void_p(t.data_ptr())
+    if not (t.is_cuda and t.is_contiguous()):
+        raise ValueError("expected a contiguous CUDA tensor")
+    return t.data_ptr()
 
 
 def _dtype(t, dt, name):
