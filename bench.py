@@ -369,15 +369,16 @@ def build_layers(args, layer, R, device, name=""):
 
 def weight_flags(pq2, args):
     """The step's weights are uploaded once and never written again, so the
-    calls may declare them static (PQ2_WEIGHTS_STATIC) unless --weights default."""
+    calls may declare them static (PQ2_WEIGHTS_STATIC: pq2_matmul_ex for M = 1,
+    pq2_gemm_small_ex, pq2_gemm_bf16_splitk) unless --weights default."""
     return pq2.PQ2_WEIGHTS_STATIC if args.weights == "static" else 0
 
 
-def run_matmul(pq2, p):
+def run_matmul(pq2, p, flags=0):
     if p["op"] == pq2.PQ2_OP_GEMV:
         pq2.pq2_gemv(p["qp"], p["S"], p["T"], p["codes"], p["ws"], p["y"])
     elif p["op"] == pq2.PQ2_OP_SMALL:
-        pq2.pq2_gemm_small(p["qp"], p["S"], p["T"], p["codes"], p["ws"], p["y"], p["wsp"])
+        pq2.pq2_gemm_small_ex(p["qp"], p["S"], p["T"], p["codes"], p["ws"], p["y"], flags, p["wsp"])
     else:
         pq2.pq2_gemm_prefill(p["qp"], p["S"], p["T"], p["codes"], p["ws"], p["y"], p["wsp"])
 
@@ -400,7 +401,7 @@ def step_fn(pq2, layers, matmul_only=False, flags=0):
                     continue
                 if not matmul_only:
                     pq2.pq2_quantize_act(p["x"], p["qp"], p["S"], p["T"])
-                run_matmul(pq2, p)
+                run_matmul(pq2, p, flags)
     return fn
 
 
@@ -624,7 +625,7 @@ def measure(args, wl, rank, world, dist, steps, warmup, target_ms, e2e_passes, f
                           f"measurement)"),
                    "graph": graph,
                    "arith": arith,
-                   "weights": ("static: M = 1 and bf16 calls pass PQ2_WEIGHTS_STATIC (weights "
+                   "weights": ("static: M = 1, small-batch and bf16 calls pass PQ2_WEIGHTS_STATIC (weights "
                                "uploaded once; each call may read them before the preceding call "
                                "ends)"
                                if args.weights == "static" else "default ordering"),

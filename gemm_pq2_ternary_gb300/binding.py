@@ -54,6 +54,7 @@ SIGNATURES = {
     "pq2_pack_weights": ([_P, _P, _I64, _I64, _P, _P, _P], _I),
     "pq2_gemv": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _P], _I),
     "pq2_gemm_small": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _I),
+    "pq2_gemm_small_ex": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P, _SZ, _P], _I),
     "pq2_gemm_prefill": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _I),
     "pq2_matmul": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _I),
     "pq2_matmul_ex": ([_P, _P, _P, _P, _I64, _I64, _I64, _U32, _P, _SZ, _P], _I),
@@ -178,6 +179,13 @@ def pq2_gemm_small(qp, S, T, codes, ws, y, workspace=None, stream=None):
     wp, wb = _ws(workspace)
     _check(_lib.pq2_gemm_small(_ptr(qp), _ptr(S), _ptr(T), _ptr(codes), _ptr(ws), _ptr(y),
                                M, N, K, wp, wb, _stream(stream)), "pq2_gemm_small")
+
+
+def pq2_gemm_small_ex(qp, S, T, codes, ws, y, flags, workspace=None, stream=None):
+    M, N, K = _mm_shapes(qp, codes)
+    wp, wb = _ws(workspace)
+    _check(_lib.pq2_gemm_small_ex(_ptr(qp), _ptr(S), _ptr(T), _ptr(codes), _ptr(ws), _ptr(y),
+                                  M, N, K, flags, wp, wb, _stream(stream)), "pq2_gemm_small_ex")
 
 
 def pq2_gemm_prefill(qp, S, T, codes, ws, y, workspace=None, stream=None):

@@ -299,10 +299,10 @@ size_t pq2_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
     }
 }
 
-pq2_status pq2_gemm_small(const int8_t* qp, const float* S, const int32_t* T,
-                          const uint8_t* codes, const void* ws_f16, float* y, int64_t M,
-                          int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
-                          void* stream) {
+// pq2_gemm_small; weights_static: PQ2_WEIGHTS_STATIC of pq2_matmul_ex
+static pq2_status gemm_small(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
+                      const void* ws_f16, float* y, int64_t M, int64_t N, int64_t K,
+                      void* workspace, size_t workspace_bytes, void* stream, bool weights_static) {
     pq2_status s = check_mm(qp, S, T, codes, ws_f16, y, M, N, K);
     if (s != PQ2_OK) return s;
     if (!S || !ws_f16) return PQ2_ERR_INVALID_ARG;
@@ -316,10 +316,27 @@ pq2_status pq2_gemm_small(const int8_t* qp, const float* S, const int32_t* T,
         return cuda_status(pq2h::launch_gemv_multi(qp, S, T, codes,
                                                    static_cast<const __half*>(ws_f16), y, nullptr,
                                                    M, N, K, static_cast<cudaStream_t>(stream),
-                                                   c.dev));
+                                                   c.dev, weights_static));
     return cuda_status(pq2h::launch_small_tc(qp, S, T, codes, static_cast<const __half*>(ws_f16), y,
                                           nullptr, M, N, K, workspace,
                                           static_cast<cudaStream_t>(stream), c.ctl, c.dev));
+}
+
+pq2_status pq2_gemm_small(const int8_t* qp, const float* S, const int32_t* T,
+                          const uint8_t* codes, const void* ws_f16, float* y, int64_t M,
+                          int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    return gemm_small(qp, S, T, codes, ws_f16, y, M, N, K, workspace, workspace_bytes, stream,
+                      false);
+}
+
+pq2_status pq2_gemm_small_ex(const int8_t* qp, const float* S, const int32_t* T,
+                             const uint8_t* codes, const void* ws_f16, float* y, int64_t M,
+                             int64_t N, int64_t K, uint32_t flags, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    if (flags & ~PQ2_WEIGHTS_STATIC) return PQ2_ERR_INVALID_ARG;
+    return gemm_small(qp, S, T, codes, ws_f16, y, M, N, K, workspace, workspace_bytes, stream,
+                      (flags & PQ2_WEIGHTS_STATIC) != 0);
 }
 
 pq2_status pq2_gemm_prefill(const int8_t* qp, const float* S, const int32_t* T,
@@ -383,8 +400,8 @@ pq2_status pq2_matmul_ex(const void* x_f16, const uint8_t* codes, const void* ws
     if (s != PQ2_OK) return s;
     if (M == 1) return pq2_gemv(qp, S, T, codes, ws_f16, y, N, K, stream);
     if (M <= 16)
-        return pq2_gemm_small(qp, S, T, codes, ws_f16, y, M, N, K, rest ? w : nullptr, rest,
-                              stream);
+        return gemm_small(qp, S, T, codes, ws_f16, y, M, N, K, rest ? w : nullptr, rest, stream,
+                          (flags & PQ2_WEIGHTS_STATIC) != 0);
     return pq2_gemm_prefill(qp, S, T, codes, ws_f16, y, M, N, K, rest ? w : nullptr, rest,
                             stream);
 }
@@ -457,7 +474,7 @@ pq2_status pq2_group_dots(int op, const int8_t* qp, const int32_t* T, const uint
     if (op == PQ2_OP_SMALL) {
         if (pq2h::gemv_multi_supported(M, N, K, c.dev.num_sms))
             return cuda_status(pq2h::launch_gemv_multi(qp, nullptr, T, codes, nullptr, nullptr,
-                                                       dots, M, N, K, st, c.dev));
+                                                       dots, M, N, K, st, c.dev, false));
         return cuda_status(pq2h::launch_small_tc(qp, nullptr, T, codes, nullptr, nullptr, dots, M, N,
                                               K, workspace, st, c.ctl, c.dev));
     }

@@ -83,9 +83,6 @@ struct GemvParams {
     pq2::DevCtl ctl;
 };
 
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 
 // One CTA per SM; many consumer warps hide the shared-memory and DP4A
@@ -409,7 +406,7 @@ __global__ void __launch_bounds__(kDirectConsumers + 32, 1) gemv_direct_kernel(c
     // kernel: wait for it before reading any of them.  (An L2 prefetch of x
     // before the wait is only a hint: a write by that kernel still lands in
     // L2.)
-    if (FUSED && tid == p.TC) bulk_prefetch_l2(p.x, 2u * p.K);
+    if (FUSED && tid == p.TC) pq2::bulk_prefetch_l2(p.x, 2u * p.K);
     pq2::pdl_wait();
     pq2::pdl_launch_dependents();
     if (rows <= 0) return;
@@ -641,7 +638,7 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
     // An L2 prefetch of it before the wait is only a hint (a write by that
     // kernel still lands in L2), and takes the round trip to HBM off the path
     // when x is final already.
-    if (tid == 32) bulk_prefetch_l2(p.x, 2u * p.K);
+    if (tid == 32) pq2::bulk_prefetch_l2(p.x, 2u * p.K);
     pq2::pdl_wait();
     pq2::pdl_launch_dependents();
     if (rows <= 0) return;

@@ -74,7 +74,7 @@ bool gemv_multi_supported(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_gemv_multi(const int8_t* qp, const float* S, const int32_t* T,
                               const uint8_t* codes, const __half* ws, float* y, int32_t* dots,
                               int64_t M, int64_t N, int64_t K, cudaStream_t st,
-                              const DeviceInfo& dev);
+                              const DeviceInfo& dev, bool weights_static);
 
 cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
                          const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,

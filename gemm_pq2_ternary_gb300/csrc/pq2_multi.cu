@@ -17,6 +17,10 @@
 // are summed in the fixed order of the M = 1 kernels (8 lanes over a stride,
 // then a 3-step butterfly), so each token's y equals pq2_gemv on that token
 // bit for bit.
+// Weights declared static (PQ2_WEIGHTS_STATIC) are requested before the
+// dependency wait: the first look-ahead rows into registers and, for slices
+// up to 64 KB, an L2 prefetch of the CTA's whole slice of code rows and
+// weight scales.  The activations are still read only after the wait.
 
 #include "pq2_internal.h"
 
@@ -25,6 +29,7 @@ namespace {
 constexpr int kMultiConsumers = 480;     // consumer threads at most
 constexpr int kMultiLookahead = 4;       // rows of code loads in flight per thread
 constexpr size_t kMultiMaxSmem = 160 * 1024;
+constexpr uint32_t kMultiPrefetchMax = 64 * 1024;  // bytes of a CTA's code slice
 
 struct MultiParams {
     const int8_t* qp;       // [M][K] plane order
@@ -42,7 +47,7 @@ struct MultiParams {
     uint32_t codes_row_bytes;
 };
 
-template <int MT, bool DOTS>
+template <int MT, bool DOTS, bool STATIC>
 __global__ void __launch_bounds__(kMultiConsumers, 1) gemv_multi_kernel(const MultiParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     float* red = reinterpret_cast<float*>(smem);  // [rows][MT][GT] group terms
@@ -53,10 +58,24 @@ __global__ void __launch_bounds__(kMultiConsumers, 1) gemv_multi_kernel(const Mu
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int nwarps = p.TC >> 5;
-    // codes and activations may come from the preceding kernel
-    pq2::pdl_wait();
-    pq2::pdl_launch_dependents();
-    if (rows <= 0) return;
+    // the slice's L2 prefetch only where it is small: a large one competes
+    // with the preceding call's own weight stream (measured slower at
+    // 5120 -> 17408, 148 KB per CTA; faster at 6144 -> 5120, 52 KB)
+    if (STATIC && rows > 0 && tid == 0 &&
+        static_cast<uint32_t>(rows) * p.codes_row_bytes <= kMultiPrefetchMax) {
+        pq2::bulk_prefetch_l2(p.codes + static_cast<size_t>(n_begin) * p.codes_row_bytes,
+                              static_cast<uint32_t>(rows) * p.codes_row_bytes);
+        if ((p.G & 7) == 0)  // 16-byte aligned slices of the scales
+            pq2::bulk_prefetch_l2(p.ws + static_cast<size_t>(n_begin) * p.G,
+                                  static_cast<uint32_t>(rows) * p.G * 2u);
+    }
+    // codes and activations may come from the preceding kernel (the codes not
+    // when declared static: their first rows are requested below, before the wait)
+    if (!STATIC) {
+        pq2::pdl_wait();
+        pq2::pdl_launch_dependents();
+        if (rows <= 0) return;
+    }
 
     const int mt = tid % MT;
     const int u = tid / MT;
@@ -88,6 +107,11 @@ __global__ void __launch_bounds__(kMultiConsumers, 1) gemv_multi_kernel(const Mu
             c1[j] = pq2::ld_nc_v4(cw + 16 * (hswap ^ 1));
             if (!DOTS) wr[j] = wbase[j * wstep];
         }
+    }
+    if (STATIC) {
+        pq2::pdl_wait();
+        pq2::pdl_launch_dependents();
+        if (rows <= 0) return;
     }
 
     // this thread's token: its group's activations (zero past M)
@@ -160,9 +184,9 @@ __global__ void __launch_bounds__(kMultiConsumers, 1) gemv_multi_kernel(const Mu
     }
 }
 
-template <int MT, bool DOTS>
+template <int MT, bool DOTS, bool STATIC = false>
 cudaError_t launch_mt(const MultiParams& p, int grid, size_t smem, cudaStream_t st) {
-    auto kern = gemv_multi_kernel<MT, DOTS>;
+    auto kern = gemv_multi_kernel<MT, DOTS, STATIC>;
     static pq2h::SmemLimit lim;
     cudaError_t e = pq2h::ensure_smem(lim, kern, smem);
     if (e != cudaSuccess) return e;
@@ -199,7 +223,7 @@ bool gemv_multi_supported(int64_t M, int64_t N, int64_t K, int num_sms) {
 cudaError_t launch_gemv_multi(const int8_t* qp, const float* S, const int32_t* T,
                               const uint8_t* codes, const __half* ws, float* y, int32_t* dots,
                               int64_t M, int64_t N, int64_t K, cudaStream_t st,
-                              const DeviceInfo& dev) {
+                              const DeviceInfo& dev, bool weights_static) {
     if (!gemv_multi_supported(M, N, K, dev.num_sms)) return cudaErrorInvalidValue;
     const int mt = tokens_per_pass(M);
     MultiParams p = {};
@@ -225,6 +249,11 @@ cudaError_t launch_gemv_multi(const int8_t* qp, const float* S, const int32_t* T
         if (mt == 2) return launch_mt<2, true>(p, grid, smem, st);
         if (mt == 4) return launch_mt<4, true>(p, grid, smem, st);
         return launch_mt<8, true>(p, grid, smem, st);
+    }
+    if (weights_static) {
+        if (mt == 2) return launch_mt<2, false, true>(p, grid, smem, st);
+        if (mt == 4) return launch_mt<4, false, true>(p, grid, smem, st);
+        return launch_mt<8, false, true>(p, grid, smem, st);
     }
     if (mt == 2) return launch_mt<2, false>(p, grid, smem, st);
     if (mt == 4) return launch_mt<4, false>(p, grid, smem, st);

@@ -174,6 +174,22 @@ pq2_status pq2_gemm_small(const int8_t* qp, const float* S, const int32_t* T,
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pq2_gemm_small_ex -- pq2_gemm_small with a flags word: 0, or
+ *   PQ2_WEIGHTS_STATIC (defined below, as for pq2_matmul_ex): the caller
+ *   promises that codes and ws_f16 are not written by any operation enqueued
+ *   on `stream` before this call that may still be running when it starts.
+ *   The DP4A kernel for 2 to 4 token rows then requests its weights (an L2
+ *   prefetch of its slice and its first rows) before the preceding kernel
+ *   has finished; qp, S and T are still read only after it.  y is
+ *   bit-identical to pq2_gemm_small.  Other bits give PQ2_ERR_INVALID_ARG;
+ *   the tensor-core path ignores the flag.
+ */
+pq2_status pq2_gemm_small_ex(const int8_t* qp, const float* S, const int32_t* T,
+                             const uint8_t* codes, const void* ws_f16, float* y, int64_t M,
+                             int64_t N, int64_t K, uint32_t flags, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
  * pq2_gemm_prefill -- prompt processing, any M >= 1 (built for M > 16).
  *   [P1] "Prompt processing: check configuration and launch costs" (2-D
  *   output tiles, per-group integer products and the same per-group
@@ -215,12 +231,12 @@ pq2_status pq2_matmul(const void* x_f16, const uint8_t* codes, const void* ws_f1
  *   PQ2_WEIGHTS_STATIC: the caller promises that codes and ws_f16 are not
  *     written by any operation enqueued on `stream` before this call that may
  *     still be running when it starts (typically: weights packed or copied
- *     once, then many calls).  The M == 1 fused kernel may then read them
- *     before the preceding kernel on the stream has finished (programmatic
- *     dependent launch).  x_f16 is still read only after that kernel is
- *     done.  If the promise is broken, y is undefined.  Results are
- *     bit-identical to pq2_matmul.  Paths other than the M == 1 fused one
- *     ignore the flag.
+ *     once, then many calls).  The M == 1 fused kernel and the DP4A kernel
+ *     for a few tokens (2 <= M <= 4 where the shape allows) may then read
+ *     them before the preceding kernel on the stream has finished
+ *     (programmatic dependent launch).  x_f16 is still read only after that
+ *     kernel is done.  If the promise is broken, y is undefined.  Results
+ *     are bit-identical to pq2_matmul.  The other paths ignore the flag.
  *   Other arguments, workspace and errors as pq2_matmul.
  */
 pq2_status pq2_matmul_ex(const void* x_f16, const uint8_t* codes, const void* ws_f16, float* y,

@@ -152,3 +152,56 @@ def test_static_weights_fall_back_where_slices_are_too_large(prob):
     torch.cuda.synchronize()
     assert pq2.pq2_last_device_error() == pq2.PQ2_OK
     assert torch.equal(y0, y1)
+
+
+FEW_TOKEN_STATIC = [inputs.Problem(f"static_m{M}_k{K}_n{N}", M, K, N, "p343", "outliers", 90 + M)
+                    for M in (2, 3, 4) for (K, N) in inputs.SMALL_SHAPES]
+
+
+@pytest.mark.parametrize("prob", FEW_TOKEN_STATIC, ids=lambda p: p.name)
+def test_static_weights_few_tokens_match_default_path(prob):
+    """2 to 4 tokens: with PQ2_WEIGHTS_STATIC the DP4A kernel requests its
+    weights before the dependency wait; y is bit-identical to pq2_matmul."""
+    from gemm_pq2_ternary_gb300 import binding as pq2
+    from gemm_pq2_ternary_gb300.binding import alloc_workspace, PQ2_OP_MATMUL
+    tern, ws, x = inputs.generate(prob)
+    codes, ws_d = pq2.pack(torch.from_numpy(tern).cuda(), torch.from_numpy(ws).cuda())
+    xd = torch.from_numpy(x).cuda()
+    wsb = alloc_workspace(PQ2_OP_MATMUL, prob.M, prob.N, prob.K)
+    torch.cuda.synchronize()
+    y0 = torch.full((prob.M, prob.N), float("nan"), device="cuda")
+    y1 = torch.full((prob.M, prob.N), float("nan"), device="cuda")
+    pq2.pq2_matmul(xd, codes, ws_d, y0, wsb)
+    pq2.pq2_matmul_ex(xd, codes, ws_d, y1, pq2.PQ2_WEIGHTS_STATIC, wsb)
+    torch.cuda.synchronize()
+    assert pq2.pq2_last_device_error() == pq2.PQ2_OK
+    assert torch.equal(y0, y1)
+
+
+def test_static_weights_few_tokens_back_to_back():
+    """Static-weight calls of 2 and 4 tokens queued back to back, each x
+    written by the kernel right before its call: y equals pq2_matmul's."""
+    from gemm_pq2_ternary_gb300 import binding as pq2
+    from gemm_pq2_ternary_gb300.binding import alloc_workspace, PQ2_OP_MATMUL
+    probs = [inputs.Problem(f"fchain{i}", 2 if i % 2 == 0 else 4, 6144, 5120, "p343", "outliers", 95 + i)
+             for i in range(4)]
+    data = [inputs.generate(p) for p in probs]
+    dev = [pq2.pack(torch.from_numpy(t).cuda(), torch.from_numpy(w).cuda()) for t, w, _ in data]
+    xs = [torch.from_numpy(x).cuda() for _, _, x in data]
+    xs_live = [torch.empty_like(x) for x in xs]
+    wsbs = [alloc_workspace(PQ2_OP_MATMUL, p.M, p.N, p.K) for p in probs]
+    torch.cuda.synchronize()
+    want = []
+    for (codes, ws_d), x, p, wsb in zip(dev, xs, probs, wsbs):
+        y = torch.empty((p.M, p.N), device="cuda")
+        pq2.pq2_matmul(x, codes, ws_d, y, wsb)
+        want.append(y)
+    torch.cuda.synchronize()
+    outs = [torch.full((p.M, p.N), float("nan"), device="cuda") for p in probs]
+    for i, ((codes, ws_d), p) in enumerate(zip(dev, probs)):
+        xs_live[i].copy_(xs[i])
+        pq2.pq2_matmul_ex(xs_live[i], codes, ws_d, outs[i], pq2.PQ2_WEIGHTS_STATIC, wsbs[i])
+    torch.cuda.synchronize()
+    assert pq2.pq2_last_device_error() == pq2.PQ2_OK
+    for a, b in zip(outs, want):
+        assert torch.equal(a, b)
