@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_objs")
 LIB = os.path.join(HERE, "libpq2.so")
 SOURCES = ["pq2_api.cu", "pq2_quant.cu", "pq2_gemv.cu", "pq2_small.cu", "pq2_tile.cu",
-           "pq2_prefill.cu", "pq2_noalloc.cu", "pq2_bf16.cu", "pq2_multi.cu"]
+           "pq2_prefill.cu", "pq2_noalloc.cu", "pq2_bf16.cu", "pq2_multi.cu", "pq2_wtile.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v"]

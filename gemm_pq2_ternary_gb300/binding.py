@@ -38,9 +38,11 @@ PQ2_VARIANT_GEMV_STAGED = 3
 PQ2_VARIANT_SMALL_DP4A = 1
 PQ2_VARIANT_SMALL_TC = 2
 PQ2_VARIANT_SMALL_TILE = 3
+PQ2_VARIANT_SMALL_WTILE = 4
 PQ2_VARIANT_PREFILL_128 = 1
 PQ2_VARIANT_PREFILL_WIDE = 2
 PQ2_VARIANT_PREFILL_TILE = 3
+PQ2_VARIANT_PREFILL_WTILE = 4
 
 SIZE_MAX = ctypes.c_size_t(-1).value
 

@@ -165,8 +165,8 @@ pq2_status pq2_debug_skip_stage(int stage) {
 pq2_status pq2_debug_force_kernel(int op, int variant) {
     int max_variant = -1;
     if (op == PQ2_OP_GEMV) max_variant = PQ2_VARIANT_GEMV_STAGED;
-    if (op == PQ2_OP_SMALL) max_variant = PQ2_VARIANT_SMALL_TILE;
-    if (op == PQ2_OP_PREFILL) max_variant = PQ2_VARIANT_PREFILL_TILE;
+    if (op == PQ2_OP_SMALL) max_variant = PQ2_VARIANT_SMALL_WTILE;
+    if (op == PQ2_OP_PREFILL) max_variant = PQ2_VARIANT_PREFILL_WTILE;
     if (variant < 0 || variant > max_variant) return PQ2_ERR_INVALID_ARG;
     g_force[op].store(variant);
     return PQ2_OK;

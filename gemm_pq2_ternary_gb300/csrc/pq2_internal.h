@@ -92,6 +92,17 @@ cudaError_t launch_tile(const int8_t* qp, const float* S, const int32_t* T, cons
                         void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                         const DeviceInfo& dev);
 
+// 1 <= M <= kTileMaxM: the weights-wide token-tile kernel (pq2_wtile.cu):
+// 256 expanded weight rows per MMA, the tokens' hi and lo parts as the
+// 128-row operand (16, 32 or 64 tokens), split-K partial sums reduced in a
+// fixed order.
+size_t wtile_workspace_bytes(int64_t M, int64_t N, int64_t K);
+size_t wtile_scratch_bytes(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_wtile(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
+                         const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
+                         int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
+                         const DeviceInfo& dev);
+
 // Back-to-back tcgen05 e4m3 MMAs (M = 128, N = n, K = 32) on every SM:
 // cycles[sm] = clock cycles for `iters` of them (pq2_debug_mma_rate).
 cudaError_t launch_mma_rate(int n, int iters, unsigned long long* cycles, cudaStream_t st,

@@ -906,7 +906,9 @@ namespace pq2h {
 size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     const WsLayout l = ws_layout(M, N, K);
     if (M > kTileMaxM) return l.total;
-    const size_t t = tile_workspace_bytes(M, N, K);
+    size_t t = tile_workspace_bytes(M, N, K);
+    const size_t u = wtile_workspace_bytes(M, N, K);
+    if (u > t) t = u;
     return t > l.total ? t : l.total;
 }
 
@@ -919,6 +921,10 @@ cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, c
     // 128 x 128 tile kernel, 32 tokens 34.2 against 34.4; at 64 tokens the
     // 128 x 128 tiles are ahead, 35.8 against 37.3).
     const int force = forced_variant(PQ2_OP_PREFILL);
+    if (force == PQ2_VARIANT_PREFILL_WTILE) {
+        if (M > kTileMaxM) return kUnsupportedVariant;
+        return launch_wtile(qp, S, T, codes, ws, y, dots, M, N, K, workspace, st, ctl, dev);
+    }
     if (force == PQ2_VARIANT_PREFILL_TILE ||
         (force == PQ2_VARIANT_DEFAULT && M <= kTileDefaultMaxM)) {
         if (M > kTileMaxM) return kUnsupportedVariant;

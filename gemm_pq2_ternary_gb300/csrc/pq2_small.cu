@@ -740,13 +740,16 @@ cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, con
 // and 15.5 against 23.9 and 18.3; at 8 tokens 22.3 and 15.2 against 23.2 and
 // 17.0.  The workspace covers either.
 size_t small_tc_scratch_bytes(int64_t M, int64_t N, int64_t K, int num_sms) {
-    return forced_variant(PQ2_OP_SMALL) == PQ2_VARIANT_SMALL_TILE
+    const int force = forced_variant(PQ2_OP_SMALL);
+    if (force == PQ2_VARIANT_SMALL_WTILE) return wtile_scratch_bytes(M, N, K, num_sms);
+    return force == PQ2_VARIANT_SMALL_TILE
                ? tile_scratch_bytes(M, N, K, num_sms)
                : small_scratch_bytes(M, N, K, num_sms);
 }
 
 size_t small_tc_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    const size_t a = small_workspace_bytes(M, N, K), b = tile_workspace_bytes(M, N, K);
+    const size_t a = small_workspace_bytes(M, N, K), b0 = tile_workspace_bytes(M, N, K);
+    const size_t b1 = wtile_workspace_bytes(M, N, K), b = b0 > b1 ? b0 : b1;
     return a > b ? a : b;
 }
 
@@ -756,6 +759,8 @@ cudaError_t launch_small_tc(const int8_t* qp, const float* S, const int32_t* T,
                             const pq2::DevCtl& ctl, const DeviceInfo& dev) {
     if (forced_variant(PQ2_OP_SMALL) == PQ2_VARIANT_SMALL_TILE)
         return launch_tile(qp, S, T, codes, ws, y, dots, M, N, K, workspace, st, ctl, dev);
+    if (forced_variant(PQ2_OP_SMALL) == PQ2_VARIANT_SMALL_WTILE)
+        return launch_wtile(qp, S, T, codes, ws, y, dots, M, N, K, workspace, st, ctl, dev);
     return launch_small(qp, S, T, codes, ws, y, dots, M, N, K, workspace, st, ctl, dev);
 }
 
