@@ -151,6 +151,7 @@ KERNEL_SOURCES = {
     "gemv": ["pq2_gemv.cu", "pq2_common.cuh"],
     "small": ["pq2_small.cu", "pq2_common.cuh"],
     "tile": ["pq2_tile.cu", "pq2_common.cuh"],
+    "wtile": ["pq2_wtile.cu", "pq2_common.cuh"],
     "prefill": ["pq2_prefill.cu", "pq2_common.cuh"],
     "bf16": ["pq2_bf16.cu", "pq2_common.cuh"],
     "multi": ["pq2_multi.cu", "pq2_common.cuh"],
@@ -169,6 +170,16 @@ def small_takes_dp4a(M, N, K, num_sms=152):
     return G * mt <= 480 and rows * mt * G * 4 <= 160 * 1024
 
 
+def prefill_takes_wtile(M, N, K, num_sms=152):
+    """The library's routing of pq2_gemm_prefill (wtile_default in
+    csrc/pq2_wtile.cu): 33-64 tokens on the weights-wide token-tile kernel
+    when a CTA gets at most 4 items of 128 weight rows x 4 groups."""
+    if M <= 32 or M > 64:
+        return False
+    items = ((N + 127) // 128) * ((K // 128 + 3) // 4)
+    return items <= 4 * min(num_sms, 256)
+
+
 def kernel_family(layer):
     if is_bf16(layer[0]):
         return "bf16"
@@ -178,8 +189,13 @@ def kernel_family(layer):
     if M == 1:
         return "gemv"
     # the library's routing: small_kernel to 16 tokens, the token-tile kernel
-    # to 32 (pq2_gemm_prefill), the 128-row tile kernels above
-    return "small" if M <= 16 else ("tile" if M <= 32 else "prefill")
+    # to 32 (pq2_gemm_prefill), then the weights-wide token-tile kernel where
+    # a CTA gets few items, else the 128-row tile kernels
+    if M <= 16:
+        return "small"
+    if M <= 32:
+        return "tile"
+    return "wtile" if prefill_takes_wtile(M, N, K) else "prefill"
 
 
 def sources_hash(family):

@@ -93,9 +93,16 @@ cudaError_t launch_tile(const int8_t* qp, const float* S, const int32_t* T, cons
                         const DeviceInfo& dev);
 
 // 1 <= M <= kTileMaxM: the weights-wide token-tile kernel (pq2_wtile.cu):
-// 256 expanded weight rows per MMA, the tokens' hi and lo parts as the
+// 128 expanded weight rows per MMA, the tokens' hi and lo parts as the
 // 128-row operand (16, 32 or 64 tokens), split-K partial sums reduced in a
-// fixed order.
+// fixed order.  pq2_gemm_prefill runs it by default for 33-64 tokens when
+// the call has few items a CTA (wtile_default: at most 4 (128-row tile,
+// 4-group) items per CTA, measured at 6144 -> 5120, 48 and 64 tokens: 30.3
+// and 32.6 us against 38.9 and 39.4 for the 128 x 128 tile kernel; at
+// 5120 -> 17408, 9 items a CTA, 47.2 and 48.9 against 34.7 and 35.5).
+constexpr int kWTileDefaultMinM = 32;
+constexpr int kWTileDefaultItemsPerCta = 4;
+bool wtile_default(int64_t M, int64_t N, int64_t K, int num_sms);
 size_t wtile_workspace_bytes(int64_t M, int64_t N, int64_t K);
 size_t wtile_scratch_bytes(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_wtile(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,

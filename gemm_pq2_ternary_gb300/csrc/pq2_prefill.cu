@@ -920,8 +920,11 @@ cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, c
     // at 5120 -> 17408, us per call: 17 tokens 33.3 against 39.4 for the
     // 128 x 128 tile kernel, 32 tokens 34.2 against 34.4; at 64 tokens the
     // 128 x 128 tiles are ahead, 35.8 against 37.3).
+    // From 33 to 64 tokens, where a CTA gets few items, the weights-wide
+    // token-tile kernel (wtile_default).
     const int force = forced_variant(PQ2_OP_PREFILL);
-    if (force == PQ2_VARIANT_PREFILL_WTILE) {
+    if (force == PQ2_VARIANT_PREFILL_WTILE ||
+        (force == PQ2_VARIANT_DEFAULT && wtile_default(M, N, K, dev.num_sms))) {
         if (M > kTileMaxM) return kUnsupportedVariant;
         return launch_wtile(qp, S, T, codes, ws, y, dots, M, N, K, workspace, st, ctl, dev);
     }

@@ -1,5 +1,7 @@
 // Weights-wide token-tile matmul for 5 to 64 token rows, on the
 // 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+// pq2_gemm_prefill runs it by default for 33 to 64 tokens where a CTA gets
+// few items (wtile_default); 5 to 64 tokens when forced.
 //
 // The method is the pages' small-batch and prefill arithmetic ("Making a
 // ternary reasoning model fast in vLLM", page "From CUDA to Triton and
@@ -13,52 +15,55 @@
 //
 // GB300 design.  tcgen05 has no int8 kind on sm_103a; kind::f8f6f4 with e4m3
 // operands is exact here.  The operand with many rows is the weights:
-//  * B = weights, N = 256 rows per tile, in shared memory in the MMA's
+//  * B = weights, N = 128 rows per tile, in shared memory in the MMA's
 //    K-major 128-byte-swizzled layout; expansion warps write plane s of each
 //    code word, (w >> 2s) & 0x03030303, as e4m3 bytes (exactly code * 2^-9);
 //  * A = tokens, M = 128 rows from shared memory (TMA): token m's exact e4m3
-//    parts 16h and l (q = 16h + l) on rows 2m and 2m + 1, zero rows past the
-//    call's tokens, so one A tile holds up to 64 tokens;
-//  * per group, 4 MMAs of M = 128, N = 256, K = 32 (k-step s = plane s): a
-//    quarter of the instructions the 128 x 32 small-batch tile needs per
-//    code byte, each keeping the tensor pipe busy for longer than it holds
-//    the issuing thread;
+//    parts 16h and l (q = 16h + l) on rows 2m and 2m + 1 (zero for tokens
+//    past the call's), so one A tile holds up to 64 tokens; the rows past
+//    the tile's 2 x 16, 32 or 64 only reach D rows that are never read;
+//  * per group, 4 MMAs of M = 128, N = 128, K = 32 (k-step s = plane s): half
+//    the instructions the 128 x 32 small-batch tile needs per code byte.
+//    A group's completion reaches its mbarrier about 1400 cycles after the
+//    commit, MMAs or not, so tensor memory holds 4 D buffers of 128 columns
+//    and shared memory 5-6 expanded-weight slots: groups in flight;
 //  * epilogue: D rows 2m and 2m + 1 sit on adjacent lanes, one shuffle adds
 //    them (exact), then dot = D_sum * 512 - t (an exact integer) and
 //    acc += dot * s * ws.
-// Items are (256-row tile, 4 groups), cut into contiguous balanced ranges, one
+// Items are (128-row tile, 4 groups), cut into contiguous balanced ranges, one
 // CTA per SM; a tile shared by several CTAs is finished by the last
 // contributor, which sums all partials in CTA order.
 //
 // Per CTA (warp roles; a warp may read only its own TMEM lane quadrant,
 // warp % 4, so the epilogue warps are the warps w < 16 whose quadrant holds
 // token rows, and the other roles take the remaining warps in order):
-//   epilogue      TMEM lane quadrant w % 4 x 64 columns (block w / 4)
+//   epilogue      TMEM lane quadrant w % 4 x 32 columns (block w / 4)
 //   producer      TMA of the item's code box and of each group's token tile
-//   MMA issuer    also allocates tensor memory (2 D buffers of 256 columns)
-//   expansion     4 warps: two weight rows per thread into a B slot; they
-//                 also stage each group's fp32 weight scales and the tokens'
-//                 (s, t) for the epilogue
+//   MMA issuer    also allocates tensor memory (4 D buffers of 128 columns)
+//   expansion     8 warps at 16 tokens (two planes of a row per thread), else
+//                 4 (a whole row); they also stage each group's fp32 weight
+//                 scales and the tokens' (s, t) for the epilogue
 // Every mbarrier wait is bounded (device error word on expiry).
 #include "pq2_internal.h"
 
 namespace {
 
-constexpr int kBN = 256;                      // weight rows per tile (MMA N)
+constexpr int kBN = 128;                      // weight rows per tile (MMA N)
+constexpr int kCB = kBN / 4;                  // columns per epilogue warp (4 column blocks)
+constexpr int kWsRows = kBN / 32;             // weight rows whose scales each producer lane copies
 constexpr int kGQ = 4;                        // groups per item
 constexpr int kMaxGrid = 256;                 // CTAs per call at most (bounds the partial slots)
-constexpr uint32_t kCodesBytes = kBN * 128;   // an item's code box: 256 rows x 4 groups
-constexpr uint32_t kATile = 128 * 128;        // a group's token tile (MMA M = 128 rows)
+constexpr uint32_t kCodesBytes = kBN * 128;   // an item's code box: kBN rows x 4 groups
 constexpr uint32_t kBTile = kBN * 128;        // a group's expanded weights
-constexpr int kCStages = 2;                   // code boxes in flight (items)
-constexpr int kASlots = 4;                    // token tiles (groups)
-constexpr int kBSlots = 2;                    // expanded weights (groups); D buffers alike
-constexpr int kESlots = 4;                    // epilogue inputs (groups)
-constexpr int kXW = 4;                        // expansion warps
-#ifndef PQ2_WTILE_LOADS
-#define PQ2_WTILE_LOADS 2
-#endif
-// kind::f8f6f4: D f32, A and B e4m3, both K-major, M = 128, N = 256
+constexpr int kCStages = 3;                   // code boxes in flight (items)
+constexpr int kMaxASlots = 16;                // token tiles (groups) in flight at most
+constexpr int kMaxBSlots = 8;                 // expanded weights (groups) in flight at most
+constexpr int kDSlots = 512 / kBN;            // D buffers in tensor memory (groups)
+constexpr int kESlots = 8;                    // epilogue inputs (groups)
+constexpr int kNL = kCB / 16;                 // 16-column tensor-memory loads per group
+constexpr int kAcc = 8 * kNL;                 // accumulators per epilogue lane
+static_assert(kNL % 2 == 0, "the last contributor sums 16 columns at a time");
+// kind::f8f6f4: D f32, A and B e4m3, both K-major, M = 128, N = kBN
 constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) |
                             (static_cast<uint32_t>(128 >> 4) << 24);
 
@@ -69,36 +74,52 @@ struct WCfg {
     static constexpr int EACT = 4 * QA;            // epilogue warps (4 column blocks each)
     // epilogue warps are the warps w < 16 with w % 4 < QA (quadrant w % 4,
     // column block w / 4); the other warps, in order, are the producer, the
-    // MMA issuer and the 4 expansion warps.  No more than 4 warps share an SM
-    // sub-partition up to 32 tokens (128 registers a thread)
-    static constexpr int WARPS = QA == 4 ? 22 : (QA == 2 ? 14 : 13);
+    // MMA issuer and XW expansion warps: 8 at 16 tokens, else 4 (no more than
+    // 4 warps share an SM sub-partition at 32 tokens: 128 registers a thread)
+    static constexpr int XW = MT == 16 ? 8 : 4;
+    // an expansion unit is one weight row's two planes 2 hp, 2 hp + 1 (unit
+    // u: row u % kBN, hp = u / kBN); each expansion thread takes UPT units
+    static constexpr int UPT = 2 * kBN / (32 * XW);
+    static constexpr int WARPS = QA == 4 ? 16 + 2 + XW : 14;
+    // expanded-weight slots: the expansion of group g waits for the MMAs of
+    // group g - BSLOTS
+    static constexpr int BSLOTS = MT == 64 ? 5 : 6;
     static constexpr int THREADS = WARPS * 32;
-    // epilogue inputs of a group: weight scales [256] fp32, then s[MT], t[MT]
+    // epilogue inputs of a group: weight scales [kBN] fp32, then s[MT], t[MT]
     static constexpr uint32_t E_S = kBN * 4;
     static constexpr uint32_t E_T = E_S + MT * 4;
     static constexpr uint32_t ESLOT = (E_T + MT * 4 + 127) / 128 * 128;
-    // code stage (an item): code box | weight scales [256 rows][4 groups]
+    // code stage (an item): code box | weight scales [kBN rows][4 groups]
     // fp16 | (s, t) [4 groups][2][MT] fp32
     static constexpr uint32_t WS_OFF = kCodesBytes;
     static constexpr uint32_t ST_OFF = WS_OFF + kBN * kGQ * 2;
     static constexpr uint32_t ST_BYTES = kGQ * 2 * MT * 4;
     static constexpr uint32_t CSTAGE = (ST_OFF + ST_BYTES + 1023) / 1024 * 1024;
+    // token tiles: the MMA reads 128 rows from a slot, of which only the
+    // first AROWS are written; the rest (the next slots' rows, or the pad after
+    // the last slot) only reach D rows no epilogue warp reads, so slots sit
+    // AROWS rows apart and more groups' tiles are in flight at few tokens
+    static constexpr uint32_t ASLOT = AROWS * 128;
+    static constexpr int ASLOTS = MT == 16 ? 12 : (MT == 32 ? 6 : 4);
     static constexpr uint32_t OFF_A = kCStages * CSTAGE;
-    static constexpr uint32_t OFF_B = OFF_A + kASlots * kATile;
-    static constexpr uint32_t OFF_E = OFF_B + kBSlots * kBTile;
+    static constexpr uint32_t OFF_B = OFF_A + ASLOTS * ASLOT + (128 - AROWS) * 128;
+    static constexpr uint32_t OFF_E = OFF_B + BSLOTS * kBTile;
     static constexpr size_t SMEM = 1024 + OFF_E + kESlots * ESLOT;
     static_assert(MT == 16 || MT == 32 || MT == 64, "token tile");
+    static_assert(ASLOTS <= kMaxASlots && ASLOT % 1024 == 0, "token tile slots");
+    static_assert(BSLOTS <= kMaxBSlots && UPT >= 1 && 32 * XW * UPT == 2 * kBN, "expansion");
+    static_assert(2 * MT <= 32 * XW, "one thread per token scale");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 struct WTileParams {
-    CUtensorMap tm_codes;  // uint8 [N][K/4], box {128, 256}, 128B swizzle
+    CUtensorMap tm_codes;  // uint8 [N][K/4], box {128, kBN}, 128B swizzle
     CUtensorMap tm_tok;    // uint8 [G4 * AROWS][128], box {128, AROWS}, 128B swizzle
     const float* st;       // [G4][2][MT]: s then t, zero past M and past G
     const __half* ws;      // [N][G]
     float* y;              // [M][N]
     int32_t* dots;         // debug: [M][N][G]
-    float* partial;        // [grid + n_tiles][M][256]
+    float* partial;        // [grid + n_tiles][M][kBN]
     unsigned* counters;    // [n_tiles], zero on entry
     int M, N, K, G;
     int Q;                 // quads per tile: ceil(G / 4)
@@ -261,14 +282,15 @@ enum WRole { kProducer, kIssuer, kExpand, kEpilogue, kIdle };
 
 // Role of warp w (idx: the expansion warp's index or the epilogue warp's
 // column block).
-__device__ __forceinline__ WRole wrole(int w, int qa, int& idx) {
+__device__ __forceinline__ WRole wrole(int w, int qa, int xw, int& idx) {
     if (w < 16 && (w & 3) < qa) {
         idx = w >> 2;
         return kEpilogue;
     }
-    const int rank = w < 16 ? w - (w >> 2) * qa - ((w & 3) < qa ? (w & 3) : qa) : w - 16;
+    // rank = the warps below w that are not epilogue warps
+    const int rank = w < 16 ? w - (w >> 2) * qa - ((w & 3) < qa ? (w & 3) : qa) : w - 4 * qa;
     idx = rank - 2;
-    return rank == 0 ? kProducer : (rank == 1 ? kIssuer : (rank < 2 + kXW ? kExpand : kIdle));
+    return rank == 0 ? kProducer : (rank == 1 ? kIssuer : (rank < 2 + xw ? kExpand : kIdle));
 }
 
 template <int MT, bool DOTS>
@@ -277,14 +299,14 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint64_t cfull[kCStages];   // an item's code box landed (TMA)
     __shared__ uint64_t cfree[kCStages];   // the box's codes were expanded (expansion warps)
-    __shared__ uint64_t afull[kASlots];    // a group's token tile landed (TMA)
-    __shared__ uint64_t afree[kASlots];    // its MMAs are done (commit)
-    __shared__ uint64_t bready[kBSlots];   // a group's weights expanded (expansion warps)
-    __shared__ uint64_t bfree[kBSlots];    // its MMAs are done (commit)
+    __shared__ uint64_t afull[kMaxASlots];  // a group's token tile landed (TMA)
+    __shared__ uint64_t afree[kMaxASlots];  // its MMAs are done (commit)
+    __shared__ uint64_t bready[kMaxBSlots];  // a group's weights expanded (expansion warps)
+    __shared__ uint64_t bfree[kMaxBSlots];   // its MMAs are done (commit)
     __shared__ uint64_t efull[kESlots];    // a group's scales, s and t staged (expansion warps)
     __shared__ uint64_t efree[kESlots];    // the epilogue read them (epilogue warps)
-    __shared__ uint64_t dfull[kBSlots];    // a group's D complete (commit)
-    __shared__ uint64_t dfree[kBSlots];    // its D read (epilogue warps)
+    __shared__ uint64_t dfull[kDSlots];    // a group's D complete (commit)
+    __shared__ uint64_t dfree[kDSlots];    // its D read (epilogue warps)
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     __shared__ int last_flag;
@@ -296,38 +318,32 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
     uint8_t* sm = smem + ((1024 - (base & 1023)) & 1023);
     const uint32_t sm_s = pq2::smem_u32(sm);
 
-    // token tiles: rows past the call's tokens stay zero (the TMA writes rows
-    // 0 .. AROWS - 1 of a slot only)
-    for (uint32_t i = tid; i < kASlots * kATile / 16; i += C::THREADS) {
-        const uint32_t off = C::OFF_A + 16 * i;
-        if ((off - C::OFF_A) % kATile >= C::AROWS * 128)
-            *reinterpret_cast<uint4*>(sm + off) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (tid == 0) {
         for (int i = 0; i < kCStages; ++i) {
             pq2::mbar_init(&cfull[i], 1 + 32);  // the TMA bytes + the producer's 32 lanes
-            pq2::mbar_init(&cfree[i], kXW);
+            pq2::mbar_init(&cfree[i], C::XW);
         }
-        for (int i = 0; i < kASlots; ++i) {
+        for (int i = 0; i < C::ASLOTS; ++i) {
             pq2::mbar_init(&afull[i], 1);
             pq2::mbar_init(&afree[i], 1);
         }
-        for (int i = 0; i < kBSlots; ++i) {
-            pq2::mbar_init(&bready[i], kXW);
+        for (int i = 0; i < C::BSLOTS; ++i) {
+            pq2::mbar_init(&bready[i], C::XW);
             pq2::mbar_init(&bfree[i], 1);
+        }
+        for (int i = 0; i < kDSlots; ++i) {
             pq2::mbar_init(&dfull[i], 1);
             pq2::mbar_init(&dfree[i], C::EACT);
         }
         for (int i = 0; i < kESlots; ++i) {
-            pq2::mbar_init(&efull[i], kXW);
+            pq2::mbar_init(&efull[i], C::XW);
             pq2::mbar_init(&efree[i], C::EACT);
         }
         abort_flag = 0;
         pq2::fence_mbar_init();
     }
     int ridx = 0;
-    const WRole role = wrole(warp, C::QA, ridx);
+    const WRole role = wrole(warp, C::QA, C::XW, ridx);
     if (role == kIssuer) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          pq2::smem_u32(&tmem_base)),
@@ -354,8 +370,8 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
     if (role == kProducer) {
         // -------------------------------- producer --------------------------------
         // Lane 0 issues the TMA of the item's code box and token tiles and one
-        // bulk copy of its (s, t).  Lane l copies the weight scales of rows
-        // 8l .. 8l + 7 (the item's 4 groups: 8 bytes of fp16 a row) with
+        // bulk copy of its (s, t).  Lane l copies the weight scales of its
+        // kWsRows rows (the item's 4 groups: 8 bytes of fp16 a row) with
         // cp.async, which arrive on the stage's barrier when they land; rows
         // past N, or every row when a row's 4 scales are not 8-byte aligned
         // (G % 4 != 0), are read with plain loads (zero past N and past G).
@@ -380,16 +396,16 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
             }
             bool lane_async = false;
             if (!DOTS) {
-                const int row0 = t * kBN + 8 * lane;
-                uint8_t* dst = stg + C::WS_OFF + 8 * lane * 8;  // [row][4 groups] fp16
-                lane_async = ws_async && row0 + 7 < p.N;
+                const int row0 = t * kBN + kWsRows * lane;
+                uint8_t* dst = stg + C::WS_OFF + kWsRows * lane * 8;  // [row][4 groups] fp16
+                lane_async = ws_async && row0 + kWsRows - 1 < p.N;
                 if (lane_async) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
+                    for (int j = 0; j < kWsRows; ++j)
                         cp_async8(dst + 8 * j, wsu + static_cast<size_t>(row0 + j) * G + q * kGQ);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < kWsRows; ++j) {
                         unsigned short v[kGQ];
 #pragma unroll
                         for (int gq = 0; gq < kGQ; ++gq) {
@@ -414,15 +430,15 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
             if (lane == 0) {
                 for (int gq = 0; gq < kGQ; ++gq) {
                     const int gi = it * kGQ + gq;
-                    const int as = gi % kASlots;
-                    if (gi >= kASlots &&
-                        !pq2::mbar_wait_bounded(&afree[as], ((gi / kASlots) - 1) & 1, p.ctl, abort_v)) {
+                    const int as = gi % C::ASLOTS;
+                    if (gi >= C::ASLOTS &&
+                        !pq2::mbar_wait_bounded(&afree[as], ((gi / C::ASLOTS) - 1) & 1, p.ctl, abort_v)) {
                         ok = false;
                         break;
                     }
                     a_issued = gi + 1;
                     pq2::mbar_arrive_expect_tx(&afull[as], C::AROWS * 128);
-                    pq2::tma_load_2d(sm + C::OFF_A + as * kATile, &p.tm_tok, 0,
+                    pq2::tma_load_2d(sm + C::OFF_A + as * C::ASLOT, &p.tm_tok, 0,
                                      (q * kGQ + gq) * C::AROWS, &afull[as]);
                 }
             }
@@ -438,10 +454,10 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                 if (last == p.ctl.debug_skip_stage) last -= kCStages;
                 if (last >= 0) pq2::mbar_wait_bounded(&cfull[k], (last / kCStages) & 1, p.ctl);
             }
-            for (int k = 0; k < kASlots; ++k) {
+            for (int k = 0; k < C::ASLOTS; ++k) {
                 if (a_issued <= k) continue;
-                const int last = k + ((a_issued - 1 - k) / kASlots) * kASlots;
-                pq2::mbar_wait_bounded(&afull[k], (last / kASlots) & 1, p.ctl);
+                const int last = k + ((a_issued - 1 - k) / C::ASLOTS) * C::ASLOTS;
+                pq2::mbar_wait_bounded(&afull[k], (last / C::ASLOTS) & 1, p.ctl);
             }
         }
     } else if (role == kIssuer) {
@@ -449,36 +465,38 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
         if (lane == 0) {
             int last = -1;
             for (int gi = 0; gi < ng; ++gi) {
-                const int as = gi % kASlots, bs = gi % kBSlots;
+                const int as = gi % C::ASLOTS, bs = gi % C::BSLOTS, ds = gi % kDSlots;
                 // busy polling: this thread is on the critical path
-                if (!pq2::mbar_spin_bounded(&afull[as], (gi / kASlots) & 1, p.ctl, abort_v) ||
-                    !pq2::mbar_spin_bounded(&bready[bs], (gi / kBSlots) & 1, p.ctl, abort_v) ||
-                    (gi >= kBSlots &&
-                     !pq2::mbar_spin_bounded(&dfree[bs], ((gi / kBSlots) - 1) & 1, p.ctl, abort_v))) {
+                if (!pq2::mbar_spin_bounded(&afull[as], (gi / C::ASLOTS) & 1, p.ctl, abort_v) ||
+                    !pq2::mbar_spin_bounded(&bready[bs], (gi / C::BSLOTS) & 1, p.ctl, abort_v) ||
+                    (gi >= kDSlots &&
+                     !pq2::mbar_spin_bounded(&dfree[ds], ((gi / kDSlots) - 1) & 1, p.ctl, abort_v))) {
                     *abort_v = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = sm_s + C::OFF_A + as * kATile;
+                const uint32_t a0 = sm_s + C::OFF_A + as * C::ASLOT;
                 const uint32_t b0 = sm_s + C::OFF_B + bs * kBTile;
-                const uint32_t d_tmem = tmem + bs * kBN;
+                const uint32_t d_tmem = tmem + ds * kBN;
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_ss(d_tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k), k > 0);
                 mma_commit(&afree[as]);
                 mma_commit(&bfree[bs]);
-                mma_commit(&dfull[bs]);
+                mma_commit(&dfull[ds]);
                 last = gi;
             }
             // no MMA may still be running when tensor memory is released
             if (last >= 0)
-                pq2::mbar_wait_bounded(&dfull[last % kBSlots], (last / kBSlots) & 1, p.ctl);
+                pq2::mbar_wait_bounded(&dfull[last % kDSlots], (last / kDSlots) & 1, p.ctl);
         }
     } else if (role == kExpand) {
         // -------------------------------- expansion --------------------------------
-        // Thread x expands weight rows x and x + 128 of the tile into the
-        // group's B slot; it also writes their fp32 weight scales and, for
-        // x < 2 MT, one of the tokens' s or t into the group's epilogue slot.
+        // Thread x expands units x + 32 XW j (j < UPT) of the tile into the
+        // group's B slot: unit u is planes 2 hp and 2 hp + 1 of weight row
+        // u % kBN, hp = u / kBN.  The thread whose unit is a row's hp = 0 also
+        // writes the row's fp32 weight scale, and thread x < 2 MT one of the
+        // tokens' s or t, into the group's epilogue slot.
         const int x = ridx * 32 + lane;
         bool failed = false;
         for (int it = 0; it < n; ++it) {
@@ -489,21 +507,24 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
 #pragma unroll 1
             for (int gq = 0; gq < kGQ; ++gq) {
                 const int gi = it * kGQ + gq;
-                const int bs = gi % kBSlots, es = gi % kESlots;
-                // this group's weight scales of rows x, x + 128 and (for x < 2 MT)
-                // s or t of a token, from the stage (zero past N, M and G)
-                float wsv[2] = {0.0f, 0.0f}, stv = 0.0f;
-                if (!failed) {
-                    if (!DOTS) {
+                const int bs = gi % C::BSLOTS, es = gi % kESlots;
+                // the weight scales of this thread's hp = 0 rows and (for x <
+                // 2 MT) s or t of a token, from the stage (zero past N, M and G)
+                float wsv[C::UPT], stv = 0.0f;
 #pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            wsv[h] = __half2float(__ushort_as_half(static_cast<unsigned short>(
-                                pq2::lds_u16(cbox + C::WS_OFF + 2 * ((x + 128 * h) * kGQ + gq)))));
+                for (int j = 0; j < C::UPT; ++j) wsv[j] = 0.0f;
+                if (!failed) {
+#pragma unroll
+                    for (int j = 0; j < C::UPT; ++j) {
+                        const int u = x + 32 * C::XW * j;
+                        if (!DOTS && u < kBN)
+                            wsv[j] = __half2float(__ushort_as_half(static_cast<unsigned short>(
+                                pq2::lds_u16(cbox + C::WS_OFF + 2 * (u * kGQ + gq)))));
                     }
                     if (x < 2 * MT) stv = pq2::lds_f32(cbox + C::ST_OFF + 4 * (gq * 2 * MT + x));
                 }
-                if (!failed && gi >= kBSlots &&
-                    !pq2::mbar_suspend_warp(&bfree[bs], ((gi / kBSlots) - 1) & 1, p.ctl, abort_v))
+                if (!failed && gi >= C::BSLOTS &&
+                    !pq2::mbar_suspend_warp(&bfree[bs], ((gi / C::BSLOTS) - 1) & 1, p.ctl, abort_v))
                     failed = true;
                 if (!failed && gi >= kESlots &&
                     !pq2::mbar_suspend_warp(&efree[es], ((gi / kESlots) - 1) & 1, p.ctl, abort_v))
@@ -511,9 +532,11 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                 if (failed) *abort_v = 1;
                 if (!failed) {
                     uint8_t* bslot = sm + C::OFF_B + bs * kBTile;
+                    float* eslot = reinterpret_cast<float*>(sm + C::OFF_E + es * C::ESLOT);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int r = x + 128 * h;  // row within the tile
+                    for (int j = 0; j < C::UPT; ++j) {
+                        const int u = x + 32 * C::XW * j;
+                        const int r = u % kBN, hp = u / kBN;  // row within the tile, plane pair
                         // code box row r: 16-byte chunks 2gq, 2gq + 1, 128-byte swizzled
                         const uint32_t crow = cbox + r * 128;
                         const uint4 lo4 = pq2::lds_v4(crow + (((2 * gq) ^ (r & 7)) << 4));
@@ -521,7 +544,8 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                         const uint32_t w[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
                         uint8_t* brow = bslot + r * 128;
 #pragma unroll
-                        for (int pl = 0; pl < 4; ++pl) {
+                        for (int pp = 0; pp < 2; ++pp) {
+                            const int pl = 2 * hp + pp;
 #pragma unroll
                             for (int hc = 0; hc < 2; ++hc) {  // 16-byte chunk 2 pl + hc of the row
                                 uint4 v;
@@ -532,10 +556,8 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                                 *reinterpret_cast<uint4*>(brow + 16 * ((2 * pl + hc) ^ (r & 7))) = v;
                             }
                         }
+                        if (u < kBN) eslot[r] = wsv[j];
                     }
-                    float* eslot = reinterpret_cast<float*>(sm + C::OFF_E + es * C::ESLOT);
-                    eslot[x] = wsv[0];
-                    eslot[x + 128] = wsv[1];
                     if (x < 2 * MT) eslot[kBN + x] = stv;  // s[m] at kBN + m, t[m] at kBN + MT + m
                     // the B tile is read by the tensor cores (async proxy)
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -552,15 +574,15 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
     } else if (role == kEpilogue) {
         // -------------------------------- epilogue --------------------------------
         const int quad = warp & 3;               // TMEM lane quadrant
-        const int cb = ridx;                     // column block: 64 cb .. 64 cb + 63
+        const int cb = ridx;                     // column block: kCB cb .. kCB (cb + 1) - 1
         const int h = lane & 1;                  // 0: the hi row of the token, 1: the lo row
         const int m = (quad * 32 + lane) >> 1;   // token
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         constexpr uint32_t kEpiThreads = C::EACT * 32;
         bool failed = false;
-        float acc[32];  // this lane's columns: 64 cb + 16 c + 8 h + i, at acc[8 c + i]
+        float acc[kAcc];  // this lane's columns: kCB cb + 16 c + 8 h + i, at acc[8 c + i]
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < kAcc; ++i) acc[i] = 0.0f;
         int te = t_first, qe = q_first;  // item being finished
         for (int it = 0; it < n; ++it) {
             const int t = te, q = qe;
@@ -568,13 +590,13 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
             if (++qe == Q) { qe = 0; ++te; }
             for (int gq = 0; gq < kGQ; ++gq) {
                 const int gi = it * kGQ + gq;
-                const int ds = gi % kBSlots, es = gi % kESlots;
+                const int ds = gi % kDSlots, es = gi % kESlots;
                 const int g = q * kGQ + gq;
                 // busy polling for D: the next MMAs into this buffer wait for its
                 // release, and a suspended try_wait can resume well after the
                 // phase completes
                 if (!failed &&
-                    (!pq2::mbar_spin_warp(&dfull[ds], (gi / kBSlots) & 1, p.ctl, abort_v) ||
+                    (!pq2::mbar_spin_warp(&dfull[ds], (gi / kDSlots) & 1, p.ctl, abort_v) ||
                      !pq2::mbar_spin_warp(&efull[es], (gi / kESlots) & 1, p.ctl, abort_v))) {
                     failed = true;
                     *abort_v = 1;
@@ -583,21 +605,20 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                 const float sv = failed ? 0.0f : eslot[kBN + m];
                 const float tv = failed ? 0.0f : eslot[kBN + MT + m];
                 if (!failed) tc_fence_after();
-                // Up to 32 tokens all 64 columns are loaded before the arithmetic
-                // (one wait), so the D buffer is released as early as it can be
-                // (the next MMAs into it wait for that); at 64 tokens, with fewer
-                // registers a thread, 16 columns per wait.
-                constexpr int kLoads = C::QA <= 2 ? PQ2_WTILE_LOADS : 1;  // 16-column loads per wait
+                // Up to 32 tokens 32 columns per wait, at 64 tokens (fewer
+                // registers a thread) 16; D is released after the last wait, before
+                // the arithmetic on those columns.
+                constexpr int kLoads = C::QA <= 2 ? 2 : 1;  // 16-column loads per wait
 #pragma unroll
-                for (int cl = 0; cl < 4; cl += kLoads) {
+                for (int cl = 0; cl < kNL; cl += kLoads) {
                     float v[16 * kLoads];
                     if (!failed) {
 #pragma unroll
                         for (int l = 0; l < kLoads; ++l)
-                            tmem_ld16(tmem + lane_off + ds * kBN + 64 * cb + 16 * (cl + l), v + 16 * l);
+                            tmem_ld16(tmem + lane_off + ds * kBN + kCB * cb + 16 * (cl + l), v + 16 * l);
                         tmem_wait_ld();
                     }
-                    if (cl + kLoads == 4) {
+                    if (cl + kLoads == kNL) {
                         // every column of the group is in registers: D is free
                         tc_fence_before();
                         __syncwarp();
@@ -618,7 +639,7 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                         const float give = h ? vc[i] : vc[8 + i];
                         sum[i] = keep + __shfl_xor_sync(0xffffffffu, give, 1);
                     }
-                    const int c0 = 64 * cb + 16 * c + 8 * h;  // first column of this lane
+                    const int c0 = kCB * cb + 16 * c + 8 * h;  // first column of this lane
                     if (DOTS) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
@@ -658,16 +679,16 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
             if (DOTS) continue;
             const int c_lo = owner_of(static_cast<long long>(t) * Q, p.items, p.grid);
             const int c_hi = owner_of(static_cast<long long>(t + 1) * Q - 1, p.items, p.grid);
-            // acc[8 c + i] is column colb + 16 c + i: four runs of 8 columns,
+            // acc[8 c + i] is column colb + 16 c + i: kNL runs of 8 columns,
             // written and read as float4 j = 2 c + (i >> 2)
-            const int colb = t * kBN + 64 * cb + 8 * h;
+            const int colb = t * kBN + kCB * cb + 8 * h;
             const bool y_vec = (p.N & 3) == 0;  // 16-byte aligned rows of y
             if (c_lo == c_hi) {
                 // the whole tile is this CTA's: straight to y
                 if (m < p.M) {
                     float* yr = p.y + static_cast<size_t>(m) * p.N;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < 2 * kNL; ++j) {
                         const int col = colb + 16 * (j >> 1) + 4 * (j & 1);
                         if (y_vec && col + 3 < p.N) {
                             *reinterpret_cast<float4*>(yr + col) =
@@ -684,7 +705,7 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                 if (m < p.M) {
                     float* pr = part + static_cast<size_t>(m) * kBN + (colb - t * kBN);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
+                    for (int j = 0; j < 2 * kNL; ++j)
                         *reinterpret_cast<float4*>(pr + 16 * (j >> 1) + 4 * (j & 1)) =
                             make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
                 }
@@ -702,7 +723,7 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                     float* yr = p.y + static_cast<size_t>(m) * p.N;
                     const size_t roff = static_cast<size_t>(m) * kBN + (colb - t * kBN);
 #pragma unroll 1
-                    for (int hb = 0; hb < 2; ++hb) {  // float4 j = 4 hb .. 4 hb + 3
+                    for (int hb = 0; hb < kNL / 2; ++hb) {  // float4 j = 4 hb .. 4 hb + 3
                         float4 sum[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) sum[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -746,7 +767,7 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                 // flushing warp has passed the first barrier there
             }
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < kAcc; ++i) acc[i] = 0.0f;
         }
     }
 
@@ -788,7 +809,7 @@ WTileLayout layout_wtile(int64_t M, int64_t N, int64_t K, int num_sms) {
     l.counters = off;
     off += align256(static_cast<size_t>(l.n_tiles) * 4);
     l.partial = off;
-    // one [M][256] slot per (CTA c, tile t) pair, at index c + t
+    // one [M][kBN] slot per (CTA c, tile t) pair, at index c + t
     off += align256(static_cast<size_t>(l.grid + l.n_tiles) * M * kBN * 4);
     l.total = off;
     return l;
@@ -843,6 +864,13 @@ cudaError_t launch_mt(const int8_t* qp, const float* S, const int32_t* T, const 
 }  // namespace
 
 namespace pq2h {
+
+bool wtile_default(int64_t M, int64_t N, int64_t K, int num_sms) {
+    if (M <= kWTileDefaultMinM || M > kTileMaxM) return false;
+    const WTileLayout l = layout_wtile(M, N, K, num_sms);
+    const long long cap = num_sms < kMaxGrid ? num_sms : kMaxGrid;
+    return l.items <= kWTileDefaultItemsPerCta * cap;
+}
 
 size_t wtile_scratch_bytes(int64_t M, int64_t N, int64_t K, int num_sms) {
     return layout_wtile(M, N, K, num_sms).total;

@@ -343,14 +343,16 @@ size_t pq2_gemm_small_noalloc_max_scratch(void);
 #define PQ2_VARIANT_SMALL_TC 2       /* tcgen05, weights in tensor memory, 16-token
                                         tile (5..16 tokens by default)              */
 #define PQ2_VARIANT_SMALL_TILE 3     /* tcgen05 token-tile kernel (16 tokens)       */
-#define PQ2_VARIANT_SMALL_WTILE 4    /* tcgen05, 256 weight rows per MMA, tokens as
+#define PQ2_VARIANT_SMALL_WTILE 4    /* tcgen05, 128 weight rows per MMA, tokens as
                                         the 128-row operand (16 tokens)             */
 #define PQ2_VARIANT_PREFILL_128 1    /* tcgen05 128 x 128 tiles, in-kernel expansion */
 #define PQ2_VARIANT_PREFILL_WIDE 2   /* tcgen05 128 x 256 tiles, pre-expanded weights */
 #define PQ2_VARIANT_PREFILL_TILE 3   /* tcgen05 token-tile kernel, M <= 64 (by
-                                        default up to 32 tokens)                    */
-#define PQ2_VARIANT_PREFILL_WTILE 4  /* tcgen05, 256 weight rows per MMA, tokens as
-                                        the 128-row operand, M <= 64                */
+                                        default 17-32 tokens)                       */
+#define PQ2_VARIANT_PREFILL_WTILE 4  /* tcgen05, 128 weight rows per MMA, tokens as
+                                        the 128-row operand, M <= 64 (by default
+                                        33-64 tokens when a CTA gets at most 4
+                                        items of 128 rows x 4 groups)               */
 
 /*
  * pq2_debug_force_kernel -- test hook: from now on, calls of `op`

@@ -158,3 +158,25 @@ def test_wtile_reports_timeout(pq2, prob):
     y = _run(pq2, c)
     ref, A = oracle.matmul(c.oqp, c.oS, c.ocodes, c.ws)
     _tol_check(c, y.cpu().numpy(), ref, A, "y after the timeout")
+
+
+@pytest.mark.parametrize("M,K,N,want", [(48, 6144, 5120, "wtile"), (64, 6144, 5120, "wtile"),
+                                        (48, 5120, 17408, "128")], ids=lambda v: str(v))
+def test_prefill_routes_mid_token_counts(pq2, M, K, N, want):
+    # 33-64 tokens take the weights-wide kernel where a CTA gets at most 4
+    # items (128 rows x 4 groups), else the 128 x 128 tile kernel: the
+    # default call is bit-identical to the forced one, and bench.py's mirror
+    # of the rule agrees
+    import bench
+    assert bench.prefill_takes_wtile(M, N, K) == (want == "wtile")
+    c = Case(pq2, inputs.Problem(f"route_m{M}", M, K, N, "p343", "outliers", 200 + M))
+    ws = pq2.alloc_workspace(pq2.PQ2_OP_PREFILL, M, N, K)
+    y_def = torch.empty((M, N), device=DEV)
+    pq2.pq2_gemm_prefill(c.qp, c.S, c.T, c.codes, c.ws_d, y_def, ws)
+    var = pq2.PQ2_VARIANT_PREFILL_WTILE if want == "wtile" else pq2.PQ2_VARIANT_PREFILL_128
+    y_f = torch.empty((M, N), device=DEV)
+    with pq2.forced_kernel(pq2.PQ2_OP_PREFILL, var):
+        pq2.pq2_gemm_prefill(c.qp, c.S, c.T, c.codes, c.ws_d, y_f, ws)
+    torch.cuda.synchronize()
+    assert pq2.pq2_last_device_error() == pq2.PQ2_OK
+    assert torch.equal(y_def, y_f)
