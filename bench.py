@@ -18,7 +18,8 @@ Workloads (--workload):
   mlp      M=--m (1 or 16): gate/up 5120 -> 34816, quantise the synthetic
            intermediate h, down 17408 -> 5120
   prefill  M=--m (128 or 4096), 5120 -> 17408
-  mid      M=--m (17..64), 5120 -> 17408 through pq2_gemm_prefill, in GB/s
+  mid      M=--m (17..64), --shape K,N (5120,17408 by default) through
+           pq2_gemm_prefill, in GB/s
   lmhead   M=1, K=5120 -> N=248320 (an lm_head-scale decode GEMV)
   mlp_swiglu  M=--m: gate/up 5120 -> 34816, then the down projection straight
            from its output (pq2_mlp_down_swiglu: SwiGLU + quantise, 17408 -> 5120)
@@ -125,7 +126,8 @@ def workload_spec(args):
     if w == "mid":
         if not 16 < args.m <= 64:
             raise SystemExit("--workload mid takes 17 <= --m <= 64")
-        return f"mid_m{args.m}_k5120_n17408", [(args.m, 5120, 17408, "p343", "outliers")], "GB/s"
+        K, N = (int(v) for v in (args.shape or "5120,17408").split(","))
+        return f"mid_m{args.m}_k{K}_n{N}", [(args.m, K, N, "p343", "outliers")], "GB/s"
     if w == "mlp":
         return f"mlp_pair_m{args.m}", [(args.m, 5120, 34816, "uniform", "normal"),
                                        (args.m, 17408, 5120, "uniform", "normal")], "GB/s"
@@ -876,7 +878,7 @@ def reference_arm(args, rank, world):
 SUITE = ([("pr1", 1, None)] +
          [("small", m, sh) for m in (2, 4, 8, 16) for sh in ("6144,5120", "5120,17408")] +
          [("mlp", 1, None), ("mlp", 16, None), ("prefill", 128, None), ("prefill", 4096, None),
-          ("mid", 32, None), ("mid", 64, None),
+          ("mid", 32, None), ("mid", 64, None), ("mid", 64, "6144,5120"),
           ("lmhead", 1, None), ("in_proj_ba", 4, None), ("mlp_swiglu", 1, None)])
 
 

@@ -259,6 +259,21 @@ __device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool 
     return r != 0;
 }
 
+// Split-K hand-off counter: fetch-and-add at gpu scope with acquire-release
+// semantics, by one thread right after a barrier of the threads that wrote
+// partial sums.  The release half publishes those writes (ordered before
+// this thread by the barrier) before the add; the acquire half orders the
+// reads after it -- and, through the next barrier, the other threads' reads
+// -- after every write released by earlier adds on the same counter.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
 // d = c + sum_i a.u8[i] * b.s8[i]   (a unsigned bytes, b signed bytes)
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     int d;

@@ -76,6 +76,7 @@ constexpr uint32_t kGCols = 32;       // TMEM columns per group (A: K = 128 e4m3
 constexpr uint32_t kDCol0 = kBufs * kGQ * kGCols;  // 256
 constexpr int kMaxGrid = 256;         // CTAs per call at most (bounds the partial-sum slots)
 constexpr int kWsAhead = 2;           // items ahead the producer loads weight scales
+constexpr int kFlushBatch = 8;        // contributors whose partials the last one loads at once
 
 constexpr uint32_t kCodesBytes = kRows * 128;          // 4 groups x 32 B per row, swizzled
 constexpr uint32_t kTokGroupBytes = 2 * kTok * 128;    // 32 rows x 128 B per group
@@ -587,30 +588,40 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
                         const int m = 4 * wq + j;
                         if (m < p.M) part[static_cast<size_t>(m) * kRows + r] = acc[j];
                     }
-                    __threadfence();
                     pq2::named_bar_sync(2, kWorkerThreads);
                     if (lead && lane == 0) {
-                        const unsigned old = atomicAdd(&p.counters[t], 1u);
+                        const unsigned old = pq2::atom_add_acq_rel_gpu(&p.counters[t], 1u);
                         last_flag = (old == static_cast<unsigned>(c_hi - c_lo)) ? 1 : 0;
                     }
                     pq2::named_bar_sync(2, kWorkerThreads);
                     if (last_flag) {
-                        __threadfence();
-                        // per contributor, in CTA order, the loads are issued
-                        // together (one L2 round trip each)
+                        // the contributors' partials added in CTA order; the
+                        // loads of kFlushBatch contributors are in flight
+                        // together (one L2 round trip per batch)
                         float sum[kTokPerWarp];
 #pragma unroll
                         for (int j = 0; j < kTokPerWarp; ++j) sum[j] = 0.0f;
-                        for (int c = c_lo; c <= c_hi; ++c) {
-                            const float* pc = p.partial + static_cast<size_t>(c + t) * p.M * kRows + r;
-                            float v[kTokPerWarp];
+                        for (int c0 = c_lo; c0 <= c_hi; c0 += kFlushBatch) {
+                            float v[kFlushBatch][kTokPerWarp];
 #pragma unroll
-                            for (int j = 0; j < kTokPerWarp; ++j) {
-                                const int m = 4 * wq + j;
-                                v[j] = m < p.M ? ld_cg(pc + static_cast<size_t>(m) * kRows) : 0.0f;
+                            for (int b = 0; b < kFlushBatch; ++b) {
+                                const int c = c0 + b;
+                                const float* pc =
+                                    p.partial + static_cast<size_t>(c + t) * p.M * kRows + r;
+#pragma unroll
+                                for (int j = 0; j < kTokPerWarp; ++j) {
+                                    const int m = 4 * wq + j;
+                                    v[b][j] = (c <= c_hi && m < p.M)
+                                                  ? ld_cg(pc + static_cast<size_t>(m) * kRows)
+                                                  : 0.0f;
+                                }
                             }
 #pragma unroll
-                            for (int j = 0; j < kTokPerWarp; ++j) sum[j] += v[j];
+                            for (int b = 0; b < kFlushBatch; ++b)
+                                if (c0 + b <= c_hi) {
+#pragma unroll
+                                    for (int j = 0; j < kTokPerWarp; ++j) sum[j] += v[b][j];
+                                }
                         }
                         if (row < p.N) {
 #pragma unroll

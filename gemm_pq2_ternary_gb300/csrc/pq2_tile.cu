@@ -696,30 +696,34 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1) tile_kernel(const __grid_
                     const int m = 16 * tb + i;
                     if (m < p.M) part[static_cast<size_t>(m) * kRows + r] = a[i];
                 }
-                __threadfence();
                 pq2::named_bar_sync(2, kFlushThreads);
                 if (e == 0 && lane == 0) {
-                    const unsigned old = atomicAdd(&p.counters[t], 1u);
+                    const unsigned old = pq2::atom_add_acq_rel_gpu(&p.counters[t], 1u);
                     last_flag = (old == static_cast<unsigned>(c_hi - c_lo)) ? 1 : 0;
                 }
                 pq2::named_bar_sync(2, kFlushThreads);
                 if (last_flag) {
-                    __threadfence();
-                    // per contributor, in CTA order; a contributor's 16 loads
-                    // are issued together (one L2 round trip each)
+                    // the contributors' partials added in CTA order, two
+                    // contributors' loads in flight together
                     float sum[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) sum[i] = 0.0f;
-                    for (int c = c_lo; c <= c_hi; ++c) {
-                        const float* pc = p.partial + static_cast<size_t>(c + t) * p.M * kRows + r;
-                        float v[16];
+                    for (int c0 = c_lo; c0 <= c_hi; c0 += 2) {
+                        const bool two = c0 + 1 <= c_hi;
+                        const float* pa = p.partial + static_cast<size_t>(c0 + t) * p.M * kRows + r;
+                        const float* pb = pa + static_cast<size_t>(p.M) * kRows;  // contributor c0 + 1
+                        float va[16], vb[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const int m = 16 * tb + i;
-                            v[i] = m < p.M ? ld_cg(pc + static_cast<size_t>(m) * kRows) : 0.0f;
+                            va[i] = m < p.M ? ld_cg(pa + static_cast<size_t>(m) * kRows) : 0.0f;
+                            vb[i] = (two && m < p.M) ? ld_cg(pb + static_cast<size_t>(m) * kRows) : 0.0f;
                         }
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) sum[i] += v[i];
+                        for (int i = 0; i < 16; ++i) {
+                            sum[i] += va[i];
+                            if (two) sum[i] += vb[i];
+                        }
                     }
                     if (row < p.N) {
 #pragma unroll

@@ -709,15 +709,13 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                         *reinterpret_cast<float4*>(pr + 16 * (j >> 1) + 4 * (j & 1)) =
                             make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
                 }
-                __threadfence();
                 pq2::named_bar_sync(2, kEpiThreads);
                 if (warp == 0 && lane == 0) {  // quadrant 0, column block 0
-                    const unsigned old = atomicAdd(&p.counters[t], 1u);
+                    const unsigned old = pq2::atom_add_acq_rel_gpu(&p.counters[t], 1u);
                     last_flag = (old == static_cast<unsigned>(c_hi - c_lo)) ? 1 : 0;
                 }
                 pq2::named_bar_sync(2, kEpiThreads);
                 if (last_flag && m < p.M) {
-                    __threadfence();
                     // the contributors' partials added in CTA order, 16 columns
                     // at a time, two contributors' loads in flight together
                     float* yr = p.y + static_cast<size_t>(m) * p.N;
