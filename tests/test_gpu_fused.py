@@ -154,14 +154,18 @@ def test_static_weights_fall_back_where_slices_are_too_large(prob):
     assert torch.equal(y0, y1)
 
 
-FEW_TOKEN_STATIC = [inputs.Problem(f"static_m{M}_k{K}_n{N}", M, K, N, "p343", "outliers", 90 + M)
-                    for M in (2, 3, 4) for (K, N) in inputs.SMALL_SHAPES]
+FEW_TOKEN_STATIC = ([inputs.Problem(f"static_m{M}_k{K}_n{N}", M, K, N, "p343", "outliers", 90 + M)
+                     for M in (2, 3, 4, 5, 8, 16) for (K, N) in inputs.SMALL_SHAPES] +
+                    # fewer items per CTA than the producer's stages, ragged N and G
+                    [inputs.Problem("static_m8_k384_n300", 8, 384, 300, "p343", "outliers", 89),
+                     inputs.Problem("static_m16_k1664_n200", 16, 1664, 200, "uniform", "outliers", 88)])
 
 
 @pytest.mark.parametrize("prob", FEW_TOKEN_STATIC, ids=lambda p: p.name)
 def test_static_weights_few_tokens_match_default_path(prob):
-    """2 to 4 tokens: with PQ2_WEIGHTS_STATIC the DP4A kernel requests its
-    weights before the dependency wait; y is bit-identical to pq2_matmul."""
+    """2 to 16 tokens: with PQ2_WEIGHTS_STATIC the DP4A kernel (2-4 tokens)
+    requests its weights before the dependency wait, and the tensor-core
+    kernel (5-16) ignores the flag; y is bit-identical to pq2_matmul."""
     from gemm_pq2_ternary_gb300 import binding as pq2
     from gemm_pq2_ternary_gb300.binding import alloc_workspace, PQ2_OP_MATMUL
     tern, ws, x = inputs.generate(prob)
