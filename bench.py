@@ -244,11 +244,12 @@ def per_layer_units(layer, kind, name=""):
 
 
 def layer_launches(layer, name=""):
-    """Kernel launches of one layer: the fused quantise + GEMV for M = 1;
-    quantise and the DP4A matmul for 2-4 tokens; quantise, token
-    preparation and matmul otherwise; SwiGLU-quantise and
-    the matmul (plus its preparation for M > 1) for a chained down
-    projection; one split-K launch for a bf16 projection."""
+    """Kernel launches of one layer (pq2_matmul_ex per projection): the fused
+    quantise + GEMV for M = 1; quantise and the DP4A matmul for 2-4 tokens;
+    quantise-into-token-tiles and the tensor-core matmul up to 16 tokens;
+    quantise, token preparation and matmul above; SwiGLU-quantise and the
+    matmul (plus its preparation for M > 1) for a chained down projection;
+    one split-K launch for a bf16 projection."""
     chain = chain_of(name)
     n = 0
     for j, (M, K, N, cdist, _) in enumerate(layer):
@@ -257,7 +258,7 @@ def layer_launches(layer, name=""):
         elif chain and j == chain[1]:
             n += 2 if M == 1 or small_takes_dp4a(M, N, K) else 3
         else:
-            n += 1 if M == 1 else (2 if small_takes_dp4a(M, N, K) else 3)
+            n += 1 if M == 1 else (2 if M <= 16 else 3)
     return n
 
 
@@ -402,9 +403,12 @@ def run_matmul(pq2, p, flags=0):
 
 
 def step_fn(pq2, layers, matmul_only=False, flags=0):
-    """One pass: per projection, M = 1 runs pq2_matmul_ex (the fused quantise +
-    GEMV kernel); M > 1 runs pq2_quantize_act then the matmul kernel (the
-    matmul alone when matmul_only)."""
+    """One pass: per projection, pq2_matmul_ex (the public call from fp16
+    activations: the fused quantise + GEMV kernel for M = 1; for 5-16 tokens
+    a kernel that quantises straight into the tensor-core kernel's token
+    tiles, then that kernel; otherwise pq2_quantize_act, then the matmul);
+    with matmul_only, the matmul entry point alone on activations quantised
+    beforehand (its preparation kernel included)."""
     def fn():
         for projs in layers:
             for p in projs:
@@ -414,11 +418,9 @@ def step_fn(pq2, layers, matmul_only=False, flags=0):
                 if "gu" in p:  # down projection from the gate/up output
                     pq2.pq2_mlp_down_swiglu(p["gu"], p["codes"], p["ws"], p["y"], p["swws"])
                     continue
-                if p["M"] == 1:
+                if p["M"] == 1 or not matmul_only:
                     pq2.pq2_matmul_ex(p["x"], p["codes"], p["ws"], p["y"], flags, p["mmws"])
                     continue
-                if not matmul_only:
-                    pq2.pq2_quantize_act(p["x"], p["qp"], p["S"], p["T"])
                 run_matmul(pq2, p, flags)
     return fn
 

@@ -80,6 +80,15 @@ cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, con
                          const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
                          int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                          const DeviceInfo& dev);
+// pq2_matmul's path for the calls pq2_gemm_small sends to small_kernel
+// (small_x_supported): one kernel quantises the fp16 activations straight
+// into small_kernel's token tiles and (s, t) table (no qp, S, T), then
+// small_kernel; y is bit-identical to pq2_quantize_act + pq2_gemm_small.
+// workspace: small_workspace_bytes(M, N, K) bytes.
+bool small_x_supported(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_small_x(const __half* x, const uint8_t* codes, const __half* ws, float* y,
+                           int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st,
+                           const pq2::DevCtl& ctl, const DeviceInfo& dev);
 
 // 1 <= M <= kTileMaxM: the weights-stationary token-tile kernel
 // (pq2_tile.cu): weights expanded into tensor memory, 16, 32 or 64 token

@@ -209,3 +209,42 @@ def test_static_weights_few_tokens_back_to_back():
     assert pq2.pq2_last_device_error() == pq2.PQ2_OK
     for a, b in zip(outs, want):
         assert torch.equal(a, b)
+
+
+# pq2_matmul for 2-16 tokens on the tensor-core small-batch kernel: one kernel
+# quantises x straight into the kernel's token tiles and (s, t) table.  y must
+# be bit-identical to pq2_quantize_act + pq2_gemm_small (the same per-group
+# quantiser), and within the fp32 tolerance of the oracle; tokens past M, G
+# not a multiple of 4, ragged N, an all-zero group and 2-4 tokens at a shape
+# the DP4A kernel cannot take are covered.
+SMALL_FROM_X = ([inputs.Problem(f"smx_m{M}_k{K}_n{N}", M, K, N, "p343", "outliers", 110 + M)
+                 for M in (5, 8, 16) for (K, N) in inputs.SMALL_SHAPES] +
+                [inputs.Problem("smx_m7_k640_n300", 7, 640, 300, "uniform", "outliers", 120),
+                 inputs.Problem("smx_m13_k1664_n1000", 13, 1664, 1000, "p343", "normal", 121),
+                 inputs.Problem("smx_m3_k24576_n640", 3, 24576, 640, "p343", "outliers", 122)])
+
+
+@pytest.mark.parametrize("prob", SMALL_FROM_X, ids=lambda p: p.name)
+def test_matmul_small_from_x_matches_two_step_path(prob):
+    from gemm_pq2_ternary_gb300 import binding as pq2
+    from gemm_pq2_ternary_gb300.binding import alloc_workspace, PQ2_OP_MATMUL, PQ2_OP_SMALL
+    tern, ws, x = inputs.generate(prob)
+    x[prob.M - 1, 128:256] = 0  # an all-zero group
+    codes, ws_d = pq2.pack(torch.from_numpy(tern).cuda(), torch.from_numpy(ws).cuda())
+    xd = torch.from_numpy(x).cuda()
+    y1 = torch.full((prob.M, prob.N), float("nan"), device="cuda")
+    pq2.pq2_matmul(xd, codes, ws_d, y1, alloc_workspace(PQ2_OP_MATMUL, prob.M, prob.N, prob.K))
+    qp, S, T = pq2.quantize(xd)
+    y2 = torch.full((prob.M, prob.N), float("nan"), device="cuda")
+    pq2.pq2_gemm_small(qp, S, T, codes, ws_d, y2, alloc_workspace(PQ2_OP_SMALL, prob.M, prob.N, prob.K))
+    torch.cuda.synchronize()
+    assert pq2.pq2_last_device_error() == pq2.PQ2_OK
+    assert torch.equal(y1, y2)
+    oqp, oS, _ = oracle.quantize_act(x)
+    ocodes = oracle.pack(tern)
+    rng = np.random.default_rng(3)
+    ms = np.concatenate([rng.integers(0, prob.M, 512), [0, prob.M - 1]])
+    ns = np.concatenate([rng.integers(0, prob.N, 512), [prob.N - 1, 0]])
+    ref, A = oracle.matmul_entries(oqp, oS, ocodes, ws, ms, ns)
+    err = np.abs(y1.cpu().numpy()[ms, ns].astype(np.float64) - ref)
+    assert np.all(err <= oracle.fp32_tolerance(ref, A, prob.K // 128)), f"max err {err.max()}"
