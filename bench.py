@@ -246,10 +246,11 @@ def per_layer_units(layer, kind, name=""):
 def layer_launches(layer, name=""):
     """Kernel launches of one layer (pq2_matmul_ex per projection): the fused
     quantise + GEMV for M = 1; quantise and the DP4A matmul for 2-4 tokens;
-    quantise-into-token-tiles and the tensor-core matmul up to 16 tokens;
-    quantise, token preparation and matmul above; SwiGLU-quantise and the
-    matmul (plus its preparation for M > 1) for a chained down projection;
-    one split-K launch for a bf16 projection."""
+    quantise-into-token-tiles and the token-tile matmul wherever a token-tile
+    kernel takes the call (up to 16 tokens, and 17-64 on tile_kernel or
+    wtile_kernel); quantise, token preparation and matmul for the 128-token
+    kernels; SwiGLU-quantise and the matmul (plus its preparation for M > 1)
+    for a chained down projection; one split-K launch for a bf16 projection."""
     chain = chain_of(name)
     n = 0
     for j, (M, K, N, cdist, _) in enumerate(layer):
@@ -257,8 +258,11 @@ def layer_launches(layer, name=""):
             n += 1
         elif chain and j == chain[1]:
             n += 2 if M == 1 or small_takes_dp4a(M, N, K) else 3
+        elif M == 1:
+            n += 1
         else:
-            n += 1 if M == 1 else (2 if M <= 16 else 3)
+            n += 2 if kernel_family([(M, K, N, cdist, None)]) in ("small", "multi", "tile", "wtile") \
+                else 3
     return n
 
 

@@ -396,19 +396,29 @@ pq2_status pq2_matmul_ex(const void* x_f16, const uint8_t* codes, const void* ws
     int32_t* T = reinterpret_cast<int32_t*>(w);
     w += align256(static_cast<size_t>(M) * G * 4);
     const size_t rest = need - static_cast<size_t>(w - static_cast<uint8_t*>(workspace));
-    if (M <= 16) {
-        // the tensor-core small-batch kernel: its token tiles straight from x
-        // (one launch fewer; y bit-identical)
+    if (M > 1 && M <= pq2h::kTileMaxM) {
+        // the token-tile tensor-core kernels: their token tiles straight from
+        // x (one launch fewer; y bit-identical to quantise + the matmul)
         Ctx c;
         s = get_ctx(&c);
         if (s != PQ2_OK) return s;
-        if (pq2h::small_x_supported(M, N, K, c.dev.num_sms)) {
+        const int tt = M <= 16 ? (pq2h::small_x_supported(M, N, K, c.dev.num_sms) ? 3 : 0)
+                               : pq2h::prefill_token_tile_kernel(M, N, K, c.dev.num_sms);
+        if (tt != 0) {
             if (!aligned16(x_f16) || !aligned16(codes) || !aligned16(ws_f16) || !aligned16(y))
                 return PQ2_ERR_MISALIGNED;
-            if (rest < pq2_workspace_bytes(PQ2_OP_SMALL, M, N, K)) return PQ2_ERR_WORKSPACE;
-            return cuda_status(pq2h::launch_small_x(
-                static_cast<const __half*>(x_f16), codes, static_cast<const __half*>(ws_f16), y, M,
-                N, K, w, static_cast<cudaStream_t>(stream), c.ctl, c.dev));
+            const int op = M <= 16 ? PQ2_OP_SMALL : PQ2_OP_PREFILL;
+            if (rest < pq2_workspace_bytes(op, M, N, K)) return PQ2_ERR_WORKSPACE;
+            const __half* xh = static_cast<const __half*>(x_f16);
+            const __half* wsh = static_cast<const __half*>(ws_f16);
+            const cudaStream_t st = static_cast<cudaStream_t>(stream);
+            if (tt == 3)
+                return cuda_status(pq2h::launch_small_x(xh, codes, wsh, y, M, N, K, w, st, c.ctl,
+                                                        c.dev));
+            if (tt == 2)
+                return cuda_status(pq2h::launch_wtile_x(xh, codes, wsh, y, M, N, K, w, st, c.ctl,
+                                                        c.dev));
+            return cuda_status(pq2h::launch_tile_x(xh, codes, wsh, y, M, N, K, w, st, c.ctl, c.dev));
         }
     }
     s = pq2_quantize_act(x_f16, M, K, qp, S, T, stream);

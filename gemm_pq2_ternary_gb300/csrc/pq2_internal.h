@@ -100,6 +100,11 @@ cudaError_t launch_tile(const int8_t* qp, const float* S, const int32_t* T, cons
                         const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N, int64_t K,
                         void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                         const DeviceInfo& dev);
+// The same from the fp16 activations x [M][K]: one kernel quantises x
+// straight into the token tiles (see pq2_tokens.cuh); y bit-identical.
+cudaError_t launch_tile_x(const __half* x, const uint8_t* codes, const __half* ws, float* y,
+                          int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st,
+                          const pq2::DevCtl& ctl, const DeviceInfo& dev);
 
 // 1 <= M <= kTileMaxM: the weights-wide token-tile kernel (pq2_wtile.cu):
 // 128 expanded weight rows per MMA, the tokens' hi and lo parts as the
@@ -118,6 +123,9 @@ cudaError_t launch_wtile(const int8_t* qp, const float* S, const int32_t* T, con
                          const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,
                          int64_t K, void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                          const DeviceInfo& dev);
+cudaError_t launch_wtile_x(const __half* x, const uint8_t* codes, const __half* ws, float* y,
+                           int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st,
+                           const pq2::DevCtl& ctl, const DeviceInfo& dev);
 
 // Back-to-back tcgen05 e4m3 MMAs (M = 128, N = n, K = 32) on every SM:
 // cycles[sm] = clock cycles for `iters` of them (pq2_debug_mma_rate).
@@ -133,6 +141,10 @@ cudaError_t launch_small_tc(const int8_t* qp, const float* S, const int32_t* T,
                             const uint8_t* codes, const __half* ws, float* y, int32_t* dots,
                             int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st,
                             const pq2::DevCtl& ctl, const DeviceInfo& dev);
+
+// The token-tile kernel pq2_gemm_prefill runs for this call (its routing):
+// 1 tile_kernel, 2 wtile_kernel, 0 a 128-token tile kernel.
+int prefill_token_tile_kernel(int64_t M, int64_t N, int64_t K, int num_sms);
 
 // Any M: tcgen05 tensor-core kernel (token planes prepared in the workspace).
 size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K);

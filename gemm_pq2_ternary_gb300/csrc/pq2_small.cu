@@ -54,6 +54,7 @@
 //               epilogue of item i-1 (the four warps take 4 tokens each)
 // Every mbarrier wait is bounded (device error word on expiry).
 #include "pq2_internal.h"
+#include "pq2_tokens.cuh"
 
 namespace {
 
@@ -177,73 +178,17 @@ __global__ void __launch_bounds__(256) small_prep_kernel(const int8_t* __restric
     for (int64_t i = i0; i < n_tiles; i += stride) counters[i] = 0u;
 }
 
-// The same token tiles, (s, t) table and counters straight from the fp16
-// activations x [M][K] (pq2_matmul's path: qp, S and T are not needed by
-// small_kernel, so they are not written).  Eight lanes quantise one
-// (group, token) as pq2_quantize_act does (the shared per-group step), keep
-// their four plane words in a shared slot, and write them as e4m3 hi and lo
-// rows; (group, token) pairs past M or G get zeros.
-__global__ void __launch_bounds__(256) small_quant_prep_kernel(const __half* __restrict__ x,
-                                                               uint32_t* __restrict__ tok,
-                                                               float2* __restrict__ st16,
-                                                               unsigned* __restrict__ counters,
-                                                               int64_t M, int64_t K, int64_t G4,
-                                                               int n_tiles) {
-    __shared__ __align__(16) int8_t qslot[8][4][128];  // [warp][team] one group's q
-    __shared__ float sslot[8][4];
-    __shared__ int32_t tslot[8][4];
-    pq2::pdl_wait();
-    pq2::pdl_launch_dependents();
-    const int64_t G = K / 128;
-    const int lane = threadIdx.x & 31;
-    const int wib = threadIdx.x >> 5;  // warp in the block
-    const int team = lane >> 3;
-    const int j = lane & 7;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t pairs = G4 * kTok;  // (group, token) pairs, token-minor
-    int8_t* qs = qslot[wib][team];
-    for (int64_t i0 = warp * 4; i0 < pairs; i0 += nwarps * 4) {
-        const int64_t i = i0 + team;
-        const int64_t g = i / kTok;
-        const int m = static_cast<int>(i - g * kTok);
-        const bool valid = i < pairs && m < M && g < G;
-        // every lane takes part in the team's shuffles; a team without a
-        // valid pair reads token 0's group 0 and stores nothing
-        const __half* src = x + (valid ? static_cast<int64_t>(m) * K + g * 128 : 0) + 16 * j;
-        const uint4 h[2] = {pq2::ld_nc_v4(reinterpret_cast<const uint4*>(src)),
-                            pq2::ld_nc_v4(reinterpret_cast<const uint4*>(src) + 1)};
-        float s_all;
-        int t_all;
-        pq2::quantize_group8(h, j, valid, qs, &sslot[wib][team], &tslot[wib][team], s_all, t_all);
-        if (i >= pairs) continue;
-        // this lane's plane words: bytes 4j..4j+3 of plane s (its own stores)
-        uint32_t* tg = tok + g * (2 * kTok * 32);
-        const int rh = 8 * (m / 4) + (m % 4);
-#pragma unroll
-        for (int sp = 0; sp < 4; ++sp) {
-            uint32_t hw = 0, lw = 0;
-            if (valid) {
-                const uint32_t qw = *reinterpret_cast<const uint32_t*>(qs + sp * 32 + 4 * j);
-                float hv[4], lv[4];
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int q = static_cast<int8_t>((qw >> (8 * b)) & 0xFFu);
-                    hv[b] = static_cast<float>(16 * (q >> 4));  // 16 * floor(q / 16), exact in e4m3
-                    lv[b] = static_cast<float>(q & 15);         // q - 16 * floor(q / 16)
-                }
-                hw = e4m3x4(hv[0], hv[1], hv[2], hv[3]);
-                lw = e4m3x4(lv[0], lv[1], lv[2], lv[3]);
-            }
-            tg[rh * 32 + sp * 8 + j] = hw;
-            tg[(rh + 4) * 32 + sp * 8 + j] = lw;
-        }
-        if (j == 0) st16[i] = valid ? make_float2(s_all, static_cast<float>(t_all)) : make_float2(0.0f, 0.0f);
+// Layout of the token tiles for quant_tiles_kernel (pq2_matmul's path: the
+// same tiles, (s, t) table and counters straight from the fp16 activations).
+struct SmallTok {
+    static constexpr int MT = kTok;
+    static constexpr int kGroupWords = 2 * kTok * 32;
+    __device__ static int row_hi(int m) { return 8 * (m / 4) + (m % 4); }
+    __device__ static int row_lo(int m) { return 8 * (m / 4) + (m % 4) + 4; }
+    __device__ static void put_st(void* st, int64_t g, int m, float s, float t) {
+        static_cast<float2*>(st)[g * kTok + m] = make_float2(s, t);
     }
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t k = tid; k < n_tiles; k += nthreads) counters[k] = 0u;
-}
+};
 
 // ---------------------------------------------------------------------------
 // tcgen05 helpers
@@ -846,13 +791,10 @@ cudaError_t launch_small_x(const __half* x, const uint8_t* codes, const __half* 
     const SmallLayout l = layout_small(M, N, K, dev.num_sms);
     uint8_t* w = static_cast<uint8_t*>(workspace);
     {
-        const int64_t pairs = l.G4 * kTok;
-        const int64_t want = (pairs + 31) / 32;  // 8 warps x 4 pairs per block
-        const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
-        const int grid = static_cast<int>(want < cap ? want : cap);
-        cudaError_t e = launch(small_quant_prep_kernel, dim3(grid), dim3(256), 0, st, true, x,
-                               reinterpret_cast<uint32_t*>(w + l.tok),
-                               reinterpret_cast<float2*>(w + l.st16),
+        cudaError_t e = launch(pq2::quant_tiles_kernel<SmallTok>,
+                               dim3(pq2::quant_tiles_grid(l.G4 * kTok, dev.num_sms)), dim3(256), 0,
+                               st, true, x, reinterpret_cast<uint32_t*>(w + l.tok),
+                               static_cast<void*>(w + l.st16),
                                reinterpret_cast<unsigned*>(w + l.counters), M, K, l.G4, l.n_tiles);
         if (e != cudaSuccess) return e;
     }

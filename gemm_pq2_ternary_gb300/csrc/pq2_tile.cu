@@ -60,6 +60,7 @@
 //                 group parities are added at the flush (even + odd)
 // Every mbarrier wait is bounded (device error word on expiry).
 #include "pq2_internal.h"
+#include "pq2_tokens.cuh"
 
 namespace {
 
@@ -858,8 +859,26 @@ TileLayout layout_tile(int64_t M, int64_t N, int64_t K, int num_sms) {
     return l;
 }
 
+// Layout of the token tiles for quant_tiles_kernel (pq2_matmul's path: the
+// same tiles, (s, t) table and counters straight from the fp16 activations).
+template <int T>
+struct TileTok {
+    static constexpr int MT = T;
+    static constexpr int kGroupWords = Cfg<T>::NB * 32;
+    __device__ static int row_hi(int m) { return Cfg<T>::HL == 2 ? 8 * (m / 4) + (m % 4) : m; }
+    __device__ static int row_lo(int m) {
+        return Cfg<T>::HL == 2 ? 8 * (m / 4) + (m % 4) + 4 : T + m;
+    }
+    __device__ static void put_st(void* st, int64_t g, int m, float s, float t) {
+        float* f = static_cast<float*>(st);
+        f[(g * 2) * T + m] = s;
+        f[(g * 2 + 1) * T + m] = t;
+    }
+};
+
 template <int MT>
-cudaError_t launch_mt(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
+cudaError_t launch_mt(const __half* x, const int8_t* qp, const float* S, const int32_t* T,
+                      const uint8_t* codes,
                       const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N, int64_t K,
                       const TileLayout& l, uint8_t* w, cudaStream_t st, const pq2::DevCtl& ctl,
                       const pq2h::DeviceInfo& dev) {
@@ -867,7 +886,14 @@ cudaError_t launch_mt(const int8_t* qp, const float* S, const int32_t* T, const 
     uint32_t* tok = reinterpret_cast<uint32_t*>(w + l.tok);
     float* stv = reinterpret_cast<float*>(w + l.st);
     unsigned* counters = reinterpret_cast<unsigned*>(w + l.counters);
-    {
+    if (x) {
+        // pq2_matmul's path: the tiles straight from the fp16 activations
+        cudaError_t e = pq2h::launch(pq2::quant_tiles_kernel<TileTok<MT>>,
+                                     dim3(pq2::quant_tiles_grid(l.G4 * MT, dev.num_sms)), dim3(256),
+                                     0, st, true, x, tok, static_cast<void*>(stv), counters, M, K,
+                                     l.G4, l.n_tiles);
+        if (e != cudaSuccess) return e;
+    } else {
         const int64_t words = l.G4 * MT * 32;
         const int64_t want = (words + 255) / 256;
         const int grid = static_cast<int>(want < dev.num_sms * 4 ? want : dev.num_sms * 4);
@@ -904,6 +930,21 @@ cudaError_t launch_mt(const int8_t* qp, const float* S, const int32_t* T, const 
     return pq2h::launch(kern, dim3(l.grid), dim3(C::THREADS), C::SMEM, st, true, p);
 }
 
+// x != nullptr: the token tiles straight from x (qp, S, T unused)
+cudaError_t launch_tile_any(const __half* x, const int8_t* qp, const float* S, const int32_t* T,
+                           const uint8_t* codes, const __half* ws, float* y, int32_t* dots,
+                           int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st,
+                           const pq2::DevCtl& ctl, const pq2h::DeviceInfo& dev) {
+    if (M < 1 || M > pq2h::kTileMaxM) return cudaErrorInvalidValue;
+    const TileLayout l = layout_tile(M, N, K, dev.num_sms);
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    if (l.mt == 16)
+        return launch_mt<16>(x, qp, S, T, codes, ws, y, dots, M, N, K, l, w, st, ctl, dev);
+    if (l.mt == 32)
+        return launch_mt<32>(x, qp, S, T, codes, ws, y, dots, M, N, K, l, w, st, ctl, dev);
+    return launch_mt<64>(x, qp, S, T, codes, ws, y, dots, M, N, K, l, w, st, ctl, dev);
+}
+
 }  // namespace
 
 namespace pq2h {
@@ -920,12 +961,14 @@ cudaError_t launch_tile(const int8_t* qp, const float* S, const int32_t* T, cons
                         const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N, int64_t K,
                         void* workspace, cudaStream_t st, const pq2::DevCtl& ctl,
                         const DeviceInfo& dev) {
-    if (M < 1 || M > kTileMaxM) return cudaErrorInvalidValue;
-    const TileLayout l = layout_tile(M, N, K, dev.num_sms);
-    uint8_t* w = static_cast<uint8_t*>(workspace);
-    if (l.mt == 16) return launch_mt<16>(qp, S, T, codes, ws, y, dots, M, N, K, l, w, st, ctl, dev);
-    if (l.mt == 32) return launch_mt<32>(qp, S, T, codes, ws, y, dots, M, N, K, l, w, st, ctl, dev);
-    return launch_mt<64>(qp, S, T, codes, ws, y, dots, M, N, K, l, w, st, ctl, dev);
+    return launch_tile_any(nullptr, qp, S, T, codes, ws, y, dots, M, N, K, workspace, st, ctl, dev);
+}
+
+cudaError_t launch_tile_x(const __half* x, const uint8_t* codes, const __half* ws, float* y,
+                          int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st,
+                          const pq2::DevCtl& ctl, const DeviceInfo& dev) {
+    return launch_tile_any(x, nullptr, nullptr, nullptr, codes, ws, y, nullptr, M, N, K, workspace,
+                          st, ctl, dev);
 }
 
 cudaError_t launch_mma_rate(int n, int iters, unsigned long long* cycles, cudaStream_t st,

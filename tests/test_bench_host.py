@@ -21,7 +21,8 @@ def _args(workload, m=1, shape="5120,17408"):
     ("decode", 1, 6144 * 5120 // 4 + 2 * 5120 * 48 + 2 * 6144 + 4 * 5120, 1),
     ("small", 16, None, 2),  # quantise into the token tiles, then small_kernel
     ("small", 4, None, 2),   # quantise, then the DP4A kernel
-    ("mid", 32, None, 3),    # quantise, token preparation, tile_kernel
+    ("mid", 32, None, 2),    # quantise into the token tiles, then tile_kernel
+    ("mid", 64, None, 3),    # quantise, token preparation, prefill_kernel (9 items a CTA)
     ("mlp_swiglu", 1, None, 1 + 2),
     ("in_proj_ba", 4, 2 * (96 * 5120 + 4 * 5120 + 4 * 96), 1),
     ("prefill", 128, 2.0 * 128 * 17408 * 5120, 3),

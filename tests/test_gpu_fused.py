@@ -248,3 +248,41 @@ def test_matmul_small_from_x_matches_two_step_path(prob):
     ref, A = oracle.matmul_entries(oqp, oS, ocodes, ws, ms, ns)
     err = np.abs(y1.cpu().numpy()[ms, ns].astype(np.float64) - ref)
     assert np.all(err <= oracle.fp32_tolerance(ref, A, prob.K // 128)), f"max err {err.max()}"
+
+
+# The same for 17-64 tokens where pq2_gemm_prefill takes a token-tile kernel
+# (tile_kernel up to 32 tokens, wtile_kernel from 33 where a CTA gets few
+# items): y bit-identical to pq2_quantize_act + pq2_gemm_prefill.
+PREFILL_FROM_X = [inputs.Problem("pfx_m17_k5120_n17408", 17, 5120, 17408, "p343", "outliers", 130),
+                  inputs.Problem("pfx_m32_k6144_n5120", 32, 6144, 5120, "p343", "outliers", 131),
+                  inputs.Problem("pfx_m24_k640_n300", 24, 640, 300, "uniform", "outliers", 132),
+                  inputs.Problem("pfx_m33_k6144_n5120", 33, 6144, 5120, "p343", "outliers", 133),
+                  inputs.Problem("pfx_m64_k6144_n5120", 64, 6144, 5120, "p343", "outliers", 134),
+                  inputs.Problem("pfx_m50_k1664_n700", 50, 1664, 700, "uniform", "normal", 135),
+                  inputs.Problem("pfx_m48_k5120_n17408", 48, 5120, 17408, "p343", "outliers", 136)]
+
+
+@pytest.mark.parametrize("prob", PREFILL_FROM_X, ids=lambda p: p.name)
+def test_matmul_token_tiles_from_x_match_two_step_path(prob):
+    from gemm_pq2_ternary_gb300 import binding as pq2
+    from gemm_pq2_ternary_gb300.binding import alloc_workspace, PQ2_OP_MATMUL, PQ2_OP_PREFILL
+    tern, ws, x = inputs.generate(prob)
+    x[prob.M - 1, 128:256] = 0  # an all-zero group
+    codes, ws_d = pq2.pack(torch.from_numpy(tern).cuda(), torch.from_numpy(ws).cuda())
+    xd = torch.from_numpy(x).cuda()
+    y1 = torch.full((prob.M, prob.N), float("nan"), device="cuda")
+    pq2.pq2_matmul(xd, codes, ws_d, y1, alloc_workspace(PQ2_OP_MATMUL, prob.M, prob.N, prob.K))
+    qp, S, T = pq2.quantize(xd)
+    y2 = torch.full((prob.M, prob.N), float("nan"), device="cuda")
+    pq2.pq2_gemm_prefill(qp, S, T, codes, ws_d, y2,
+                         alloc_workspace(PQ2_OP_PREFILL, prob.M, prob.N, prob.K))
+    torch.cuda.synchronize()
+    assert pq2.pq2_last_device_error() == pq2.PQ2_OK
+    assert torch.equal(y1, y2)
+    oqp, oS, _ = oracle.quantize_act(x)
+    rng = np.random.default_rng(4)
+    ms = np.concatenate([rng.integers(0, prob.M, 512), [0, prob.M - 1]])
+    ns = np.concatenate([rng.integers(0, prob.N, 512), [prob.N - 1, 0]])
+    ref, A = oracle.matmul_entries(oqp, oS, oracle.pack(tern), ws, ms, ns)
+    err = np.abs(y1.cpu().numpy()[ms, ns].astype(np.float64) - ref)
+    assert np.all(err <= oracle.fp32_tolerance(ref, A, prob.K // 128)), f"max err {err.max()}"
