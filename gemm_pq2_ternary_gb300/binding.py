@@ -21,6 +21,7 @@ PQ2_ERR_MISALIGNED = 3
 PQ2_ERR_CUDA = 4
 PQ2_ERR_TIMEOUT = 5
 PQ2_ERR_WORKSPACE = 6
+PQ2_ERR_BOUNDS = 7
 
 PQ2_OP_GEMV = 0
 PQ2_OP_SMALL = 1
@@ -68,6 +69,8 @@ SIGNATURES = {
     "pq2_last_device_error": ([_P], _I),
     "pq2_debug_set_wait_limit_ns": ([_U64], _I),
     "pq2_debug_skip_stage": ([_I], _I),
+    "pq2_bounds_checked": ([], _I),
+    "pq2_debug_shrink_bounds": ([_I], _I),
     "pq2_debug_force_kernel": ([_I, _I], _I),
     "pq2_debug_gemv_floor": ([_I64, _I64, _U32, _P], _I),
     "pq2_debug_mma_rate": ([_I, _I, _P, _P], _I),
@@ -271,6 +274,14 @@ def pq2_debug_set_wait_limit_ns(ns: int):
 
 def pq2_debug_skip_stage(stage: int):
     _check(_lib.pq2_debug_skip_stage(stage), "pq2_debug_skip_stage")
+
+
+def pq2_bounds_checked() -> bool:
+    return bool(_lib.pq2_bounds_checked())
+
+
+def pq2_debug_shrink_bounds(elements: int):
+    _check(_lib.pq2_debug_shrink_bounds(elements), "pq2_debug_shrink_bounds")
 
 
 def pq2_debug_force_kernel(op: int, variant: int):

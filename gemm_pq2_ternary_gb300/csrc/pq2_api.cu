@@ -18,6 +18,7 @@ pq2h::DeviceInfo g_dev[kMaxDevices];
 bool g_dev_ok[kMaxDevices] = {};
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_debug_skip_stage{-1};
+std::atomic<int> g_debug_bounds_shrink{0};
 // pq2_debug_force_kernel: forced variant per op (GEMV, SMALL, PREFILL)
 std::atomic<int> g_force[3] = {{0}, {0}, {0}};
 
@@ -126,6 +127,7 @@ bool make_ctl(pq2::DevCtl* ctl) {
     ctl->err = d.err;
     ctl->wait_limit_ns = g_wait_limit_ns.load();
     ctl->debug_skip_stage = g_debug_skip_stage.load();
+    ctl->debug_bounds_shrink = g_debug_bounds_shrink.load();
     return true;
 }
 
@@ -142,6 +144,7 @@ const char* pq2_status_string(int status) {
         case PQ2_ERR_CUDA: return "CUDA error";
         case PQ2_ERR_TIMEOUT: return "device wait timed out";
         case PQ2_ERR_WORKSPACE: return "workspace missing or too small";
+        case PQ2_ERR_BOUNDS: return "bounds-checked build: a store outside its buffer";
         default: return "unknown status";
     }
 }
@@ -159,6 +162,14 @@ pq2_status pq2_debug_set_wait_limit_ns(uint64_t ns) {
 // timeout test only.
 pq2_status pq2_debug_skip_stage(int stage) {
     g_debug_skip_stage.store(stage < 0 ? -1 : stage);
+    return PQ2_OK;
+}
+
+int pq2_bounds_checked(void) { return PQ2_DEBUG; }
+
+pq2_status pq2_debug_shrink_bounds(int elements) {
+    if (elements < 0) return PQ2_ERR_INVALID_ARG;
+    g_debug_bounds_shrink.store(elements);
     return PQ2_OK;
 }
 
@@ -316,7 +327,7 @@ static pq2_status gemm_small(const int8_t* qp, const float* S, const int32_t* T,
         return cuda_status(pq2h::launch_gemv_multi(qp, S, T, codes,
                                                    static_cast<const __half*>(ws_f16), y, nullptr,
                                                    M, N, K, static_cast<cudaStream_t>(stream),
-                                                   c.dev, weights_static));
+                                                   c.dev, weights_static, c.ctl));
     return cuda_status(pq2h::launch_small_tc(qp, S, T, codes, static_cast<const __half*>(ws_f16), y,
                                           nullptr, M, N, K, workspace,
                                           static_cast<cudaStream_t>(stream), c.ctl, c.dev));
@@ -475,7 +486,7 @@ pq2_status pq2_gemm_bf16_splitk(const uint16_t* x, const uint16_t* w, uint16_t* 
     if (s != PQ2_OK) return s;
     return cuda_status(pq2h::launch_bf16_splitk(x, w, y, M, N, K,
                                                 (flags & PQ2_WEIGHTS_STATIC) != 0,
-                                                static_cast<cudaStream_t>(stream)));
+                                                static_cast<cudaStream_t>(stream), c.ctl));
 }
 
 pq2_status pq2_group_dots(int op, const int8_t* qp, const int32_t* T, const uint8_t* codes,
@@ -499,7 +510,7 @@ pq2_status pq2_group_dots(int op, const int8_t* qp, const int32_t* T, const uint
     if (op == PQ2_OP_SMALL) {
         if (pq2h::gemv_multi_supported(M, N, K, c.dev.num_sms))
             return cuda_status(pq2h::launch_gemv_multi(qp, nullptr, T, codes, nullptr, nullptr,
-                                                       dots, M, N, K, st, c.dev, false));
+                                                       dots, M, N, K, st, c.dev, false, c.ctl));
         return cuda_status(pq2h::launch_small_tc(qp, nullptr, T, codes, nullptr, nullptr, dots, M, N,
                                               K, workspace, st, c.ctl, c.dev));
     }
@@ -521,6 +532,7 @@ pq2_status pq2_last_device_error(void* stream) {
     if (cudaMemcpy(c.dev.err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
         return PQ2_ERR_CUDA;
     if (word & pq2::DEVERR_TIMEOUT) return PQ2_ERR_TIMEOUT;
+    if (word & pq2::DEVERR_BOUNDS) return PQ2_ERR_BOUNDS;
     if (word & pq2::DEVERR_BAD_TERNARY) return PQ2_ERR_INVALID_ARG;
     return PQ2_OK;
 }

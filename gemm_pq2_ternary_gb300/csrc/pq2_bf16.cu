@@ -86,6 +86,7 @@ struct Bf16Params {
     int M, N, K;
     int kv_per_split;    // column vectors (kVK values of K) per cluster rank
     int weights_static;  // w may be read before the preceding kernel ends
+    DevCtl ctl;
 };
 
 // A column vector: kVK consecutive bf16 values of one row (kVK = 8: 16
@@ -236,7 +237,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bf16_splitk_kernel(Bf16Params 
         for (int r = 0; r < kSplits; ++r) sum += red[r][tid];
         const int o = static_cast<int>(rank) * kOutPerRank + tid;
         const int m = m0 + o / kNT, n = n0 + o % kNT;
-        if (m < p.M && n < p.N) p.y[static_cast<size_t>(m) * p.N + n] = f32_to_bf16_rn(sum);
+        if (m < p.M && n < p.N &&
+            store_ok(p.ctl, static_cast<long long>(m) * p.N + n, 1, static_cast<long long>(p.M) * p.N))
+            p.y[static_cast<size_t>(m) * p.N + n] = f32_to_bf16_rn(sum);
     }
 }
 
@@ -246,9 +249,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bf16_splitk_kernel(Bf16Params 
 namespace pq2h {
 
 cudaError_t launch_bf16_splitk(const uint16_t* x, const uint16_t* w, uint16_t* y, int64_t M,
-                               int64_t N, int64_t K, bool weights_static, cudaStream_t stream) {
+                               int64_t N, int64_t K, bool weights_static, cudaStream_t stream,
+                               const pq2::DevCtl& ctl) {
     using namespace pq2;
     Bf16Params p = {};
+    p.ctl = ctl;
     p.x = x;
     p.w = w;
     p.y = y;

@@ -21,6 +21,7 @@ namespace pq2 {
 enum : unsigned {
     DEVERR_TIMEOUT = 1u,      // a bounded wait ran out
     DEVERR_BAD_TERNARY = 2u,  // pack met a value outside {-1,0,1}
+    DEVERR_BOUNDS = 4u,       // bounds-checked build: a store outside its buffer (skipped)
 };
 
 // Passed by value to every kernel.
@@ -28,7 +29,32 @@ struct DevCtl {
     unsigned* err;          // device error word (never null)
     unsigned long long wait_limit_ns;
     int debug_skip_stage;   // >= 0: producer withholds that stage (timeout tests)
+    int debug_bounds_shrink;  // bounds-checked build: the checks treat the last
+                              // elements of every buffer as outside (test hook)
 };
+
+// Bounds-checked build (compiled with PQ2_DEBUG=1; a separate library): every
+// store to an output or scratch buffer first asks store_ok whether its w
+// elements i .. i + w - 1 lie inside the buffer's n elements (less
+// ctl.debug_bounds_shrink).  If not, the error word gets DEVERR_BOUNDS and the
+// store is skipped, so an indexing mistake is reported instead of corrupting
+// memory.  In the normal build store_ok is the constant true.
+#ifndef PQ2_DEBUG
+#define PQ2_DEBUG 0
+#endif
+__device__ __forceinline__ bool store_ok(const DevCtl& ctl, long long i, int w, long long n) {
+#if PQ2_DEBUG
+    if (i >= 0 && i + w <= n - ctl.debug_bounds_shrink) return true;
+    atomicOr(ctl.err, DEVERR_BOUNDS);
+    return false;
+#else
+    (void)ctl;
+    (void)i;
+    (void)w;
+    (void)n;
+    return true;
+#endif
+}
 
 // ----------------------------------------------------------------------------
 // small PTX wrappers

@@ -355,7 +355,8 @@ __global__ void __launch_bounds__((GPT == 1 ? kMaxConsumersSmall : kMaxConsumers
                 s += __shfl_xor_sync(0xffffffffu, s, 4);
                 s += __shfl_xor_sync(0xffffffffu, s, 2);
                 s += __shfl_xor_sync(0xffffffffu, s, 1);
-                if (sub == 0 && r < crows) p.y[crow0 + r] = s;
+                if (sub == 0 && r < crows && pq2::store_ok(p.ctl, crow0 + r, 1, p.N))
+                    p.y[crow0 + r] = s;
             }
         }
         redb_s = (redb_s == red_s) ? red_s + 4u * red_stride : red_s;
@@ -502,7 +503,9 @@ __global__ void __launch_bounds__(kDirectConsumers + 32, 1) gemv_direct_kernel(c
             const int dot64 = pq2::group_codes_dot64(w, q, t64);
             const int r = rp + k * p.RP;
             if (DOTS) {
-                p.dots[static_cast<size_t>(n_begin + r) * p.G + gi] = dot64 >> 6;  // exact
+                if (pq2::store_ok(p.ctl, static_cast<long long>(n_begin + r) * p.G + gi, 1,
+                                  static_cast<long long>(p.N) * p.G))
+                    p.dots[static_cast<size_t>(n_begin + r) * p.G + gi] = dot64 >> 6;  // exact
             } else {
                 // float(dot64) exactly (|dot64| < 2^22) by the 1.5 * 2^23 bit trick
                 const float dotf = __fsub_rn(__int_as_float(0x4B400000 + dot64), 12582912.0f);
@@ -530,7 +533,8 @@ __global__ void __launch_bounds__(kDirectConsumers + 32, 1) gemv_direct_kernel(c
         sum += __shfl_xor_sync(0xffffffffu, sum, 4);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        if (sub == 0 && r < rows) p.y[n_begin + r] = sum;
+        if (sub == 0 && r < rows && pq2::store_ok(p.ctl, n_begin + r, 1, p.N))
+            p.y[n_begin + r] = sum;
     }
 }
 
@@ -777,7 +781,8 @@ __global__ void __launch_bounds__(kStagedThreads, 2) gemv_staged_kernel(const Ge
         sum += __shfl_xor_sync(0xffffffffu, sum, 4);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        if (sub == 0 && r < rows) p.y[n_begin + r] = sum;
+        if (sub == 0 && r < rows && pq2::store_ok(p.ctl, n_begin + r, 1, p.N))
+            p.y[n_begin + r] = sum;
     }
 }
 

@@ -40,7 +40,8 @@ cudaError_t launch_quantize_swiglu(const float* gu, int8_t* qp, float* S, int32_
 // y = bf16(x . w^T), bf16 operands as 16-bit patterns, split-K over a
 // cluster of CTAs with a fixed-order reduction (pq2_bf16.cu).
 cudaError_t launch_bf16_splitk(const uint16_t* x, const uint16_t* w, uint16_t* y, int64_t M,
-                               int64_t N, int64_t K, bool weights_static, cudaStream_t stream);
+                               int64_t N, int64_t K, bool weights_static, cudaStream_t stream,
+                               const pq2::DevCtl& ctl);
 
 cudaError_t launch_pack(const int8_t* tern, uint8_t* codes, int64_t N, int64_t K,
                         cudaStream_t st, const pq2::DevCtl& ctl, const DeviceInfo& dev);
@@ -74,7 +75,7 @@ bool gemv_multi_supported(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_gemv_multi(const int8_t* qp, const float* S, const int32_t* T,
                               const uint8_t* codes, const __half* ws, float* y, int32_t* dots,
                               int64_t M, int64_t N, int64_t K, cudaStream_t st,
-                              const DeviceInfo& dev, bool weights_static);
+                              const DeviceInfo& dev, bool weights_static, const pq2::DevCtl& ctl);
 
 cudaError_t launch_small(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
                          const __half* ws, float* y, int32_t* dots, int64_t M, int64_t N,

@@ -45,6 +45,7 @@ struct MultiParams {
     int TC;                 // consumer threads (multiple of 32)
     int rows_per_cta;
     uint32_t codes_row_bytes;
+    pq2::DevCtl ctl;
 };
 
 template <int MT, bool DOTS, bool STATIC>
@@ -147,7 +148,9 @@ __global__ void __launch_bounds__(kMultiConsumers, 1) gemv_multi_kernel(const Mu
             const int dot64 = pq2::group_codes_dot64(w, q, t64);
             const int r = rp + k * p.RP;
             if (DOTS) {
-                if (mvalid)
+                if (mvalid &&
+                    pq2::store_ok(p.ctl, (static_cast<long long>(mt) * p.N + n_begin + r) * p.G + gi,
+                                  1, static_cast<long long>(p.M) * p.N * p.G))
                     p.dots[(static_cast<size_t>(mt) * p.N + n_begin + r) * p.G + gi] =
                         dot64 >> 6;  // exact
             } else {
@@ -179,7 +182,8 @@ __global__ void __launch_bounds__(kMultiConsumers, 1) gemv_multi_kernel(const Mu
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         const int r = pr / MT, m = pr - r * MT;
-        if (sub == 0 && pr < pairs && m < p.M)
+        if (sub == 0 && pr < pairs && m < p.M &&
+            pq2::store_ok(p.ctl, static_cast<long long>(m) * p.N + n_begin + r, 1, static_cast<long long>(p.M) * p.N))
             p.y[static_cast<size_t>(m) * p.N + n_begin + r] = sum;
     }
 }
@@ -223,10 +227,11 @@ bool gemv_multi_supported(int64_t M, int64_t N, int64_t K, int num_sms) {
 cudaError_t launch_gemv_multi(const int8_t* qp, const float* S, const int32_t* T,
                               const uint8_t* codes, const __half* ws, float* y, int32_t* dots,
                               int64_t M, int64_t N, int64_t K, cudaStream_t st,
-                              const DeviceInfo& dev, bool weights_static) {
+                              const DeviceInfo& dev, bool weights_static, const pq2::DevCtl& ctl) {
     if (!gemv_multi_supported(M, N, K, dev.num_sms)) return cudaErrorInvalidValue;
     const int mt = tokens_per_pass(M);
     MultiParams p = {};
+    p.ctl = ctl;
     p.qp = qp;
     p.S = S;
     p.T = T;

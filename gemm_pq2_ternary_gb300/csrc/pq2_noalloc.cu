@@ -72,7 +72,7 @@ pq2_status pq2_gemm_small_noalloc(const int8_t* qp, const float* S, const int32_
     if (pq2h::gemv_multi_supported(M, N, K, dev.num_sms))  // needs no scratch
         return pq2h::launch_gemv_multi(qp, S, T, codes, static_cast<const __half*>(ws_f16), y,
                                        nullptr, M, N, K, static_cast<cudaStream_t>(stream),
-                                       dev, false) == cudaSuccess
+                                       dev, false, ctl) == cudaSuccess
                    ? PQ2_OK
                    : PQ2_ERR_CUDA;
     // scratch this shape needs on this device (split-K partial sums)

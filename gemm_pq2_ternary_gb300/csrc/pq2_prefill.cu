@@ -462,7 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                             for (int j = 0; j < 32; ++j) {
                                 const float dot = fmaf(d[j], 512.0f, -stv.y);  // exact integer
                                 const int n = nt * kTileN + col0 + c + j;
-                                if (mvalid && n < p.N)
+                                if (mvalid && n < p.N &&
+                                    pq2::store_ok(p.ctl, (static_cast<long long>(m) * p.N + n) * G + g,
+                                                  1, static_cast<long long>(p.M) * p.N * G))
                                     p.dots[(static_cast<size_t>(m) * p.N + n) * G + g] =
                                         static_cast<int>(dot);
                             }
@@ -498,15 +500,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (!DOTS && !failed && mvalid) {
                 const int nb = nt * kTileN + col0;
                 float* yrow = p.y + static_cast<size_t>(m) * p.N + nb;
+                const long long yi = static_cast<long long>(m) * p.N + nb;
                 if (nb + 64 <= p.N && (p.N & 3) == 0) {
 #pragma unroll
                     for (int j = 0; j < 64; j += 4)
-                        *reinterpret_cast<float4*>(yrow + j) =
-                            make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                        if (pq2::store_ok(p.ctl, yi + j, 4, static_cast<long long>(p.M) * p.N))
+                            *reinterpret_cast<float4*>(yrow + j) =
+                                make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 64; ++j)
-                        if (nb + j < p.N) yrow[j] = acc[j];
+                        if (nb + j < p.N && pq2::store_ok(p.ctl, yi + j, 1, static_cast<long long>(p.M) * p.N))
+                            yrow[j] = acc[j];
                 }
             }
         }
@@ -774,7 +779,9 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
                             for (int j = 0; j < 64; ++j) {
                                 const float dot = fmaf(d[j], 512.0f, -stv.y);  // exact integer
                                 const int n = nt * kWTileN + col0 + c + j;
-                                if (mvalid && n < p.N)
+                                if (mvalid && n < p.N &&
+                                    pq2::store_ok(p.ctl, (static_cast<long long>(m) * p.N + n) * G + g,
+                                                  1, static_cast<long long>(p.M) * p.N * G))
                                     p.dots[(static_cast<size_t>(m) * p.N + n) * G + g] =
                                         static_cast<int>(dot);
                             }
@@ -806,21 +813,25 @@ __global__ void __launch_bounds__(kWThreads, 1) prefill_wide_kernel(const __grid
             if (!DOTS && !failed && mvalid) {
                 const int nb = nt * kWTileN + col0;
                 float* yrow = p.y + static_cast<size_t>(m) * p.N + nb;
+                const long long yi = static_cast<long long>(m) * p.N + nb;
                 if (nb + 128 <= p.N && (p.N & 3) == 0) {
 #pragma unroll
                     for (int j = 0; j < 64; j += 2) {
                         float a0, a1, a2, a3;
                         f2unpack(acc2[j], a0, a1);
                         f2unpack(acc2[j + 1], a2, a3);
-                        *reinterpret_cast<float4*>(yrow + 2 * j) = make_float4(a0, a1, a2, a3);
+                        if (pq2::store_ok(p.ctl, yi + 2 * j, 4, static_cast<long long>(p.M) * p.N))
+                            *reinterpret_cast<float4*>(yrow + 2 * j) = make_float4(a0, a1, a2, a3);
                     }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 64; ++j) {
                         float a0, a1;
                         f2unpack(acc2[j], a0, a1);
-                        if (nb + 2 * j < p.N) yrow[2 * j] = a0;
-                        if (nb + 2 * j + 1 < p.N) yrow[2 * j + 1] = a1;
+                        if (nb + 2 * j < p.N && pq2::store_ok(p.ctl, yi + 2 * j, 1, static_cast<long long>(p.M) * p.N))
+                            yrow[2 * j] = a0;
+                        if (nb + 2 * j + 1 < p.N && pq2::store_ok(p.ctl, yi + 2 * j + 1, 1, static_cast<long long>(p.M) * p.N))
+                            yrow[2 * j + 1] = a1;
                     }
                 }
             }

@@ -558,7 +558,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
                         if (DOTS) {
                             const int m = 4 * wq + j;
                             const float dot = fmaf(d, 512.0f, -tv[j]);  // exact integer
-                            if (m < p.M && row < p.N && g < G)
+                            if (m < p.M && row < p.N && g < G &&
+                                pq2::store_ok(p.ctl, (static_cast<long long>(m) * p.N + row) * G + g, 1,
+                                              static_cast<long long>(p.M) * p.N * G))
                                 p.dots[(static_cast<size_t>(m) * p.N + row) * G + g] =
                                     static_cast<int>(dot);
                         } else {
@@ -591,7 +593,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
 #pragma unroll
                         for (int j = 0; j < kTokPerWarp; ++j) {
                             const int m = 4 * wq + j;
-                            if (m < p.M) p.y[static_cast<size_t>(m) * p.N + row] = acc[j];
+                            if (m < p.M &&
+                                pq2::store_ok(p.ctl, static_cast<long long>(m) * p.N + row, 1, static_cast<long long>(p.M) * p.N))
+                                p.y[static_cast<size_t>(m) * p.N + row] = acc[j];
                         }
                     }
                 } else {
@@ -599,7 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
 #pragma unroll
                     for (int j = 0; j < kTokPerWarp; ++j) {
                         const int m = 4 * wq + j;
-                        if (m < p.M) part[static_cast<size_t>(m) * kRows + r] = acc[j];
+                        if (m < p.M &&
+                            pq2::store_ok(p.ctl, static_cast<long long>(blockIdx.x + t) * p.M * kRows +
+                                                     static_cast<long long>(m) * kRows + r,
+                                          1, static_cast<long long>(p.grid + p.n_tiles) * p.M * kRows))
+                            part[static_cast<size_t>(m) * kRows + r] = acc[j];
                     }
                     pq2::named_bar_sync(2, kWorkerThreads);
                     if (lead && lane == 0) {
@@ -640,7 +648,9 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
 #pragma unroll
                             for (int j = 0; j < kTokPerWarp; ++j) {
                                 const int m = 4 * wq + j;
-                                if (m < p.M) p.y[static_cast<size_t>(m) * p.N + row] = sum[j];
+                                if (m < p.M &&
+                                    pq2::store_ok(p.ctl, static_cast<long long>(m) * p.N + row, 1, static_cast<long long>(p.M) * p.N))
+                                    p.y[static_cast<size_t>(m) * p.N + row] = sum[j];
                             }
                         }
                     }

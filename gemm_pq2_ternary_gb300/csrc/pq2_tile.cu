@@ -636,7 +636,9 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1) tile_kernel(const __grid_
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const int m = 16 * tb + 4 * v + j;
-                            if (m < p.M && row < p.N && g < G)
+                            if (m < p.M && row < p.N && g < G &&
+                                pq2::store_ok(p.ctl, (static_cast<long long>(m) * p.N + row) * G + g, 1,
+                                              static_cast<long long>(p.M) * p.N * G))
                                 p.dots[(static_cast<size_t>(m) * p.N + row) * G + g] =
                                     static_cast<int>(ev[j]);
                         }
@@ -687,7 +689,9 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1) tile_kernel(const __grid_
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int m = 16 * tb + i;
-                        if (m < p.M) p.y[static_cast<size_t>(m) * p.N + row] = a[i];
+                        if (m < p.M &&
+                            pq2::store_ok(p.ctl, static_cast<long long>(m) * p.N + row, 1, static_cast<long long>(p.M) * p.N))
+                            p.y[static_cast<size_t>(m) * p.N + row] = a[i];
                     }
                 }
             } else {
@@ -695,7 +699,11 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1) tile_kernel(const __grid_
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int m = 16 * tb + i;
-                    if (m < p.M) part[static_cast<size_t>(m) * kRows + r] = a[i];
+                    if (m < p.M &&
+                        pq2::store_ok(p.ctl, static_cast<long long>(blockIdx.x + t) * p.M * kRows +
+                                                 static_cast<long long>(m) * kRows + r,
+                                      1, static_cast<long long>(p.grid + p.n_tiles) * p.M * kRows))
+                        part[static_cast<size_t>(m) * kRows + r] = a[i];
                 }
                 pq2::named_bar_sync(2, kFlushThreads);
                 if (e == 0 && lane == 0) {
@@ -730,7 +738,9 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1) tile_kernel(const __grid_
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const int m = 16 * tb + i;
-                            if (m < p.M) p.y[static_cast<size_t>(m) * p.N + row] = sum[i];
+                            if (m < p.M &&
+                                pq2::store_ok(p.ctl, static_cast<long long>(m) * p.N + row, 1, static_cast<long long>(p.M) * p.N))
+                                p.y[static_cast<size_t>(m) * p.N + row] = sum[i];
                         }
                     }
                 }

@@ -646,7 +646,9 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                         for (int i = 0; i < 8; ++i) {
                             const int col = t * kBN + c0 + i;
                             const float dot = fmaf(sum[i], 512.0f, -tv);  // exact integer
-                            if (m < p.M && col < p.N && g < G)
+                            if (m < p.M && col < p.N && g < G &&
+                                pq2::store_ok(p.ctl, (static_cast<long long>(m) * p.N + col) * G + g, 1,
+                                              static_cast<long long>(p.M) * p.N * G))
                                 p.dots[(static_cast<size_t>(m) * p.N + col) * G + g] =
                                     static_cast<int>(dot);
                         }
@@ -691,13 +693,16 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
 #pragma unroll
                     for (int j = 0; j < 2 * kNL; ++j) {
                         const int col = colb + 16 * (j >> 1) + 4 * (j & 1);
+                        const long long yi = static_cast<long long>(m) * p.N + col;
                         if (y_vec && col + 3 < p.N) {
-                            *reinterpret_cast<float4*>(yr + col) =
-                                make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                            if (pq2::store_ok(p.ctl, yi, 4, static_cast<long long>(p.M) * p.N))
+                                *reinterpret_cast<float4*>(yr + col) = make_float4(
+                                    acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
                         } else {
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                if (col + e < p.N) yr[col + e] = acc[4 * j + e];
+                                if (col + e < p.N && pq2::store_ok(p.ctl, yi + e, 1, static_cast<long long>(p.M) * p.N))
+                                    yr[col + e] = acc[4 * j + e];
                         }
                     }
                 }
@@ -706,9 +711,13 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                 if (m < p.M) {
                     float* pr = part + static_cast<size_t>(m) * kBN + (colb - t * kBN);
 #pragma unroll
-                    for (int j = 0; j < 2 * kNL; ++j)
-                        *reinterpret_cast<float4*>(pr + 16 * (j >> 1) + 4 * (j & 1)) =
-                            make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                    for (int j = 0; j < 2 * kNL; ++j) {
+                        float* dst = pr + 16 * (j >> 1) + 4 * (j & 1);
+                        if (pq2::store_ok(p.ctl, dst - p.partial, 4,
+                                          static_cast<long long>(p.grid + p.n_tiles) * p.M * kBN))
+                            *reinterpret_cast<float4*>(dst) = make_float4(
+                                acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                    }
                 }
                 pq2::named_bar_sync(2, kEpiThreads);
                 if (warp == 0 && lane == 0) {  // quadrant 0, column block 0
@@ -751,13 +760,16 @@ __global__ void __launch_bounds__(WCfg<MT>::THREADS, 1) wtile_kernel(const __gri
                         for (int j = 0; j < 4; ++j) {
                             const int jj = 4 * hb + j;
                             const int col = colb + 16 * (jj >> 1) + 4 * (jj & 1);
+                            const long long yi = static_cast<long long>(m) * p.N + col;
                             if (y_vec && col + 3 < p.N) {
-                                *reinterpret_cast<float4*>(yr + col) = sum[j];
+                                if (pq2::store_ok(p.ctl, yi, 4, static_cast<long long>(p.M) * p.N))
+                                    *reinterpret_cast<float4*>(yr + col) = sum[j];
                             } else {
                                 const float e4[4] = {sum[j].x, sum[j].y, sum[j].z, sum[j].w};
 #pragma unroll
                                 for (int e = 0; e < 4; ++e)
-                                    if (col + e < p.N) yr[col + e] = e4[e];
+                                    if (col + e < p.N && pq2::store_ok(p.ctl, yi + e, 1, static_cast<long long>(p.M) * p.N))
+                                        yr[col + e] = e4[e];
                             }
                         }
                     }

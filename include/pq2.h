@@ -65,7 +65,9 @@ typedef enum pq2_status {
     PQ2_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned      */
     PQ2_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed  */
     PQ2_ERR_TIMEOUT = 5,           /* a kernel's bounded wait ran out       */
-    PQ2_ERR_WORKSPACE = 6          /* workspace missing or too small        */
+    PQ2_ERR_WORKSPACE = 6,         /* workspace missing or too small        */
+    PQ2_ERR_BOUNDS = 7             /* bounds-checked build: a kernel skipped
+                                      a store outside its buffer            */
 } pq2_status;
 
 /* Operation selectors for pq2_workspace_bytes and pq2_group_dots. */
@@ -300,7 +302,9 @@ pq2_status pq2_group_dots(int op, const int8_t* qp, const int32_t* T, const uint
 /*
  * pq2_last_device_error -- synchronises `stream`, then reads and clears the
  * current device's error word: PQ2_ERR_TIMEOUT if a kernel's bounded wait ran
- * out, PQ2_ERR_INVALID_ARG if pq2_pack_weights met a non-ternary value,
+ * out, PQ2_ERR_BOUNDS (bounds-checked build only) if a kernel skipped a store
+ * outside its buffer, PQ2_ERR_INVALID_ARG if pq2_pack_weights met a
+ * non-ternary value,
  * PQ2_OK otherwise (PQ2_ERR_CUDA if the synchronisation itself failed).
  */
 pq2_status pq2_last_device_error(void* stream);
@@ -406,6 +410,27 @@ pq2_status pq2_debug_set_wait_limit_ns(uint64_t ns);
  * through pq2_last_device_error.  -1 turns it off (the default).
  */
 pq2_status pq2_debug_skip_stage(int stage);
+
+/*
+ * pq2_bounds_checked -- 1 in the bounds-checked build of the library
+ * (libpq2_debug.so, compiled with PQ2_DEBUG=1), 0 in the normal one.  In the
+ * bounds-checked build every kernel store to y, to the integer-dot output and
+ * to the split-K scratch first checks that it lies inside its buffer; a store
+ * that does not is skipped and pq2_last_device_error reports PQ2_ERR_BOUNDS.
+ * Results are otherwise bit-identical to the normal build's.  It stands in
+ * for a memory checker on GPUs where none can be run.
+ */
+int pq2_bounds_checked(void);
+
+/*
+ * pq2_debug_shrink_bounds -- test hook of the bounds-checked build: from now
+ * on the checks treat the last `elements` elements of every checked buffer as
+ * outside it, so that the stores a call makes there are reported
+ * (PQ2_ERR_BOUNDS) and skipped (no memory outside the buffers is touched).
+ * 0 turns it off (the default); no effect in the normal build.
+ * PQ2_ERR_INVALID_ARG for a negative count.
+ */
+pq2_status pq2_debug_shrink_bounds(int elements);
 
 #ifdef __cplusplus
 }

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_version_and_status_strings(lib):
     from gemm_pq2_ternary_gb300 import binding as b
     assert "sm_103a" in b.pq2_version()
-    for s in range(7):
+    for s in range(8):
         assert b.pq2_status_string(s) not in ("", "unknown status")
     assert b.pq2_status_string(99) == "unknown status"
 
@@ -225,3 +225,16 @@ def test_measurement_hooks_check_their_arguments(lib):
     assert lib.pq2_debug_mma_rate(256, 16, None, None) == b.PQ2_ERR_INVALID_ARG
     assert lib.pq2_debug_gemv_floor(5120, 6144, 2, None) == b.PQ2_ERR_INVALID_ARG
     assert lib.pq2_debug_gemv_floor(5120, 100, 0, None) == b.PQ2_ERR_UNSUPPORTED_SHAPE
+
+
+def test_bounds_checked_build_hooks(lib):
+    # the normal library reports 0; the checked one (PQ2_DEBUG=1) 1 and the
+    # same exports; the shrink hook takes no negative count
+    from gemm_pq2_ternary_gb300 import _build, binding as b
+    assert lib.pq2_bounds_checked() == 0
+    assert lib.pq2_debug_shrink_bounds(-1) == b.PQ2_ERR_INVALID_ARG
+    assert lib.pq2_debug_shrink_bounds(0) == b.PQ2_OK
+    dbg = b.load_library(_build.build(debug=True))
+    assert dbg.pq2_bounds_checked() == 1
+    for name in _declared():
+        assert hasattr(dbg, name), name
