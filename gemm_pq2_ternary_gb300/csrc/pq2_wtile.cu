@@ -22,8 +22,9 @@
 //    parts 16h and l (q = 16h + l) on rows 2m and 2m + 1 (zero for tokens
 //    past the call's), so one A tile holds up to 64 tokens; the rows past
 //    the tile's 2 x 16, 32 or 64 only reach D rows that are never read;
-//  * per group, 4 MMAs of M = 128, N = 128, K = 32 (k-step s = plane s): half
-//    the instructions the 128 x 32 small-batch tile needs per code byte.
+//  * per group, 4 MMAs of M = 128, N = 128, K = 32 (k-step s = plane s): as
+//    many instructions per code byte as the 128 x 32 small-batch tile, for up
+//    to 64 tokens instead of 16.
 //    A group's completion reaches its mbarrier about 1400 cycles after the
 //    commit, MMAs or not, so tensor memory holds 4 D buffers of 128 columns
 //    and shared memory 5-6 expanded-weight slots: groups in flight;
