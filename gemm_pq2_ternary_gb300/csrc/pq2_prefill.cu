@@ -47,6 +47,7 @@
 // default from 8 token tiles on, once its tiles fill every SM.
 // Every mbarrier wait is bounded (device error word on expiry).
 #include "pq2_internal.h"
+#include "pq2_tokens.cuh"
 
 namespace {
 
@@ -82,15 +83,6 @@ struct PrefillParams {
 // ---------------------------------------------------------------------------
 // token planes: q = 16h + l -> e4m3(16h), e4m3(l); (s, t) transposed to [G][M]
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
-    uint32_t lo, hi;
-    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
-        : "=r"(lo) : "f"(v0), "f"(v1));
-    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
-        : "=r"(hi) : "f"(v2), "f"(v3));
-    return lo | (hi << 16);
-}
-
 __global__ void __launch_bounds__(256) token_planes_kernel(const int8_t* __restrict__ qp,
                                                            const float* __restrict__ S,
                                                            const int32_t* __restrict__ T,
@@ -111,15 +103,10 @@ __global__ void __launch_bounds__(256) token_planes_kernel(const int8_t* __restr
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < words;
          i += stride) {
         const uint32_t qw = reinterpret_cast<const uint32_t*>(qp)[i];
-        float h[4], l[4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int q = static_cast<int8_t>((qw >> (8 * b)) & 0xFFu);
-            h[b] = static_cast<float>(16 * (q >> 4));  // 16 * floor(q / 16)
-            l[b] = static_cast<float>(q & 15);         // q - 16 * floor(q / 16)
-        }
-        ahi[i] = e4m3x4(h[0], h[1], h[2], h[3]);
-        alo[i] = e4m3x4(l[0], l[1], l[2], l[3]);
+        uint32_t hw, lw;  // e4m3 of 16 * floor(q / 16) and q - 16 * floor(q / 16)
+        pq2::hi_lo_words(qw, hw, lw);
+        ahi[i] = hw;
+        alo[i] = lw;
     }
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < M * G;
          i += stride) {

@@ -132,15 +132,6 @@ __host__ __device__ __forceinline__ int owner_of(long long i, long long items, i
 // ---------------------------------------------------------------------------
 // per-call preparation: token tiles, (s, t), tile counters
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
-    uint32_t lo, hi;
-    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
-        : "=r"(lo) : "f"(v0), "f"(v1));
-    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
-        : "=r"(hi) : "f"(v2), "f"(v3));
-    return lo | (hi << 16);
-}
-
 // tok [G4][NB][128]: token m's e4m3(16h) and e4m3(l) (q = 16h + l,
 // h = floor(q/16)) in rows hi(m), lo(m) of its group: 8(m/4) + m%4 and 4 rows
 // further (hi and lo side by side in D), or m and MT + m (same D).  Zero for
@@ -170,15 +161,7 @@ __global__ void __launch_bounds__(256) tile_prep_kernel(const int8_t* __restrict
         uint32_t hw = 0, lw = 0;
         if (m < M && g < G) {
             const uint32_t qw = reinterpret_cast<const uint32_t*>(qp + m * K + g * 128)[wq];
-            float h[4], l[4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int q = static_cast<int8_t>((qw >> (8 * b)) & 0xFFu);
-                h[b] = static_cast<float>(16 * (q >> 4));  // 16 * floor(q / 16), exact in e4m3
-                l[b] = static_cast<float>(q & 15);         // q - 16 * floor(q / 16)
-            }
-            hw = e4m3x4(h[0], h[1], h[2], h[3]);
-            lw = e4m3x4(l[0], l[1], l[2], l[3]);
+            pq2::hi_lo_words(qw, hw, lw);  // e4m3 of 16 * floor(q / 16), q mod 16
         }
         uint32_t* tg = tok + g * (C::NB * 32);
         const int rh = C::HL == 2 ? 8 * (m / 4) + (m % 4) : m;
