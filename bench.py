@@ -154,7 +154,7 @@ KERNEL_SOURCES = {
     "small": ["pq2_small.cu", "pq2_tokens.cuh", "pq2_common.cuh"],
     "tile": ["pq2_tile.cu", "pq2_tokens.cuh", "pq2_common.cuh"],
     "wtile": ["pq2_wtile.cu", "pq2_tokens.cuh", "pq2_common.cuh"],
-    "prefill": ["pq2_prefill.cu", "pq2_common.cuh"],
+    "prefill": ["pq2_prefill.cu", "pq2_tokens.cuh", "pq2_common.cuh"],
     "bf16": ["pq2_bf16.cu", "pq2_common.cuh"],
     "multi": ["pq2_multi.cu", "pq2_common.cuh"],
 }
