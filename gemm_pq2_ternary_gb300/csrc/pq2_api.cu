@@ -413,9 +413,12 @@ pq2_status pq2_matmul_ex(const void* x_f16, const uint8_t* codes, const void* ws
         Ctx c;
         s = get_ctx(&c);
         if (s != PQ2_OK) return s;
-        const int tt = M <= 16 ? (pq2h::small_x_supported(M, N, K, c.dev.num_sms) ? 3 : 0)
-                               : pq2h::prefill_token_tile_kernel(M, N, K, c.dev.num_sms);
-        if (tt != 0) {
+        using pq2h::TokenTile;
+        const TokenTile tt =
+            M <= 16 ? (pq2h::small_x_supported(M, N, K, c.dev.num_sms) ? TokenTile::kSmall
+                                                                       : TokenTile::kNone)
+                    : pq2h::prefill_token_tile_kernel(M, N, K, c.dev.num_sms);
+        if (tt != TokenTile::kNone) {
             if (!aligned16(x_f16) || !aligned16(codes) || !aligned16(ws_f16) || !aligned16(y))
                 return PQ2_ERR_MISALIGNED;
             const int op = M <= 16 ? PQ2_OP_SMALL : PQ2_OP_PREFILL;
@@ -423,10 +426,10 @@ pq2_status pq2_matmul_ex(const void* x_f16, const uint8_t* codes, const void* ws
             const __half* xh = static_cast<const __half*>(x_f16);
             const __half* wsh = static_cast<const __half*>(ws_f16);
             const cudaStream_t st = static_cast<cudaStream_t>(stream);
-            if (tt == 3)
+            if (tt == TokenTile::kSmall)
                 return cuda_status(pq2h::launch_small_x(xh, codes, wsh, y, M, N, K, w, st, c.ctl,
                                                         c.dev));
-            if (tt == 2)
+            if (tt == TokenTile::kWide)
                 return cuda_status(pq2h::launch_wtile_x(xh, codes, wsh, y, M, N, K, w, st, c.ctl,
                                                         c.dev));
             return cuda_status(pq2h::launch_tile_x(xh, codes, wsh, y, M, N, K, w, st, c.ctl, c.dev));

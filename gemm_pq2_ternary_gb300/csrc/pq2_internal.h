@@ -143,9 +143,11 @@ cudaError_t launch_small_tc(const int8_t* qp, const float* S, const int32_t* T,
                             int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st,
                             const pq2::DevCtl& ctl, const DeviceInfo& dev);
 
+// The token-tile kernels (their tiles can be quantised straight from x).
+enum class TokenTile { kNone, kSmall, kTile, kWide };
 // The token-tile kernel pq2_gemm_prefill runs for this call (its routing):
-// 1 tile_kernel, 2 wtile_kernel, 0 a 128-token tile kernel.
-int prefill_token_tile_kernel(int64_t M, int64_t N, int64_t K, int num_sms);
+// kTile (tile_kernel), kWide (wtile_kernel) or kNone (a 128-token kernel).
+TokenTile prefill_token_tile_kernel(int64_t M, int64_t N, int64_t K, int num_sms);
 
 // Any M: tcgen05 tensor-core kernel (token planes prepared in the workspace).
 size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K);

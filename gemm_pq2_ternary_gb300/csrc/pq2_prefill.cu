@@ -911,17 +911,17 @@ size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 }
 
 // The token-tile kernel pq2_gemm_prefill would run (the routing of
-// launch_prefill below): 1 tile_kernel, 2 wtile_kernel, 0 a 128-token kernel.
-int prefill_token_tile_kernel(int64_t M, int64_t N, int64_t K, int num_sms) {
-    if (M < 1 || M > kTileMaxM) return 0;
+// launch_prefill below).
+TokenTile prefill_token_tile_kernel(int64_t M, int64_t N, int64_t K, int num_sms) {
+    if (M < 1 || M > kTileMaxM) return TokenTile::kNone;
     const int force = forced_variant(PQ2_OP_PREFILL);
     if (force == PQ2_VARIANT_PREFILL_WTILE ||
         (force == PQ2_VARIANT_DEFAULT && wtile_default(M, N, K, num_sms)))
-        return 2;
+        return TokenTile::kWide;
     if (force == PQ2_VARIANT_PREFILL_TILE ||
         (force == PQ2_VARIANT_DEFAULT && M <= kTileDefaultMaxM))
-        return 1;
-    return 0;
+        return TokenTile::kTile;
+    return TokenTile::kNone;
 }
 
 cudaError_t launch_prefill(const int8_t* qp, const float* S, const int32_t* T, const uint8_t* codes,
