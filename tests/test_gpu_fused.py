@@ -286,3 +286,40 @@ def test_matmul_token_tiles_from_x_match_two_step_path(prob):
     ref, A = oracle.matmul_entries(oqp, oS, oracle.pack(tern), ws, ms, ns)
     err = np.abs(y1.cpu().numpy()[ms, ns].astype(np.float64) - ref)
     assert np.all(err <= oracle.fp32_tolerance(ref, A, prob.K // 128)), f"max err {err.max()}"
+
+
+# Forced kernels on pq2_matmul's path: a forced token-tile kernel also takes
+# its tiles straight from x (a forced 128-token or DP4A kernel keeps the
+# two-step path); y is bit-identical to quantise + the forced entry point.
+FORCED_FROM_X = [
+    ("small", "SMALL_TC", inputs.Problem("fx_tc_m3", 3, 384, 77, "p343", "outliers", 170)),
+    ("small", "SMALL_DP4A", inputs.Problem("fx_dp4a_m3", 3, 384, 77, "p343", "outliers", 171)),
+    ("prefill", "PREFILL_TILE", inputs.Problem("fx_tile_m40", 40, 640, 261, "p343", "outliers", 172)),
+    ("prefill", "PREFILL_WTILE", inputs.Problem("fx_wtile_m20", 20, 640, 261, "uniform", "outliers", 173)),
+    ("prefill", "PREFILL_128", inputs.Problem("fx_pf128_m20", 20, 640, 261, "uniform", "normal", 174)),
+]
+
+
+@pytest.mark.parametrize("op,variant,prob", FORCED_FROM_X, ids=lambda v: getattr(v, "name", str(v)))
+def test_forced_kernels_from_x_match_two_step_path(op, variant, prob):
+    from gemm_pq2_ternary_gb300 import binding as pq2
+    from gemm_pq2_ternary_gb300.binding import alloc_workspace, PQ2_OP_MATMUL
+    tern, ws, x = inputs.generate(prob)
+    codes, ws_d = pq2.pack(torch.from_numpy(tern).cuda(), torch.from_numpy(ws).cuda())
+    xd = torch.from_numpy(x).cuda()
+    opc = pq2.PQ2_OP_SMALL if op == "small" else pq2.PQ2_OP_PREFILL
+    fn = pq2.pq2_gemm_small if op == "small" else pq2.pq2_gemm_prefill
+    var = getattr(pq2, "PQ2_VARIANT_" + variant)
+    y1 = torch.full((prob.M, prob.N), float("nan"), device="cuda")
+    y2 = torch.full((prob.M, prob.N), float("nan"), device="cuda")
+    with pq2.forced_kernel(opc, var):
+        pq2.pq2_matmul(xd, codes, ws_d, y1, alloc_workspace(PQ2_OP_MATMUL, prob.M, prob.N, prob.K))
+        qp, S, T = pq2.quantize(xd)
+        fn(qp, S, T, codes, ws_d, y2, alloc_workspace(opc, prob.M, prob.N, prob.K))
+    torch.cuda.synchronize()
+    assert pq2.pq2_last_device_error() == pq2.PQ2_OK
+    assert torch.equal(y1, y2)
+    oqp, oS, _ = oracle.quantize_act(x)
+    ref, A = oracle.matmul(oqp, oS, oracle.pack(tern), ws)
+    err = np.abs(y1.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= oracle.fp32_tolerance(ref, A, prob.K // 128)), f"max err {err.max()}"
