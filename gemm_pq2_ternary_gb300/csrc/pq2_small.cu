@@ -501,9 +501,12 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
                 failed = true;
                 *abort_v = 1;
             }
-            // D columns 8wq .. 8wq+7 of each group: hi of the 4 tokens, then lo
+            // D columns 8wq .. 8wq+7 of each group: hi of the 4 tokens, then lo.
+            // A warp whose 4 tokens are all past M loads and adds nothing (its
+            // tensor-memory reads would only slow the MMAs down).
             float dv[kGQ][8];
-            if (!failed) {
+            const bool live = 4 * wq < p.M;  // warp-uniform
+            if (!failed && live) {
                 tc_fence_after();
 #pragma unroll
                 for (int gq = 0; gq < kGQ; ++gq)
@@ -521,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_kernel(const __grid_constan
             if (++eb == kBufs) { eb = 0; epb ^= 1u; }
             const uint32_t es_s = stage0_s + es * kStageBytes;
             const int row = t * kRows + r;
-            if (!failed) {
+            if (!failed && live) {
 #pragma unroll
                 for (int gq = 0; gq < kGQ; ++gq) {
                     // (s, t) of the 4 tokens (dots: (0, t)), weight scale of this row
