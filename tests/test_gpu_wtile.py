@@ -1,6 +1,7 @@
-"""GPU checks of the weights-wide token-tile kernel (wtile_kernel: 256 weight
+"""GPU checks of the weights-wide token-tile kernel (wtile_kernel: 128 weight
 rows per MMA, the tokens' hi and lo parts as the 128-row operand), forced
-through pq2_debug_force_kernel for the small-batch and prefill entry points.
+through pq2_debug_force_kernel for the small-batch and prefill entry points,
+and of pq2_gemm_prefill's default routing of 33-64 tokens to it.
 
 Its integer group dots must equal the oracle's bit for bit and y must meet
 the fp32 tolerance (on every output at small sizes, on sampled outputs at the
@@ -77,7 +78,7 @@ def _tol_check(c, y, ref, A, what):
     assert np.all(err <= tol), f"{c.p.name} {what}: max err {err.max():.3e}"
 
 
-# ragged shapes: N not a multiple of 256, G not a multiple of 4, tokens that
+# ragged shapes: N not a multiple of 128, G not a multiple of 4, tokens that
 # leave part of each 16/32/64-token tile empty
 RAGGED = [
     inputs.Problem("wt_m2", 2, 384, 77, "p343", "outliers", 170),
@@ -117,7 +118,7 @@ def test_wtile_forced_sweep_shapes_sampled(pq2, prob):
 
 @pytest.mark.parametrize("prob", [SWEEP[3], SWEEP[7]], ids=lambda p: p.name)
 def test_wtile_forced_sweep_dots_rows(pq2, prob):
-    # the dots of the first and last 256-row tiles (the last one ragged)
+    # the dots of the first and last 256 rows (two 128-row tiles each; the last ragged)
     c = Case(pq2, prob)
     got = _dots(pq2, c)
     rows = np.r_[0:256, prob.N - 256:prob.N]
